@@ -1,0 +1,389 @@
+"""Benchmark: one relay decode-attention step (system attention + context
+attention + relay fusion, one attention layer) on synthetic Llama-2-7B
+shapes, through the C ABI of librelay.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl relay|reference]
+                    [--workload llama2_7b] [--Ls L]
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s over the whole job (a
+token = one query row of one request, all heads), measured with CUDA events
+around each step's kernel on device-resident inputs, L2 flushed between
+steps.  `e2e` repeats the measurement through the public API with the
+step's per-request inputs (q, block tables, lengths) copied from pinned host
+memory and the output copied back inside the timed region; the KV caches are
+persistent device state, as in a serving system.  `--impl reference` times
+the fp64 CPU oracle on the host cores instead.
+
+Under torchrun (N > 1) every rank runs an independent batch (weak scaling):
+there is no exchange step in the path, so no collective touches the data.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "relay decode-attention step µs, tokens/s & HBM GB/s (% of 8 TB/s), Llama2-7B"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+KERNEL_SOURCES = ["shared_prompt_decode_gb300/csrc/relay.cu", "shared_prompt_decode_gb300/csrc/relay_kernels.cuh"]
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the relay kernel from a committed ncu summary,
+    or None if the kernel changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "relay_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_hash") != kernel_hash():
+        return None
+    entry = rec.get("workloads", {}).get(workload)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_case(args, rank):
+    over = {}
+    if args.Ls is not None:
+        over["Ls"] = args.Ls
+    wl = synth.workload(args.workload, **over)
+    return synth.make_case(wl, seed=args.seed + rank)
+
+
+def algorithmic_bytes(case):
+    kv_tok = 2 * case.H * case.D * 2
+    rows = case.total_q()
+    return case.Ls * kv_tok + int(case.ctx_lens.sum()) * kv_tok + 2 * rows * case.H * case.D * 2
+
+
+def workload_config(case, args):
+    return {"workload": case.wl.name, "B": case.B, "H": case.H, "D": case.D, "Ls": case.Ls,
+            "Lq": case.Lq, "query_rows": case.total_q(), "ctx_tokens": int(case.ctx_lens.sum()),
+            "block_size": 16, "seed": args.seed, "l2": "flushed between steps (256 MB write)",
+            "parallelism": f"replicas x{args.world} (independent batches)"}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+def time_oracle(case, frac_rows: float, min_seconds: float, max_reps: int):
+    import oracle
+    oracle.build()
+    rows = oracle.all_rows(case)
+    stride = max(1, int(round(1.0 / frac_rows)))
+    sample = rows[::stride]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_rows(case, sample)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    tokens = reps * len(sample) / case.H
+    return {"value": tokens / el, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(sample)} of {len(rows)} (request, row, head) outputs per step, {reps} steps, "
+                      f"{el:.1f} s wall; fp64 C with OpenMP"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    case = build_case(args, 0)
+    import oracle
+    oracle.build()
+    rows = oracle.all_rows(case)
+    stride = args.ref_stride
+    sample = rows[::stride]
+    for _ in range(args.warmup):
+        oracle.attention_rows(case, sample[: max(1, len(sample) // 8)])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_rows(case, sample)
+    el = time.perf_counter() - t0
+    tokens = args.steps * len(sample) / case.H
+    value = tokens / el
+    cpu = {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": f"{len(sample)} of {len(rows)} (request, row, head) outputs per step (every {stride}th), "
+                     f"fp64 C with OpenMP"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(case, args), "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU timing
+def run_relay(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    args.world = world
+
+    from shared_prompt_decode_gb300 import build as relay_build
+    if rank == 0 or world == 1:
+        relay_build.build()
+    barrier(world)
+    import shared_prompt_decode_gb300 as relay
+
+    case = build_case(args, rank)
+    g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
+                                              "ctx_lens")}
+    rows = case.total_q()
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    ws = relay.make_workspace(dims, dev)
+    out = torch.empty_like(g["q"])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
+                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims,
+                                     stream=stream)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        w0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        wall = time.perf_counter() - w0
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return ms, wall
+
+    with ClockSampler(local) as clk:
+        ms, wall = timed(step, args.steps, args.warmup)
+    clocks = clk.summary()
+    mean_ms = max_over_ranks(sum(ms) / len(ms), world, dev)
+    value = world * rows / (mean_ms * 1e-3)
+    abytes = algorithmic_bytes(case)
+    peaks = load_peaks()
+    achieved = abytes / (statistics.mean(ms) * 1e-3) / 1e9
+    traffic = recorded_traffic(case.wl.name if args.Ls is None else f"{case.wl.name}_Ls{args.Ls}")
+
+    # non-relay baseline: same requests, system KV re-read per request from the paged pool
+    kp, vp, ids = synth.with_system_in_pool(case)
+    kp, vp, ids = kp.to(dev), vp.to(dev), ids.to(dev)
+    dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks)
+    ws_b = relay.make_workspace(dims_b, dev)
+    out_b = torch.empty_like(out)
+
+    def base_step():
+        relay.relay_baseline_decode(g["q"], kp, vp, ids, case.Ls, g["block_tables"], g["ctx_lens"], out=out_b,
+                                    workspace=ws_b, dims=dims_b, stream=stream)
+    ms_b, _ = timed(base_step, max(5, args.steps // 2), args.warmup)
+    del kp, vp
+
+    # end to end through the public API, host buffers, copies inside the timed region
+    hq = case.q.pin_memory()
+    hbt = case.block_tables.pin_memory()
+    hcl = case.ctx_lens.pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dbt, dcl = torch.empty_like(g["q"]), torch.empty_like(g["block_tables"]), torch.empty_like(g["ctx_lens"])
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dcl.copy_(hcl, non_blocking=True)
+        relay.relay_attention_decode(dq, g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"], dbt, dcl, out=out,
+                                     workspace=ws, dims=dims, stream=stream)
+        hout.copy_(out, non_blocking=True)
+    ms_e, _ = timed(e2e_step, args.steps, args.warmup)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(sum(ms_e) / len(ms_e), world, dev)
+    h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4
+    d2h = hout.numel() * hout.element_size()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=8)
+
+    if rank != 0:
+        return 0
+    base_mean = statistics.mean(ms_b)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
+        "config": workload_config(case, args),
+        "step_us": 1e3 * mean_ms,
+        "step_us_p10_p50_p90": [1e3 * x for x in statistics.quantiles(ms, n=10)[::4]] if len(ms) >= 10 else None,
+        "hbm_gbs": achieved, "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
+        "algorithmic_bytes_per_step": abytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "relay_kernel<128> (one launch per step)",
+                     "peak_source": f"{peaks['source']} copy bandwidth (burst)"},
+        "nonrelay_baseline": {"kernel": "relay_baseline_decode (system KV re-read per request)",
+                              "step_us": 1e3 * base_mean, "tokens_per_s": rows / (base_mean * 1e-3),
+                              "relay_speedup": base_mean / statistics.mean(ms)},
+        "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["relay", "reference"], default="relay")
+    ap.add_argument("--workload", default="llama2_7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--Ls", type=int, default=None, help="override the system-prompt length")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--ref-stride", type=int, default=8, help="reference arm: time every n-th output row")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    args.world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_relay(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * relay.h -- C ABI of librelay.so: RelayAttention decode attention on GB300.
+ *
+ * The operation (RelayAttention for Efficient Large Language Model Serving
+ * with Long System Prompts, arXiv 2402.14808, Abstract; atyun.com article on
+ * RelayAttention, section "RelayAttention"): causal attention for a batch of
+ * requests that all share one system prompt, computed in three steps --
+ *   1. system attention: every query row of the batch against the shared
+ *      system-prompt KV cache, which is read from memory once per batch
+ *      (the per-request matrix-vector products become one matrix-matrix
+ *      product per head);
+ *   2. context attention: every query row against its own request's paged
+ *      context KV cache;
+ *   3. relay fusion: the two partial outputs combined as a convex
+ *      combination weighted by each part's softmax mass (its log-sum-exp).
+ * The result equals causal attention over the concatenation
+ * [system prompt; request context] exactly, up to rounding.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - fp16 arrays are IEEE binary16 (`const void*` here); accumulation is fp32.
+ *  - Every pointer is a DEVICE pointer unless stated otherwise; the caller
+ *    owns every buffer, including the workspace.  The library never
+ *    allocates, frees or synchronises (except relay_device_status, which
+ *    says so).  All work is queued on `stream`; the calls return at once.
+ *  - Layouts are contiguous, row-major:
+ *      q, out             [B, Lq, H, D]            fp16
+ *      sys_k, sys_v       [Ls, H, D]               fp16
+ *      k_cache, v_cache   [num_blocks, H, 16, D]   fp16 (paged pool; one
+ *                                                  head of one block is 16
+ *                                                  contiguous rows of D)
+ *      block_tables       [B, max_blocks_per_seq]  int32 (physical block of
+ *                                                  context token t of request
+ *                                                  b is block_tables[b][t/16],
+ *                                                  row t%16)
+ *      ctx_lens           [B]                      int32 context tokens
+ *      q_lens             [B]                      int32 query rows (nullable:
+ *                                                  every request has Lq)
+ *      lse arrays         [B, Lq, H]               fp32, natural log
+ *      o_sys, o_ctx       [B, Lq, H, D]            fp32
+ *    q, out, sys_k, sys_v, k_cache, v_cache must be 16-byte aligned.
+ *  - Query row i of request b is context position ctx_lens[b]-q_lens[b]+i;
+ *    it sees the whole system prompt and context tokens
+ *    t < max(0, ctx_lens[b] - q_lens[b] + 1 + i).  Rows i >= q_lens[b] of
+ *    the outputs are left untouched.
+ *  - A row with no visible key at all gets out = 0 and lse = -inf.
+ *  - Supported: D in {64, 128}; block size 16; B <= 512; MHA (H query
+ *    heads = H KV heads).  Others return RELAY_ERR_UNSUPPORTED.
+ *  - Errors: argument problems are found on the host before anything is
+ *    queued and returned synchronously.  Launch failures return
+ *    RELAY_ERR_CUDA.  Values that can only be checked on the device (a
+ *    q_lens or ctx_lens entry out of range, a block id outside the pool, a
+ *    sum of q_lens above the bound) set a flag word in the workspace; the
+ *    kernel then skips the bad access (or the whole batch), and
+ *    relay_device_status reports it.  Nothing traps.
+ */
+#ifndef RELAY_H
+#define RELAY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RELAY_OK = 0,
+    RELAY_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, ... */
+    RELAY_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shapes */
+    RELAY_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    RELAY_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    RELAY_ERR_DEVICE_CHECK = 5,  /* relay_device_status: a device-side check failed */
+    RELAY_ERR_TIMEOUT = 6        /* reserved: a bounded device wait gave up */
+} relay_status_t;
+
+/* Device-side check flags (bit mask reported by relay_device_status). */
+#define RELAY_FLAG_BAD_Q_LEN    1u  /* q_lens[b] outside [0, Lq] */
+#define RELAY_FLAG_BAD_CTX_LEN  2u  /* ctx_lens[b] outside [0, 16*max_blocks_per_seq] */
+#define RELAY_FLAG_BAD_BLOCK    4u  /* a block id outside [0, num_blocks) */
+#define RELAY_FLAG_Q_TOTAL      8u  /* sum of q_lens above max_q_total */
+
+/* Opaque CUDA stream (binary-compatible with cudaStream_t); NULL = legacy stream. */
+typedef struct CUstream_st *relay_stream_t;
+
+/* Problem shape.  Value semantics; the library keeps no pointer to it. */
+typedef struct {
+    int32_t B;                  /* requests in the batch (0: nothing to do) */
+    int32_t Lq;                 /* query-row stride of q/out (max q_lens) */
+    int32_t H;                  /* heads */
+    int32_t D;                  /* head dimension: 64 or 128 */
+    int32_t Ls;                 /* system-prompt tokens (0 allowed) */
+    int32_t block_size;         /* paged block size: must be 16 */
+    int32_t num_blocks;         /* blocks in the paged pool */
+    int32_t max_blocks_per_seq; /* row stride of block_tables */
+    int32_t max_q_total;        /* bound on sum(q_lens); 0 means B*Lq */
+    int32_t ctx_split;          /* context keys per work item for 1-row requests;
+                                   0 = automatic; else a multiple of 64 */
+    int32_t sys_range;          /* system keys per work item; 0 = automatic;
+                                   else a multiple of 64 */
+    float scale;                /* softmax scale; <= 0 means 1/sqrt(D) */
+} relay_dims_t;
+
+/* Bytes of workspace any entry point below needs for `dims` (0 if `dims` is
+ * invalid).  The workspace holds fp32 partial results of the work items and
+ * a few counters.  It must be zero-filled once when first allocated (or by
+ * relay_workspace_init); every call leaves its counters at zero again.
+ * Calls that share one workspace must be ordered (same stream, or events). */
+size_t relay_workspace_size(const relay_dims_t *dims);
+
+/* Queue a zero-fill of the workspace's counter header on `stream`. */
+relay_status_t relay_workspace_init(void *ws, size_t ws_bytes, relay_stream_t stream);
+
+/* Step 1, system attention (atyun.com RelayAttention article, section
+ * "RelayAttention": the intermediate output as if only the shared system
+ * prompt were present).  For every valid row: o_sys = softmax(scale q K_sys^T)
+ * V_sys over all Ls system tokens, lse_sys its natural-log normaliser.
+ * Ls == 0 gives o_sys = 0, lse_sys = -inf. */
+relay_status_t relay_sys_attn(const relay_dims_t *dims, const void *q,
+                              const void *sys_k, const void *sys_v, const int32_t *q_lens,
+                              float *o_sys, float *lse_sys,
+                              void *ws, size_t ws_bytes, relay_stream_t stream);
+
+/* Step 2, context attention (same section: the intermediate output as if only
+ * the request-specific context were present), over the causally visible
+ * context tokens read through the block tables (PagedAttention layout). */
+relay_status_t relay_ctx_attn(const relay_dims_t *dims, const void *q,
+                              const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *ctx_lens,
+                              const int32_t *q_lens, float *o_ctx, float *lse_ctx,
+                              void *ws, size_t ws_bytes, relay_stream_t stream);
+
+/* Step 3, relay fusion (same section: the final output is a convex
+ * combination of the two intermediate outputs).  With
+ * a = exp(lse_sys) / (exp(lse_sys) + exp(lse_ctx)):
+ *   out = a * o_sys + (1 - a) * o_ctx   (stored fp16),
+ *   lse_out = log(exp(lse_sys) + exp(lse_ctx))   (lse_out nullable).
+ * Both lse = -inf gives out = 0, lse_out = -inf.  Needs no workspace. */
+relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const float *lse_sys,
+                          const float *o_ctx, const float *lse_ctx, const int32_t *q_lens,
+                          void *out, float *lse_out, relay_stream_t stream);
+
+/* All three steps in ONE launch: a persistent grid works through system
+ * items (one head, a range of system keys, 64 query rows) and context items
+ * (one request, one head, a range of its context); each item leaves an fp32
+ * partial result with its log-sum-exp, and the item that completes a
+ * (request, head) merges all of that pair's partials into `out` (fp16) and
+ * `lse_out` (fp32 natural log, nullable). */
+relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
+                                      const void *sys_k, const void *sys_v,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, const int32_t *ctx_lens,
+                                      const int32_t *q_lens, void *out, float *lse_out,
+                                      void *ws, size_t ws_bytes, relay_stream_t stream);
+
+/* The non-relay formulation, as a paged-attention system with prefix sharing
+ * runs it (atyun.com RelayAttention article, section "RelayAttention": the
+ * system KVs are read from memory once per request).  The system prompt's KV
+ * sits in the same pool as the contexts, in blocks sys_block_ids[0 ..
+ * ceil(Ls/16)-1] (token s in block sys_block_ids[s/16], row s%16), and every
+ * request attends over [those Ls tokens; its own context].  dims->Ls is the
+ * system-prompt length and dims->num_blocks the size of the whole pool. */
+relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q,
+                                     const void *k_pool, const void *v_pool,
+                                     const int32_t *sys_block_ids,
+                                     const int32_t *block_tables, const int32_t *ctx_lens,
+                                     const int32_t *q_lens, void *out, float *lse_out,
+                                     void *ws, size_t ws_bytes, relay_stream_t stream);
+
+/* Read and clear the device-side check flags of a workspace.  SYNCHRONOUS:
+ * waits for `stream`.  *flags_out (host pointer, nullable) receives the
+ * RELAY_FLAG_* mask.  Returns RELAY_ERR_DEVICE_CHECK if any flag was set. */
+relay_status_t relay_device_status(void *ws, uint32_t *flags_out, relay_stream_t stream);
+
+/* Static description of a status code. */
+const char *relay_status_string(relay_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELAY_H */

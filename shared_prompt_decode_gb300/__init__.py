@@ -1,0 +1,259 @@
+"""Relay decode attention on GB300: thin Python binding of librelay.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of librelay.so (built from csrc/ by build.py).  torch supplies device
+memory and the current stream.  There is no CPU or PyTorch fallback: if the
+library is missing, importing the binding's functions raises.
+
+Entry points (same names as the C ABI in include/relay.h):
+    relay_attention_decode(...)   all three steps in one launch
+    relay_sys_attn(...)           step 1: system attention -> fp32 o, lse
+    relay_ctx_attn(...)           step 2: context attention -> fp32 o, lse
+    relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
+    relay_baseline_decode(...)    non-relay paged attention over [system; context]
+    workspace_size(dims), make_workspace(dims), device_status(ws)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librelay.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
+FLAG_BAD_Q_LEN, FLAG_BAD_CTX_LEN, FLAG_BAD_BLOCK, FLAG_Q_TOTAL = 1, 2, 4, 8
+
+
+class RelayError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Lq", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("Ls", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("max_q_total", ctypes.c_int32), ("ctx_split", ctypes.c_int32),
+                ("sys_range", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+    def __repr__(self):
+        return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+_lib = None
+
+_VP = ctypes.c_void_p
+_SIGS = {
+    "relay_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Dims)]),
+    "relay_workspace_init": (ctypes.c_int, [_VP, ctypes.c_size_t, _VP]),
+    "relay_sys_attn": (ctypes.c_int, [ctypes.POINTER(Dims), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                      ctypes.c_size_t, _VP]),
+    "relay_ctx_attn": (ctypes.c_int, [ctypes.POINTER(Dims), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                      _VP, ctypes.c_size_t, _VP]),
+    "relay_fuse": (ctypes.c_int, [ctypes.POINTER(Dims), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "relay_attention_decode": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 11 + [ctypes.c_size_t, _VP]),
+    "relay_baseline_decode": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 10 + [ctypes.c_size_t, _VP]),
+    "relay_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), _VP]),
+    "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def lib():
+    """The loaded librelay.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"librelay.so is not built ({LIB_PATH}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().relay_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise RelayError(code, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_dims(q: torch.Tensor, Ls: int, num_blocks: int, max_blocks: int, scale: Optional[float] = None,
+              max_q_total: int = 0, ctx_split: int = 0, sys_range: int = 0) -> Dims:
+    B, Lq, H, D = q.shape
+    return Dims(B, Lq, H, D, Ls, 16, num_blocks, max_blocks, max_q_total, ctx_split, sys_range,
+                0.0 if scale is None else float(scale))
+
+
+def workspace_size(dims: Dims) -> int:
+    return int(lib().relay_workspace_size(ctypes.byref(dims)))
+
+
+def make_workspace(dims: Dims, device=None) -> torch.Tensor:
+    """Zero-filled workspace of the size `dims` needs (torch owns the memory)."""
+    n = workspace_size(dims)
+    if n == 0:
+        raise ValueError(f"invalid dims {dims}")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(dims, workspace, device):
+    if workspace is None:
+        workspace = make_workspace(dims, device)
+    return workspace
+
+
+def relay_attention_decode(q, sys_k, sys_v, k_cache, v_cache, block_tables, ctx_lens, q_lens=None,
+                           out=None, lse_out=None, workspace=None, scale=None, max_q_total=0,
+                           ctx_split=0, sys_range=0, stream=None, dims=None):
+    """All three steps in one launch.  Returns out [B, Lq, H, D] fp16."""
+    dev = q.device
+    _need(q, "q", torch.float16)
+    for name, t in (("sys_k", sys_k), ("sys_v", sys_v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, torch.float16, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    if q_lens is not None:
+        _need(q_lens, "q_lens", torch.int32, dev)
+    if dims is None:
+        dims = make_dims(q, sys_k.shape[0], k_cache.shape[0], block_tables.shape[1], scale,
+                         max_q_total, ctx_split, sys_range)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, dev)
+    ws = _ws(dims, workspace, dev)
+    rc = lib().relay_attention_decode(ctypes.byref(dims), _ptr(q), _ptr(sys_k), _ptr(sys_v), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
+                                      _ptr(out), _ptr(lse_out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "relay_attention_decode")
+    return out
+
+
+def relay_sys_attn(q, sys_k, sys_v, q_lens=None, o_sys=None, lse_sys=None, workspace=None, scale=None,
+                   max_q_total=0, sys_range=0, stream=None, max_blocks=0):
+    dev = q.device
+    _need(q, "q", torch.float16)
+    _need(sys_k, "sys_k", torch.float16, dev)
+    _need(sys_v, "sys_v", torch.float16, dev)
+    B, Lq, H, D = q.shape
+    dims = make_dims(q, sys_k.shape[0], 0, max_blocks, scale, max_q_total, 0, sys_range)
+    if o_sys is None:
+        o_sys = torch.empty(B, Lq, H, D, dtype=torch.float32, device=dev)
+    if lse_sys is None:
+        lse_sys = torch.empty(B, Lq, H, dtype=torch.float32, device=dev)
+    ws = _ws(dims, workspace, dev)
+    rc = lib().relay_sys_attn(ctypes.byref(dims), _ptr(q), _ptr(sys_k), _ptr(sys_v), _ptr(q_lens), _ptr(o_sys),
+                              _ptr(lse_sys), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "relay_sys_attn")
+    return o_sys, lse_sys
+
+
+def relay_ctx_attn(q, k_cache, v_cache, block_tables, ctx_lens, q_lens=None, o_ctx=None, lse_ctx=None,
+                   workspace=None, scale=None, max_q_total=0, ctx_split=0, stream=None):
+    dev = q.device
+    _need(q, "q", torch.float16)
+    _need(k_cache, "k_cache", torch.float16, dev)
+    _need(v_cache, "v_cache", torch.float16, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    B, Lq, H, D = q.shape
+    dims = make_dims(q, 0, k_cache.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0)
+    if o_ctx is None:
+        o_ctx = torch.empty(B, Lq, H, D, dtype=torch.float32, device=dev)
+    if lse_ctx is None:
+        lse_ctx = torch.empty(B, Lq, H, dtype=torch.float32, device=dev)
+    ws = _ws(dims, workspace, dev)
+    rc = lib().relay_ctx_attn(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              _ptr(ctx_lens), _ptr(q_lens), _ptr(o_ctx), _ptr(lse_ctx), _ptr(ws), ws.numel(),
+                              _stream(stream))
+    _check(rc, "relay_ctx_attn")
+    return o_ctx, lse_ctx
+
+
+def relay_fuse(o_sys, lse_sys, o_ctx, lse_ctx, q_lens=None, out=None, lse_out=None, stream=None):
+    dev = o_sys.device
+    for name, t in (("o_sys", o_sys), ("lse_sys", lse_sys), ("o_ctx", o_ctx), ("lse_ctx", lse_ctx)):
+        _need(t, name, torch.float32, dev)
+    B, Lq, H, D = o_sys.shape
+    dims = Dims(B, Lq, H, D, 0, 16, 0, 0, 0, 0, 0, 0.0)
+    if out is None:
+        out = torch.empty(B, Lq, H, D, dtype=torch.float16, device=dev)
+    rc = lib().relay_fuse(ctypes.byref(dims), _ptr(o_sys), _ptr(lse_sys), _ptr(o_ctx), _ptr(lse_ctx), _ptr(q_lens),
+                          _ptr(out), _ptr(lse_out), _stream(stream))
+    _check(rc, "relay_fuse")
+    return out
+
+
+def relay_baseline_decode(q, k_pool, v_pool, sys_block_ids, Ls, block_tables, ctx_lens, q_lens=None,
+                          out=None, lse_out=None, workspace=None, scale=None, max_q_total=0, ctx_split=0,
+                          stream=None, dims=None):
+    dev = q.device
+    _need(q, "q", torch.float16)
+    _need(k_pool, "k_pool", torch.float16, dev)
+    _need(v_pool, "v_pool", torch.float16, dev)
+    _need(sys_block_ids, "sys_block_ids", torch.int32, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    if dims is None:
+        dims = make_dims(q, Ls, k_pool.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    ws = _ws(dims, workspace, dev)
+    rc = lib().relay_baseline_decode(ctypes.byref(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(sys_block_ids),
+                                     _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens), _ptr(out), _ptr(lse_out),
+                                     _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "relay_baseline_decode")
+    return out
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Read and clear the device-side check flags (synchronises the stream)."""
+    flags = ctypes.c_uint32(0)
+    rc = lib().relay_device_status(_ptr(workspace), ctypes.byref(flags), _stream(stream))
+    if rc not in (OK, ERR_DEVICE_CHECK):
+        raise RelayError(rc, "relay_device_status")
+    return int(flags.value)
+
+
+def algorithmic_bytes(B, H, D, Ls, ctx_lens, q_rows) -> int:
+    """Bytes the relay step must move at minimum: the system KV once, every
+    request's context KV once, q read and out written (fp16)."""
+    kv_token = 2 * H * D * 2
+    return Ls * kv_token + int(sum(int(n) for n in ctx_lens)) * kv_token + 2 * q_rows * H * D * 2

@@ -1,0 +1,375 @@
+// librelay: host side of the C ABI declared in include/relay.h.
+//
+// Host work is argument checking, the workspace layout, the choice of work
+// item sizes, and one launch per call.  No allocation, no synchronisation
+// (relay_device_status excepted), no state beyond a per-device cache of the
+// SM count and the kernels' occupancy.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "relay.h"
+#include "relay_kernels.cuh"
+
+namespace {
+
+using namespace relay;
+
+constexpr int kMaxDevices = 64;
+constexpr int kAutoCtxSplit = 512;
+constexpr int kGridTarget = 2 * 152;   // resident CTAs on a GB300 (2 per SM)
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+    int occ64 = 0, occ128 = 0;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+template <int D>
+cudaError_t prepare_kernel(int *occ)
+{
+    cudaError_t e = cudaFuncSetAttribute(relay_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(Smem<D>));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, relay_kernel<D>, kThreads, sizeof(Smem<D>));
+}
+
+relay_status_t device_info(const DevInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return RELAY_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            prepare_kernel<64>(&d.occ64) != cudaSuccess || prepare_kernel<128>(&d.occ128) != cudaSuccess) {
+            cudaGetLastError();
+            return RELAY_ERR_CUDA;
+        }
+        if (d.occ64 < 1 || d.occ128 < 1) return RELAY_ERR_CUDA;
+        d.ready = true;
+    }
+    *out = &d;
+    return RELAY_OK;
+}
+
+relay_status_t check_dims(const relay_dims_t *d)
+{
+    if (!d) return RELAY_ERR_INVALID_ARG;
+    if (d->B < 0 || d->Lq < 1 || d->H < 1 || d->D < 1 || d->Ls < 0 || d->block_size < 1 ||
+        d->num_blocks < 0 || d->max_blocks_per_seq < 0 || d->max_q_total < 0 || d->ctx_split < 0 ||
+        d->sys_range < 0 || !(d->scale == d->scale))
+        return RELAY_ERR_INVALID_ARG;
+    if (d->ctx_split % kTileK || d->sys_range % kTileK) return RELAY_ERR_INVALID_ARG;
+    if (d->D != 64 && d->D != 128) return RELAY_ERR_UNSUPPORTED;
+    if (d->block_size != kBlock) return RELAY_ERR_UNSUPPORTED;
+    if (d->B > kMaxB) return RELAY_ERR_UNSUPPORTED;
+    // 32-bit item and row counters on the device
+    if ((int64_t)d->B * d->Lq > INT_MAX / 2 || (int64_t)d->B * d->H > INT_MAX / 2 ||
+        (int64_t)d->max_blocks_per_seq * kBlock + d->Ls > INT_MAX / 2)
+        return RELAY_ERR_UNSUPPORTED;
+    return RELAY_OK;
+}
+
+struct Plan {
+    int Mtot = 0;
+    int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
+    int n_parts = 0, ctx_base = 0, n_prefix = 0;
+    size_t off_arrive = 0, off_part_o = 0, off_part_lse = 0, total = 0;
+};
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Work-item sizes and workspace layout for one mode.
+Plan make_plan(const relay_dims_t *d, int mode)
+{
+    Plan pl;
+    pl.Mtot = d->max_q_total > 0 ? d->max_q_total : d->B * d->Lq;
+    const bool sys = mode == MODE_FUSED || mode == MODE_SYS;
+    const bool ctx = mode != MODE_SYS;
+    pl.n_prefix = mode == MODE_BASELINE ? d->Ls : 0;
+    if (sys) {
+        if (d->Ls > 0) {
+            int range = d->sys_range;
+            if (range == 0) {
+                // Enough system items to spread over the GPU, but long enough
+                // ranges that each range's partial results stay small next to
+                // the system keys it streams.
+                int tiles = (pl.Mtot + kTileM - 1) / kTileM;
+                int r_want = (kGridTarget + d->H * tiles - 1) / (d->H * tiles);
+                int r_cap = d->Ls / std::max(256, 16 * pl.Mtot);
+                int r = std::max(1, std::min(r_want, r_cap));
+                range = round_up((d->Ls + r - 1) / r, kTileK);
+            }
+            pl.sys_range = range;
+            pl.R_sys = (d->Ls + range - 1) / range;
+        } else {
+            pl.R_sys = 1;   // one empty range still reports lse = -inf for sys-only output
+            pl.sys_range = kTileK;
+        }
+        if (mode == MODE_FUSED && d->Ls == 0) pl.R_sys = 0;
+    }
+    if (ctx) {
+        pl.ctx_split = d->ctx_split > 0 ? d->ctx_split : kAutoCtxSplit;
+        int max_keys = pl.n_prefix + d->max_blocks_per_seq * kBlock;
+        pl.C_max = std::max(1, (max_keys + pl.ctx_split - 1) / pl.ctx_split);
+    }
+    pl.ctx_base = sys ? pl.R_sys : 0;
+    pl.n_parts = (sys ? pl.R_sys : 0) + (ctx ? pl.C_max : 0);
+    pl.off_arrive = 256;
+    size_t arrive_bytes = ((size_t)d->B * d->H * sizeof(unsigned) + 255) / 256 * 256;
+    pl.off_part_o = pl.off_arrive + arrive_bytes;
+    size_t rows = (size_t)pl.n_parts * pl.Mtot * d->H;
+    pl.off_part_lse = pl.off_part_o + (rows * d->D * sizeof(float) + 255) / 256 * 256;
+    pl.total = pl.off_part_lse + (rows * sizeof(float) + 255) / 256 * 256;
+    return pl;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+float scale_log2_of(const relay_dims_t *d)
+{
+    float sc = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->D);
+    return sc * 1.4426950408889634f;
+}
+
+relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws, size_t ws_bytes,
+                            relay_stream_t stream)
+{
+    if (!ws) return RELAY_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return RELAY_ERR_INVALID_ARG;
+    Plan pl = make_plan(d, mode);
+    if (ws_bytes < pl.total) return RELAY_ERR_WORKSPACE;
+    const DevInfo *dev = nullptr;
+    relay_status_t st = device_info(&dev);
+    if (st != RELAY_OK) return st;
+
+    unsigned char *base = static_cast<unsigned char *>(ws);
+    p.B = d->B;
+    p.Lq = d->Lq;
+    p.H = d->H;
+    p.Ls = d->Ls;
+    p.num_blocks = d->num_blocks;
+    p.max_blocks = d->max_blocks_per_seq;
+    p.max_q_total = pl.Mtot;
+    p.scale_log2 = scale_log2_of(d);
+    p.n_prefix = pl.n_prefix;
+    p.ctrl = reinterpret_cast<unsigned *>(base);
+    p.arrive = reinterpret_cast<unsigned *>(base + pl.off_arrive);
+    p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
+    p.part_lse = reinterpret_cast<float *>(base + pl.off_part_lse);
+    p.R_sys = pl.R_sys;
+    p.sys_range = pl.sys_range;
+    p.ctx_split = pl.ctx_split;
+    p.ctx_base = pl.ctx_base;
+    p.mode = mode;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d->D == 128) {
+        relay_kernel<128><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
+    } else {
+        relay_kernel<64><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
+    return RELAY_OK;
+}
+
+Params blank_params()
+{
+    Params p{};
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t relay_workspace_size(const relay_dims_t *dims)
+{
+    if (check_dims(dims) != RELAY_OK) return 0;
+    size_t m = 0;
+    for (int mode : {MODE_FUSED, MODE_SYS, MODE_CTX, MODE_BASELINE}) m = std::max(m, make_plan(dims, mode).total);
+    return m;
+}
+
+relay_status_t relay_workspace_init(void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    if (!ws || ws_bytes < 256) return RELAY_ERR_WORKSPACE;
+    if (cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return RELAY_ERR_CUDA;
+    }
+    return RELAY_OK;
+}
+
+relay_status_t relay_sys_attn(const relay_dims_t *dims, const void *q, const void *sys_k, const void *sys_v,
+                              const int32_t *q_lens, float *o_sys, float *lse_sys, void *ws, size_t ws_bytes,
+                              relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!q || !o_sys || !lse_sys || (dims->Ls > 0 && (!sys_k || !sys_v))) return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(sys_k, 16) || !aligned(sys_v, 16) || !aligned(o_sys, 16) ||
+        !aligned(lse_sys, 4) || !aligned(q_lens, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    Params p = blank_params();
+    p.q = static_cast<const __half *>(q);
+    p.sys_k = static_cast<const __half *>(sys_k);
+    p.sys_v = static_cast<const __half *>(sys_v);
+    p.q_lens = q_lens;
+    p.o_f32 = o_sys;
+    p.lse_f32 = lse_sys;
+    return launch_relay(dims, MODE_SYS, p, ws, ws_bytes, stream);
+}
+
+relay_status_t relay_ctx_attn(const relay_dims_t *dims, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                              float *o_ctx, float *lse_ctx, void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!q || !o_ctx || !lse_ctx || !ctx_lens || (dims->max_blocks_per_seq > 0 && !block_tables) ||
+        (dims->num_blocks > 0 && (!k_cache || !v_cache)))
+        return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o_ctx, 16) ||
+        !aligned(lse_ctx, 4) || !aligned(block_tables, 4) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    Params p = blank_params();
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const __half *>(k_cache);
+    p.v_cache = static_cast<const __half *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = ctx_lens;
+    p.q_lens = q_lens;
+    p.o_f32 = o_ctx;
+    p.lse_f32 = lse_ctx;
+    return launch_relay(dims, MODE_CTX, p, ws, ws_bytes, stream);
+}
+
+relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const float *lse_sys, const float *o_ctx,
+                          const float *lse_ctx, const int32_t *q_lens, void *out, float *lse_out,
+                          relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!o_sys || !lse_sys || !o_ctx || !lse_ctx || !out) return RELAY_ERR_INVALID_ARG;
+    if (!aligned(o_sys, 16) || !aligned(o_ctx, 16) || !aligned(out, 16) || !aligned(lse_sys, 4) ||
+        !aligned(lse_ctx, 4) || !aligned(lse_out, 4) || !aligned(q_lens, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    const DevInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != RELAY_OK) return st;
+    size_t n = (size_t)dims->B * dims->Lq * dims->H * (dims->D / 4);
+    size_t blocks = (n + 255) / 256;
+    size_t cap = (size_t)dev->sms * 8;
+    int grid = (int)std::max<size_t>(1, std::min(blocks, cap));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    __half *o = static_cast<__half *>(out);
+    if (dims->D == 128)
+        fuse_kernel<128><<<grid, 256, 0, s>>>(dims->B, dims->Lq, dims->H, o_sys, lse_sys, o_ctx, lse_ctx, q_lens, o,
+                                              lse_out);
+    else
+        fuse_kernel<64><<<grid, 256, 0, s>>>(dims->B, dims->Lq, dims->H, o_sys, lse_sys, o_ctx, lse_ctx, q_lens, o,
+                                             lse_out);
+    if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
+    return RELAY_OK;
+}
+
+relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q, const void *sys_k, const void *sys_v,
+                                      const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *ctx_lens, const int32_t *q_lens, void *out, float *lse_out,
+                                      void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!q || !out || !ctx_lens || (dims->Ls > 0 && (!sys_k || !sys_v)) ||
+        (dims->max_blocks_per_seq > 0 && !block_tables) || (dims->num_blocks > 0 && (!k_cache || !v_cache)))
+        return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(sys_k, 16) || !aligned(sys_v, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(out, 16) || !aligned(lse_out, 4) || !aligned(block_tables, 4) ||
+        !aligned(ctx_lens, 4) || !aligned(q_lens, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    Params p = blank_params();
+    p.q = static_cast<const __half *>(q);
+    p.sys_k = static_cast<const __half *>(sys_k);
+    p.sys_v = static_cast<const __half *>(sys_v);
+    p.k_cache = static_cast<const __half *>(k_cache);
+    p.v_cache = static_cast<const __half *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = ctx_lens;
+    p.q_lens = q_lens;
+    p.out = static_cast<__half *>(out);
+    p.lse_out = lse_out;
+    return launch_relay(dims, MODE_FUSED, p, ws, ws_bytes, stream);
+}
+
+relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q, const void *k_pool, const void *v_pool,
+                                     const int32_t *sys_block_ids, const int32_t *block_tables,
+                                     const int32_t *ctx_lens, const int32_t *q_lens, void *out, float *lse_out,
+                                     void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!q || !out || !ctx_lens || (dims->Ls > 0 && !sys_block_ids) ||
+        (dims->max_blocks_per_seq > 0 && !block_tables) || (dims->num_blocks > 0 && (!k_pool || !v_pool)))
+        return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(lse_out, 4) || !aligned(block_tables, 4) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4) ||
+        !aligned(sys_block_ids, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    Params p = blank_params();
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const __half *>(k_pool);
+    p.v_cache = static_cast<const __half *>(v_pool);
+    p.block_tables = block_tables;
+    p.ctx_lens = ctx_lens;
+    p.q_lens = q_lens;
+    p.prefix_ids = sys_block_ids;
+    p.out = static_cast<__half *>(out);
+    p.lse_out = lse_out;
+    return launch_relay(dims, MODE_BASELINE, p, ws, ws_bytes, stream);
+}
+
+relay_status_t relay_device_status(void *ws, uint32_t *flags_out, relay_stream_t stream)
+{
+    if (!ws) return RELAY_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t flags = 0;
+    if (cudaMemcpyAsync(&flags, ws, sizeof(flags), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(ws, 0, sizeof(flags), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return RELAY_ERR_CUDA;
+    }
+    if (flags_out) *flags_out = flags;
+    return flags ? RELAY_ERR_DEVICE_CHECK : RELAY_OK;
+}
+
+const char *relay_status_string(relay_status_t status)
+{
+    switch (status) {
+    case RELAY_OK: return "ok";
+    case RELAY_ERR_INVALID_ARG: return "invalid argument";
+    case RELAY_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case RELAY_ERR_WORKSPACE: return "workspace missing or too small";
+    case RELAY_ERR_CUDA: return "CUDA runtime error";
+    case RELAY_ERR_DEVICE_CHECK: return "device-side check failed";
+    case RELAY_ERR_TIMEOUT: return "bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+its struct layout matches the binding, and host-side validation rejects bad
+arguments before anything is queued (no CUDA call is reached)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "relay.h")
+
+
+@pytest.fixture(scope="module")
+def relay():
+    from shared_prompt_decode_gb300 import build
+    build.build()
+    import shared_prompt_decode_gb300 as r
+    r.lib()
+    return r
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(relay_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(relay):
+    names = _declared()
+    assert {"relay_attention_decode", "relay_sys_attn", "relay_ctx_attn", "relay_fuse",
+            "relay_baseline_decode", "relay_workspace_size", "relay_status_string"} <= set(names)
+    lib = ctypes.CDLL(relay.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_dims_layout_matches_header(relay, tmp_path):
+    prog = tmp_path / "layout.c"
+    prog.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "relay.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(relay_dims_t),"
+        " offsetof(relay_dims_t, max_q_total), offsetof(relay_dims_t, sys_range),"
+        " offsetof(relay_dims_t, scale));return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    D = relay.Dims
+    assert got == [ctypes.sizeof(D), D.max_q_total.offset, D.sys_range.offset, D.scale.offset]
+
+
+def test_status_strings(relay):
+    for code in range(7):
+        assert relay.status_string(code) and relay.status_string(code) != "unknown status"
+    assert relay.status_string(99) == "unknown status"
+
+
+def _dims(relay, **kw):
+    base = dict(B=32, Lq=1, H=32, D=128, Ls=2048, block_size=16, num_blocks=1200, max_blocks_per_seq=64,
+                max_q_total=0, ctx_split=0, sys_range=0, scale=0.0)
+    base.update(kw)
+    return relay.Dims(**base)
+
+
+def test_workspace_size(relay):
+    lib = relay.lib()
+    n = lib.relay_workspace_size(ctypes.byref(_dims(relay)))
+    assert n > 0 and n % 256 == 0
+    assert lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64))) > n
+    assert lib.relay_workspace_size(None) == 0
+    for bad in (dict(D=96), dict(block_size=32), dict(B=513), dict(H=0), dict(Lq=0), dict(Ls=-1),
+                dict(ctx_split=100), dict(sys_range=-64)):
+        assert lib.relay_workspace_size(ctypes.byref(_dims(relay, **bad))) == 0, bad
+    # a bound on the total query rows shrinks the partial storage
+    big = lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64, Lq=128, H=40, Ls=32768, max_blocks_per_seq=256)))
+    small = lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64, Lq=128, H=40, Ls=32768, max_blocks_per_seq=256,
+                                                        max_q_total=1080)))
+    assert small < big / 4
+
+
+FAKE = 0x7f0000000000      # never dereferenced: validation fails first
+
+
+def _call_decode(relay, dims, ws_bytes=1 << 30, **over):
+    args = dict(q=FAKE, sys_k=FAKE, sys_v=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, ql=None, out=FAKE,
+                lse=None, ws=FAKE)
+    args.update(over)
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    return relay.lib().relay_attention_decode(
+        ctypes.byref(dims) if dims is not None else None, vp(args["q"]), vp(args["sys_k"]), vp(args["sys_v"]),
+        vp(args["k"]), vp(args["v"]), vp(args["bt"]), vp(args["cl"]), vp(args["ql"]), vp(args["out"]),
+        vp(args["lse"]), vp(args["ws"]), ws_bytes, None)
+
+
+def test_host_validation(relay):
+    d = _dims(relay)
+    assert _call_decode(relay, None) == relay.ERR_INVALID_ARG
+    assert _call_decode(relay, _dims(relay, D=96)) == relay.ERR_UNSUPPORTED
+    assert _call_decode(relay, _dims(relay, block_size=8)) == relay.ERR_UNSUPPORTED
+    assert _call_decode(relay, _dims(relay, B=1024)) == relay.ERR_UNSUPPORTED
+    assert _call_decode(relay, d, q=None) == relay.ERR_INVALID_ARG
+    assert _call_decode(relay, d, out=None) == relay.ERR_INVALID_ARG
+    assert _call_decode(relay, d, cl=None) == relay.ERR_INVALID_ARG
+    assert _call_decode(relay, d, sys_k=None) == relay.ERR_INVALID_ARG
+    assert _call_decode(relay, d, q=FAKE + 2) == relay.ERR_INVALID_ARG      # not 16-byte aligned
+    assert _call_decode(relay, d, lse=FAKE + 2) == relay.ERR_INVALID_ARG    # not 4-byte aligned
+    assert _call_decode(relay, d, ws=None) == relay.ERR_WORKSPACE
+    assert _call_decode(relay, d, ws_bytes=1024) == relay.ERR_WORKSPACE
+    assert _call_decode(relay, d, ws=FAKE + 16) == relay.ERR_INVALID_ARG    # workspace not 256-aligned
+    # Ls == 0: the system cache may be absent; B == 0: nothing to do, nothing queued
+    assert _call_decode(relay, _dims(relay, B=0)) == relay.OK
+    lib = relay.lib()
+    assert lib.relay_fuse(ctypes.byref(d), None, None, None, None, None, None, None, None) == relay.ERR_INVALID_ARG
+    assert lib.relay_sys_attn(ctypes.byref(_dims(relay, D=80)), *([ctypes.c_void_p(FAKE)] * 7), 1 << 30,
+                              None) == relay.ERR_UNSUPPORTED
+    assert lib.relay_device_status(None, None, None) == relay.ERR_WORKSPACE
+
+
+def test_binding_refuses_cpu_tensors(relay):
+    import torch
+    q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        relay.relay_attention_decode(q, q, q, q, q, torch.zeros(1, 1, dtype=torch.int32),
+                                     torch.zeros(1, dtype=torch.int32))

@@ -1,0 +1,314 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Tolerance (fp16 I/O, fp32 accumulation): max-abs 2e-3 and normwise relative
+1e-2 on outputs, 1e-3 absolute on the natural-log LSE.  Page-table indexing
+is checked bit for bit (one-hot keys, pool relabelling).  Unused pool slots
+and padding query rows are NaN, so an unmasked read fails the comparison.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import relay_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from shared_prompt_decode_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def wl(name, **kw):
+    return synth.workload(name, **kw)
+
+
+# ----------------------------------------------------------------------------- the five workloads
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_fused(seed):
+    case = synth.make_case("tiny", seed)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+
+
+def test_tiny_three_steps():
+    case = synth.make_case("tiny", 4)
+    o_s, l_s, o_c, l_c, out, lse = T.run_split(case)
+    ref_s, refl_s = oracle.attention_full(case, "sys")
+    ref_c, refl_c = oracle.attention_full(case, "ctx")
+    m = T.valid_mask(case)
+    T.check(o_s, ref_s, "o_sys", m)
+    T.check(l_s, refl_s, "lse_sys", m)
+    T.check(o_c, ref_c, "o_ctx", m)
+    T.check(l_c, refl_c, "lse_ctx", m)
+    T.check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_llama2_7b_full(seed):
+    case = synth.make_case("llama2_7b", seed)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+
+
+def test_llama2_7b_three_steps():
+    case = synth.make_case("llama2_7b", 2)
+    o_s, l_s, o_c, l_c, out, lse = T.run_split(case)
+    m = T.valid_mask(case)
+    ref_s, refl_s = oracle.attention_full(case, "sys")
+    T.check(o_s, ref_s, "o_sys", m)
+    T.check(l_s, refl_s, "lse_sys", m)
+    ref_c, refl_c = oracle.attention_full(case, "ctx")
+    T.check(o_c, ref_c, "o_ctx", m)
+    T.check(l_c, refl_c, "lse_ctx", m)
+    T.check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("Ls", synth.SWEEP_LS)
+def test_llama30b_sweep(Ls):
+    case = synth.make_case(wl("llama30b_sweep", Ls=Ls), 0)
+    out, lse = T.run_fused(case)
+    if Ls <= 4096:
+        T.check_full(case, out, lse)
+    else:
+        T.check_rows(case, out, lse, synth.sample_rows(case, 400, seed=Ls))
+
+
+def test_llama2_7b_b256():
+    case = synth.make_case("llama2_7b_b256", 0)
+    out, lse = T.run_fused(case)
+    T.check_rows(case, out, lse, synth.sample_rows(case, 1500, seed=1))
+
+
+def test_llama2_13b_mixed():
+    case = synth.make_case("llama2_13b_mixed", 0)
+    out, lse = T.run_fused(case)
+    rows = synth.sample_rows(case, 200, seed=2)
+    # every decode request and both ends of every chunk request, on a few heads
+    rows += [(b, 0, b % case.H) for b in range(56)]
+    rows += [(b, i, (b * 7 + i) % case.H) for b in range(56, 64) for i in (0, 1, 63, 64, 127)]
+    T.check_rows(case, out, lse, rows)
+    # outputs are finite everywhere they are defined, and padding rows untouched
+    ql = case.q_lens_list()
+    o = out.float().cpu()
+    for b in range(case.B):
+        assert torch.isfinite(o[b, :ql[b]]).all()
+        assert torch.isnan(o[b, ql[b]:]).all()
+
+
+# ----------------------------------------------------------------------------- merge paths
+@pytest.mark.parametrize("ctx_split,sys_range", [(64, 64), (128, 192), (64, 0), (0, 64)])
+def test_forced_splits_tiny(ctx_split, sys_range):
+    case = synth.make_case("tiny", 5)
+    out, lse = T.run_fused(case, ctx_split=ctx_split, sys_range=sys_range)
+    T.check_full(case, out, lse)
+    o_s, l_s, o_c, l_c, out2, lse2 = T.run_split(case, ctx_split=ctx_split, sys_range=sys_range)
+    T.check_full(case, out2, lse2)
+
+
+def test_forced_splits_llama2_7b():
+    case = synth.make_case("llama2_7b", 3)
+    out, lse = T.run_fused(case, ctx_split=128, sys_range=256)
+    T.check_full(case, out, lse)
+
+
+# ----------------------------------------------------------------------------- edge cases
+EDGE = [
+    ("empty_ctx_some", dict(), [0, 5, 0, 17], None),
+    ("empty_system", dict(Ls=0), None, None),
+    ("both_empty_some", dict(Ls=0), [0, 0, 4, 0], None),
+    ("ragged_block_edges", dict(), [1, 15, 16, 17], None),
+    ("ragged_tile_edges", dict(), [63, 64, 65, 128], None),
+    ("short_system", dict(Ls=1), [3, 64, 33, 0], None),
+    ("odd_system", dict(Ls=100), [100, 1, 2, 64], None),
+    ("single_request", dict(B=1), [37], None),
+]
+
+
+@pytest.mark.parametrize("name,over,ctx,ql", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_cases(name, over, ctx, ql):
+    case = synth.make_case(wl("tiny", pool_blocks=40, **over), 6, ctx_lens=ctx, q_lens=ql)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+    *_, out2, lse2 = T.run_split(case)
+    T.check_full(case, out2, lse2)
+    outb, lseb = T.run_baseline(case)
+    T.check_full(case, outb, lseb)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_mixed_query_rows(D):
+    w = synth.Workload("mixed", B=5, H=3, D=D, Ls=300, ctx_dist=("uniform", 1, 200), value_scale=0.5, Lq=80)
+    case = synth.make_case(w, 7, ctx_lens=[150, 80, 5, 200, 2], q_lens=[1, 80, 0, 65, 3])
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+    *_, out2, lse2 = T.run_split(case, ctx_split=64)
+    T.check_full(case, out2, lse2)
+    outb, lseb = T.run_baseline(case)
+    T.check_full(case, outb, lseb)
+    # rows past q_lens are untouched
+    assert torch.isnan(out[2].float()).all() and torch.isnan(out[0, 1:].float()).all()
+
+
+def test_max_batch():
+    w = synth.Workload("maxb", B=512, H=2, D=64, Ls=64, ctx_dist=("uniform", 0, 40), value_scale=1.0)
+    case = synth.make_case(w, 8)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+
+
+# ----------------------------------------------------------------------------- non-relay baseline
+@pytest.mark.parametrize("name,rows", [("tiny", None), ("llama2_7b", 600)])
+def test_baseline(name, rows):
+    case = synth.make_case(name, 9)
+    out, lse = T.run_baseline(case)
+    if rows is None:
+        T.check_full(case, out, lse)
+    else:
+        T.check_rows(case, out, lse, synth.sample_rows(case, rows, seed=3))
+
+
+# ----------------------------------------------------------------------------- page-table indexing, bit-exact
+def _one_hot_ctx(case, hot):
+    """Zero every real key; make key hot[(b,h)] of each pair dominate."""
+    kc = case.k_cache.clone()
+    kc = torch.where(torch.isnan(kc), kc, torch.zeros_like(kc))
+    sk = torch.zeros_like(case.sys_k)
+    D = case.D
+    expect = torch.empty(case.B, case.H, D, dtype=torch.float16)
+    for (b, h), t in hot.items():
+        blk, slot = int(case.block_tables[b, t // 16]), t % 16
+        qv = case.q[b, 0, h].double()
+        kc[blk, h, slot] = (8.0 * qv / qv.norm() * math.sqrt(D)).to(torch.float16)
+        expect[b, h] = case.v_cache[blk, h, slot]
+    c = synth.Case(case.wl, case.seed, case.q, sk, case.sys_v, kc, case.v_cache, case.block_tables,
+                   case.ctx_lens, case.q_lens)
+    return c, expect
+
+
+def test_one_hot_every_context_position_tiny():
+    case = synth.make_case("tiny", 10)
+    n = [int(x) for x in case.ctx_lens]
+    for r in range(max(n)):
+        hot = {(b, h): (r + 7 * h) % n[b] for b in range(case.B) for h in range(case.H)}
+        c, expect = _one_hot_ctx(case, hot)
+        out, _ = T.run_fused(c)
+        assert torch.equal(out[:, 0].cpu(), expect), f"position sweep step {r}"
+
+
+def test_one_hot_context_llama2_7b():
+    case = synth.make_case("llama2_7b", 11)
+    g = torch.Generator().manual_seed(0)
+    for r in range(3):
+        hot = {(b, h): int(torch.randint(0, int(case.ctx_lens[b]), (1,), generator=g))
+               for b in range(case.B) for h in range(case.H)}
+        c, expect = _one_hot_ctx(case, hot)
+        out, _ = T.run_fused(c)
+        assert torch.equal(out[:, 0].cpu(), expect)
+        outb, _ = T.run_baseline(c)
+        assert torch.equal(outb[:, 0].cpu(), expect)
+
+
+def test_one_hot_system_position():
+    case = synth.make_case("llama2_7b", 12)
+    q = case.q.clone()
+    q[:] = q[0:1]                         # one query per head, shared by every request
+    kc = torch.where(torch.isnan(case.k_cache), case.k_cache, torch.zeros_like(case.k_cache))
+    sk = torch.zeros_like(case.sys_k)
+    expect = torch.empty(case.H, case.D, dtype=torch.float16)
+    for h in range(case.H):
+        s = (h * 61 + 5) % case.Ls
+        qv = q[0, 0, h].double()
+        sk[s, h] = (8.0 * qv / qv.norm() * math.sqrt(case.D)).to(torch.float16)
+        expect[h] = case.sys_v[s, h]
+    c = synth.Case(case.wl, case.seed, q, sk, case.sys_v, kc, case.v_cache, case.block_tables,
+                   case.ctx_lens, case.q_lens)
+    out, _ = T.run_fused(c)
+    assert torch.equal(out[:, 0].cpu(), expect[None].expand(case.B, -1, -1))
+
+
+def test_pool_relabelling_bitwise():
+    case = synth.make_case("llama2_7b", 13)
+    out1, lse1 = T.run_fused(case)
+    out2, lse2 = T.run_fused(synth.relabel_pool(case, 77))
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+# ----------------------------------------------------------------------------- runtime behaviour
+def test_deterministic_and_workspace_reuse():
+    import shared_prompt_decode_gb300 as relay
+    case = synth.make_case("llama2_7b", 14)
+    g = T.to_dev(case)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    ws = relay.make_workspace(dims)
+    outs = [T.run_fused(case, ws=ws, g=g) for _ in range(3)]
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    # the same workspace serves the three-step path in between
+    relay.relay_sys_attn(g["q"], g["sys_k"], g["sys_v"], workspace=ws)
+    o4, l4 = T.run_fused(case, ws=ws, g=g)
+    assert torch.equal(o4, outs[0][0])
+    assert relay.device_status(ws) == 0
+
+
+def test_cuda_graph_replay():
+    import shared_prompt_decode_gb300 as relay
+    case = synth.make_case("llama2_7b", 15)
+    g = T.to_dev(case)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    ws = relay.make_workspace(dims)
+    out = torch.empty_like(g["q"])
+    ref, _ = T.run_fused(case, g=g)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
+                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
+                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("what", ["block", "ctx_len", "q_len", "q_total"])
+def test_device_checks_flag_bad_values(what):
+    import shared_prompt_decode_gb300 as relay
+    case = synth.make_case(wl("tiny", Lq=2), 16, q_lens=[1, 2, 1, 2])
+    g = T.to_dev(case)
+    mq = case.total_q()
+    expect = {"block": relay.FLAG_BAD_BLOCK, "ctx_len": relay.FLAG_BAD_CTX_LEN,
+              "q_len": relay.FLAG_BAD_Q_LEN, "q_total": relay.FLAG_Q_TOTAL}[what]
+    if what == "block":
+        g["block_tables"][1, 0] = case.num_blocks + 3
+    elif what == "ctx_len":
+        g["ctx_lens"][2] = case.max_blocks * 16 + 1
+    elif what == "q_len":
+        g["q_lens"][0] = 3
+    else:
+        mq = 3
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, max_q_total=mq)
+    ws = relay.make_workspace(dims)
+    out = torch.zeros_like(g["q"])
+    relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
+                                 g["block_tables"], g["ctx_lens"], g["q_lens"], out=out, workspace=ws, dims=dims)
+    assert relay.device_status(ws) & expect
+    assert relay.device_status(ws) == 0        # reading clears the flags
+    # the workspace stays usable: a clean call afterwards is correct
+    case2 = synth.make_case(wl("tiny", Lq=2), 17, q_lens=[1, 2, 1, 2])
+    dims2 = relay.make_dims(g["q"], case2.Ls, case2.num_blocks, case2.max_blocks, max_q_total=case2.total_q())
+    ws2 = ws if relay.workspace_size(dims2) <= ws.numel() else relay.make_workspace(dims2)
+    out2, lse2 = T.run_fused(case2, ws=ws2)
+    T.check_full(case2, out2, lse2)
