@@ -366,10 +366,33 @@ def run_relay(args):
     return 0
 
 
+def run_profile(args):
+    """A short, fixed sequence of relay launches for an external profiler."""
+    dev = torch.device("cuda", 0)
+    from shared_prompt_decode_gb300 import build as relay_build
+    relay_build.build()
+    import shared_prompt_decode_gb300 as relay
+    case = build_case(args, 0)
+    g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
+                                              "ctx_lens")}
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    ws = relay.make_workspace(dims, dev)
+    out = torch.empty_like(g["q"])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.profile):
+        flush.zero_()
+        relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
+                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_launches": args.profile, "workload": case.wl.name,
+                      "algorithmic_bytes_per_launch": algorithmic_bytes(case)}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["relay", "reference"], default="relay")
     ap.add_argument("--workload", default="llama2_7b", choices=sorted(synth.WORKLOADS))
@@ -377,11 +400,15 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--ref-stride", type=int, default=8, help="reference arm: time every n-th output row")
+    ap.add_argument("--profile", type=int, default=0, metavar="N",
+                    help="profiling driver: run N relay launches (L2 flushed between) and exit, no timing")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     args.world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     return run_relay(args)
 
 
