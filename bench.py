@@ -256,7 +256,8 @@ def run_relay(args):
     g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
                                               "ctx_lens")}
     rows = case.total_q()
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
+                           sys_range=args.sys_range)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -297,6 +298,12 @@ def run_relay(args):
     peaks = load_peaks()
     achieved = abytes / (statistics.mean(ms) * 1e-3) / 1e9
     traffic = recorded_traffic(case.wl.name if args.Ls is None else f"{case.wl.name}_Ls{args.Ls}")
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "step_us": 1e3 * mean_ms,
+                              "hbm_gbs": achieved, "frac": achieved / peaks["hbm_gbs"], "ctx_split": args.ctx_split,
+                              "sys_range": args.sys_range, "config": workload_config(case, args)}), flush=True)
+        return 0
 
     # non-relay baseline: same requests, system KV re-read per request from the paged pool
     kp, vp, ids = synth.with_system_in_pool(case)
@@ -375,7 +382,8 @@ def run_profile(args):
     case = build_case(args, 0)
     g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
                                               "ctx_lens")}
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
+                           sys_range=args.sys_range)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -399,6 +407,9 @@ def main(argv=None):
     ap.add_argument("--Ls", type=int, default=None, help="override the system-prompt length")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--quick", action="store_true", help="relay timing only: no baseline, e2e or CPU legs")
+    ap.add_argument("--ctx-split", type=int, default=0, help="context keys per decode work item (0: automatic)")
+    ap.add_argument("--sys-range", type=int, default=0, help="system keys per work item (0: automatic)")
     ap.add_argument("--ref-stride", type=int, default=8, help="reference arm: time every n-th output row")
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling driver: run N relay launches (L2 flushed between) and exit, no timing")

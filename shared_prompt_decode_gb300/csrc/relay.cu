@@ -21,7 +21,7 @@ using namespace relay;
 
 constexpr int kMaxDevices = 64;
 constexpr int kAutoCtxSplit = 512;
-constexpr int kGridTarget = 2 * 152;   // resident CTAs on a GB300 (2 per SM)
+constexpr int kGridTarget = 152;       // resident CTAs on a GB300 (one per SM)
 
 struct DevInfo {
     bool ready = false;
@@ -119,9 +119,13 @@ Plan make_plan(const relay_dims_t *d, int mode)
         if (mode == MODE_FUSED && d->Ls == 0) pl.R_sys = 0;
     }
     if (ctx) {
+        // context splits per request: decode rows split pages (prefix pages
+        // + context pages) into ctx_split/16-page items; multi-row requests
+        // use splits of at least ctx_split keys, so the page count bounds both
         pl.ctx_split = d->ctx_split > 0 ? d->ctx_split : kAutoCtxSplit;
-        int max_keys = pl.n_prefix + d->max_blocks_per_seq * kBlock;
-        pl.C_max = std::max(1, (max_keys + pl.ctx_split - 1) / pl.ctx_split);
+        int max_pages = (pl.n_prefix + kBlock - 1) / kBlock + d->max_blocks_per_seq;
+        int pages_per_split = pl.ctx_split / kBlock;
+        pl.C_max = std::max(1, (max_pages + pages_per_split - 1) / pages_per_split);
     }
     pl.ctx_base = sys ? pl.R_sys : 0;
     pl.n_parts = (sys ? pl.R_sys : 0) + (ctx ? pl.C_max : 0);

@@ -7,23 +7,32 @@
 //   MODE_CTX       context items only, merged into fp32 o_ctx / lse_ctx
 //   MODE_BASELINE  context items over [system blocks; context] per request
 //
-// Work items (scheduled dynamically by an atomic counter over a persistent
-// grid, largest items first):
-//   system item  (h, key range rho, row tile tau): 64 query rows of the whole
-//                batch against one range of system keys.  This is the
-//                matrix-matrix product of the system-attention step
-//                (atyun.com RelayAttention article, section "RelayAttention").
-//   multi-row context item (b, h, split, row tile): up to 64 query rows of one
-//                request against a range of its paged context, causal mask.
-//   decode context item (b, h, split): the single query row of a decode
-//                request against a range of its paged context; the four
-//                warps split the keys of each tile.
-// Every item computes with mma.sync m16n8k16 (fp16 in, fp32 accumulate)
-// over K/V tiles of 64 keys staged through a 3-deep cp.async ring in
-// XOR-swizzled shared memory, keeps an online softmax in the log2 domain,
-// and writes one fp32 partial (normalised output + log2-sum-exp).  The item
-// that brings a (request, head) counter to its target merges all partials of
-// that pair -- the relay fusion, generalised to any number of parts.
+// One CTA of 8 warps per SM works through two queues.
+//
+// Phase 1, row items (the whole CTA per item):
+//   system item  (h, key range, 128-row tile): 128 query rows of the whole
+//                batch against one range of system keys -- the matrix-matrix
+//                product of the system-attention step (atyun.com RelayAttention
+//                article, section "RelayAttention").  Each warp owns 16 rows.
+//   multi-row context item (b, h, split, 128-row tile): the rows of one
+//                request that carries several query tokens against a range of
+//                its paged context, with the causal mask.
+//   K/V tiles of 64 keys flow through a deep cp.async ring in XOR-swizzled
+//   shared memory; S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in,
+//   fp32 accumulate) with an online softmax in the log2 domain.
+//
+// Phase 2, decode items (one warp per item, each warp independent):
+//   (b, h, split): the one query row of a decode request against a range of
+//   its paged context (the context-attention step).  A warp streams the
+//   16-token pages of its items through a private cp.async ring, prefetching
+//   the next item's pages while it finishes the current one.  Scores are
+//   computed transposed, S^T = K q (keys on the MMA's M side), and the
+//   output as O^T = V^T P, so a single query row wastes no MMA rows.
+//
+// Every item writes one fp32 partial result (normalised output and its
+// log2-sum-exp).  The item whose arrival completes a (request, head) pair
+// merges all of that pair's partials: the relay fusion, generalised to any
+// number of parts, as a convex combination weighted by softmax mass.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -32,11 +41,11 @@
 namespace relay {
 
 constexpr int kBlock = 16;      // paged block size (tokens)
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTileK = 64;      // keys per pipeline stage
-constexpr int kTileM = 64;      // query rows per row-tile item (16 per warp)
-constexpr int kStages = 3;
+constexpr int kTileK = 64;      // keys per stage in phase 1
+constexpr int kTileM = 16 * kWarps;   // query rows per phase-1 item
+constexpr int kRingBytes = 192 * 1024;
 constexpr int kMaxB = 512;
 
 enum Mode : int { MODE_FUSED = 0, MODE_SYS = 1, MODE_CTX = 2, MODE_BASELINE = 3 };
@@ -44,6 +53,9 @@ enum Mode : int { MODE_FUSED = 0, MODE_SYS = 1, MODE_CTX = 2, MODE_BASELINE = 3 
 enum : unsigned {
     FLAG_BAD_Q_LEN = 1u, FLAG_BAD_CTX_LEN = 2u, FLAG_BAD_BLOCK = 4u, FLAG_Q_TOTAL = 8u
 };
+
+// ctrl words in the workspace
+enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DONE = 2, CTRL_DEC_ITEMS = 3 };
 
 struct Params {
     int B, Lq, H, Ls, num_blocks, max_blocks, max_q_total;
@@ -55,7 +67,7 @@ struct Params {
     __half *out;                      // fused / baseline output
     float *lse_out;                   // nullable
     float *o_f32, *lse_f32;           // sys-only / ctx-only outputs
-    unsigned *ctrl;                   // [0] flags, [1] work counter, [2] finished CTAs
+    unsigned *ctrl;                   // see CTRL_*
     unsigned *arrive;                 // [B*H] arrival counters
     float *part_o;                    // [n_parts][max_q_total][H][D]
     float *part_lse;                  // [n_parts][max_q_total][H]  (log2 domain)
@@ -65,11 +77,12 @@ struct Params {
 
 template <int D>
 struct Smem {
-    __half k[kStages][kTileK * D];
-    __half v[kStages][kTileK * D];
-    float red_o[kWarps][D];
-    float red_m[kWarps];
-    float red_l[kWarps];
+    static constexpr int kStageC = kTileK * D * 2 * 2;        // bytes of one phase-1 stage (K + V)
+    static constexpr int kStagesC = kRingBytes / kStageC < 8 ? kRingBytes / kStageC : 8;   // phase-1 ring depth
+    static constexpr int kStageW = kBlock * D * 2 * 2;        // bytes of one page (K + V)
+    static constexpr int kStagesW =
+        kRingBytes / (kWarps * kStageW) < 6 ? kRingBytes / (kWarps * kStageW) : 6;   // per-warp ring depth
+    alignas(128) unsigned char ring[kRingBytes];
     int qo[kMaxB + 1];        // exclusive prefix of query rows
     int mq[kMaxB + 1];        // exclusive prefix of multi-row context items
     int dec[kMaxB + 1];       // exclusive prefix of decode context items
@@ -77,7 +90,12 @@ struct Smem {
     int item;
     int bad;
     int n_merge;
-    int merge_b[kTileM + kThreads];
+    int merge_b[kTileM];
+
+    __device__ __half *ck(int st) { return reinterpret_cast<__half *>(ring + st * kStageC); }
+    __device__ __half *cv(int st) { return ck(st) + kTileK * D; }
+    __device__ __half *wk(int w, int st) { return reinterpret_cast<__half *>(ring + (w * kStagesW + st) * kStageW); }
+    __device__ __half *wv(int w, int st) { return wk(w, st) + kBlock * D; }
 };
 
 // ----------------------------------------------------------------------------- PTX helpers
@@ -94,6 +112,21 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool vali
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+// wait until at most n groups are pending (n < 8)
+__device__ __forceinline__ void cp_async_wait_dyn(int n)
+{
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+    }
+}
 
 __device__ __forceinline__ void ldsm_x4(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3, const void *p)
 {
@@ -141,6 +174,13 @@ __device__ __forceinline__ unsigned ld_u32(const __half *p)
 
 #define kNegInf (-__int_as_float(0x7f800000))
 
+// swizzled element offset of (row, 16-byte chunk) in a [rows][D] fp16 tile
+template <int D>
+__device__ __forceinline__ int swz(int row, int ch)
+{
+    return row * D + ((ch ^ (row & 7)) << 3);
+}
+
 // Largest b in [0, n) with a[b] <= x (a nondecreasing, a[0] <= x < a[n]).
 __device__ __forceinline__ int find_owner(const int *a, int n, int x)
 {
@@ -153,47 +193,62 @@ __device__ __forceinline__ int find_owner(const int *a, int n, int x)
 }
 
 // ----------------------------------------------------------------------------- schedule
+__device__ __forceinline__ bool has_sys(int mode) { return mode == MODE_FUSED || mode == MODE_SYS; }
+__device__ __forceinline__ bool has_ctx(int mode) { return mode != MODE_SYS; }
+
+// Context work of one request.
+//   decode request (one query row): its key sequence is cut into pages --
+//     ceil(n_prefix/16) prefix pages then ceil(n_ctx/16) context pages -- and
+//     the pages into splits of ctx_split/16 pages (one warp item each);
+//   multi-row request: keys [0, n_prefix + n_ctx) in splits of `split` keys,
+//     rows in tiles of kTileM (one CTA item per split and row tile).
 struct ReqInfo {
-    int ql;       // query rows
-    int nkeys;    // keys of the context sequence (prefix + context)
-    int split;    // keys per context item
-    int ns;       // context items along the keys
-    int mt;       // row tiles (1 for decode rows)
+    int ql, n_ctx;
+    int pp;        // prefix pages (decode)
+    int pages;     // total pages (decode)
+    int tps;       // pages per split (decode)
+    int split;     // keys per split (multi-row)
+    int ns;        // splits
+    int mt;        // row tiles (multi-row), 1 for decode
 };
 
 __device__ __forceinline__ ReqInfo req_info(const Params &p, int b, int ql)
 {
     ReqInfo r;
     r.ql = ql;
-    r.nkeys = p.n_prefix + p.ctx_lens[b];
+    r.n_ctx = p.ctx_lens[b];
+    r.pp = (p.n_prefix + kBlock - 1) / kBlock;
+    r.pages = r.pp + (r.n_ctx + kBlock - 1) / kBlock;
+    r.tps = p.ctx_split / kBlock;
     if (ql <= 1) {
         r.split = p.ctx_split;
+        r.ns = (r.pages + r.tps - 1) / r.tps;
+        r.mt = 1;
     } else {
-        // Longer splits for multi-row requests keep the partial traffic small
-        // next to the keys each item streams.
+        // longer splits for multi-row requests keep the partial traffic small
+        // next to the keys each item streams
         int want = ql * 64;
         r.split = ((want + p.ctx_split - 1) / p.ctx_split) * p.ctx_split;
-        if (r.split < p.ctx_split) r.split = p.ctx_split;
+        int nkeys = p.n_prefix + r.n_ctx;
+        r.ns = (nkeys + r.split - 1) / r.split;
+        r.mt = (ql + kTileM - 1) / kTileM;
     }
-    r.ns = (r.nkeys + r.split - 1) / r.split;
     if (r.ns < 1) r.ns = 1;
-    r.mt = (ql + kTileM - 1) / kTileM;
     return r;
 }
 
-__device__ __forceinline__ bool has_sys(int mode) { return mode == MODE_FUSED || mode == MODE_SYS; }
-__device__ __forceinline__ bool has_ctx(int mode) { return mode != MODE_SYS; }
-
-// Per-CTA prefix sums over the batch (B <= kMaxB, four entries per thread).
+// Per-CTA prefix sums over the batch (B <= kMaxB, two entries per thread).
 template <int D>
 __device__ void build_schedule(const Params &p, Smem<D> &s)
 {
+    constexpr int PER = (kMaxB + kThreads - 1) / kThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int cnt[3][4];
+    int cnt[3][PER];
     int loc[3] = {0, 0, 0};
     unsigned flags = 0;
-    for (int k = 0; k < 4; k++) {
-        int b = tid * 4 + k;
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int b = tid * PER + k;
         int c0 = 0, c1 = 0, c2 = 0;
         if (b < p.B) {
             int ql = p.q_lens ? p.q_lens[b] : p.Lq;
@@ -209,9 +264,10 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
         cnt[0][k] = c0; cnt[1][k] = c1; cnt[2][k] = c2;
         loc[0] += c0; loc[1] += c1; loc[2] += c2;
     }
-    // warp-level inclusive scan of the per-thread totals
     int inc[3] = {loc[0], loc[1], loc[2]};
+#pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
         for (int a = 0; a < 3; a++) {
             int v = __shfl_up_sync(0xffffffffu, inc[a], off);
             if (lane >= off) inc[a] += v;
@@ -229,8 +285,9 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
         base[a] = w + inc[a] - loc[a];
     }
     int *arr[3] = {s.qo, s.mq, s.dec};
-    for (int k = 0; k < 4; k++) {
-        int b = tid * 4 + k;
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int b = tid * PER + k;
         if (b < p.B)
             for (int a = 0; a < 3; a++) {
                 arr[a][b] = base[a];
@@ -244,7 +301,99 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
     __syncthreads();
 }
 
-// ----------------------------------------------------------------------------- key sources
+// ----------------------------------------------------------------------------- merge (relay fusion)
+__device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int h)
+{
+    return ((size_t)part * p.max_q_total + r) * p.H + h;
+}
+
+// Merge every partial of (b, h) into the output: the convex combination of
+// the parts weighted by their softmax mass.  Executed by a team of TEAM
+// threads (a warp or the CTA); thread t of the team handles D/32 adjacent
+// elements of row (t/32) + k*(TEAM/32).
+template <int D, int TEAM>
+__device__ void merge_pair(const Params &p, const int *qo, int b, int h, int t)
+{
+    constexpr int V = D / 32;
+    constexpr float kLn2 = 0.69314718055994531f;
+    const int r0 = qo[b], ql = qo[b + 1] - qo[b];
+    const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
+    const int n_ctx = has_ctx(p.mode) ? req_info(p, b, ql).ns : 0;
+    const int n = n_sys + n_ctx;
+    const int d0 = (t & 31) * V;
+    for (int rr = t >> 5; rr < ql; rr += TEAM / 32) {
+        const int r = r0 + rr;
+        float M = kNegInf;
+        for (int j = 0; j < n; j++) {
+            int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
+            M = fmaxf(M, __ldcg(p.part_lse + part_row(p, part, r, h)));
+        }
+        float W = 0.f, acc[V];
+#pragma unroll
+        for (int v = 0; v < V; v++) acc[v] = 0.f;
+        if (M != kNegInf) {
+            for (int j = 0; j < n; j++) {
+                int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
+                size_t pr = part_row(p, part, r, h);
+                float w = ex2(__ldcg(p.part_lse + pr) - M);
+                W += w;
+                const float *src = p.part_o + pr * D + d0;
+                if constexpr (V == 4) {
+                    float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+                } else {
+                    float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y;
+                }
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        const float lse = W > 0.f ? (M + lg2(W)) * kLn2 : kNegInf;
+        const size_t orow = ((size_t)b * p.Lq + rr) * p.H + h;
+        if (p.mode == MODE_FUSED || p.mode == MODE_BASELINE) {
+            __half *dst = p.out + orow * D + d0;
+            if constexpr (V == 4) {
+                uint2 pk = make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+                *reinterpret_cast<uint2 *>(dst) = pk;
+            } else {
+                *reinterpret_cast<unsigned *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+            }
+            if (p.lse_out && (t & 31) == 0) p.lse_out[orow] = lse;
+        } else {
+            float *dst = p.o_f32 + orow * D + d0;
+#pragma unroll
+            for (int v = 0; v < V; v++) dst[v] = acc[v] * inv;
+            if ((t & 31) == 0) p.lse_f32[orow] = lse;
+        }
+    }
+}
+
+// Count one arrival for (b, h); true for the caller whose increment completed
+// the pair (it then resets the counter for the next call).
+__device__ __forceinline__ bool arrive(const Params &p, int b, int h, int target)
+{
+    unsigned old = atomicAdd(&p.arrive[b * p.H + h], 1u);
+    if ((int)old + 1 == target) {
+        p.arrive[b * p.H + h] = 0;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ int pair_target(const Params &p, const int *qo, int b)
+{
+    const int r0 = qo[b], r1 = qo[b + 1];
+    int t = 0;
+    if (r1 <= r0) return 0;
+    if (has_sys(p.mode)) t += p.R_sys * ((r1 - 1) / kTileM - r0 / kTileM + 1);
+    if (has_ctx(p.mode)) {
+        ReqInfo ri = req_info(p, b, r1 - r0);
+        t += ri.ns * ri.mt;
+    }
+    return t;
+}
+
+// ============================================================================= phase 1: row items
 struct KeySrc {
     const __half *k, *v;
     const int *table;       // this request's block table row (paged) or nullptr (system cache)
@@ -286,6 +435,7 @@ __device__ __forceinline__ void load_tile(Smem<D> &s, int st, const KeySrc &src,
     constexpr int CPR = D / 8;                      // 16-byte chunks per row
     constexpr int PER = kTileK * CPR / kThreads;    // chunks per thread
     const int tid = threadIdx.x;
+    __half *K = s.ck(st), *V = s.cv(st);
 #pragma unroll
     for (int k = 0; k < PER; k++) {
         int c = tid + k * kThreads;
@@ -294,57 +444,52 @@ __device__ __forceinline__ void load_tile(Smem<D> &s, int st, const KeySrc &src,
         size_t off = 0;
         bool valid = t < key_end;
         if (valid) valid = key_offset(src, t, off, flags, D);
-        int dst = key * D + ((ch ^ (key & 7)) << 3);
-        cp_async16(&s.k[st][dst], valid ? src.k + off + ch * 8 : src.k, valid);
-        cp_async16(&s.v[st][dst], valid ? src.v + off + ch * 8 : src.v, valid);
+        int dst = swz<D>(key, ch);
+        cp_async16(K + dst, valid ? src.k + off + ch * 8 : src.k, valid);
+        cp_async16(V + dst, valid ? src.v + off + ch * 8 : src.v, valid);
     }
 }
 
-// ----------------------------------------------------------------------------- warp attention core
-// One warp: 16 query rows (A fragments in qf) against NT*8 keys of the staged
-// tile starting at tile row kb.  Online softmax state per lane: rows g, g+8.
-template <int D, int NT>
-struct WarpState {
+template <int D>
+struct RowState {
     float o[D / 8][4];
     float m[2], l[2];
 };
 
-template <int D, int NT>
-__device__ __forceinline__ void warp_tile(const Smem<D> &s, int st, int kb, const unsigned (&qf)[D / 16][4],
-                                          WarpState<D, NT> &ws, int key_tile0, int end0, int end1,
-                                          float scale_log2)
+// One warp: 16 query rows (A fragments in qf) against the 64 keys of a staged
+// tile.  Lane state: rows g and g+8.
+template <int D>
+__device__ __forceinline__ void row_tile(const __half *K, const __half *V, const unsigned (&qf)[D / 16][4],
+                                         RowState<D> &ws, int key_tile0, int end0, int end1, float scale_log2)
 {
+    constexpr int NT = kTileK / 8;
     const int lane = threadIdx.x & 31;
-    const __half *K = s.k[st];
-    const __half *V = s.v[st];
     float sc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; n++)
 #pragma unroll
         for (int e = 0; e < 4; e++) sc[n][e] = 0.f;
 
-    // S = Q K^T
 #pragma unroll
     for (int kt = 0; kt < D / 16; kt++) {
 #pragma unroll
         for (int np = 0; np < NT / 2; np++) {
-            int row = kb + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            int row = np * 16 + (lane & 7) + ((lane >> 4) << 3);
             int ch = 2 * kt + ((lane >> 3) & 1);
             unsigned b0, b1, b2, b3;
-            ldsm_x4(b0, b1, b2, b3, K + row * D + ((ch ^ (row & 7)) << 3));
+            ldsm_x4(b0, b1, b2, b3, K + swz<D>(row, ch));
             mma16816(sc[2 * np], qf[kt], b0, b1);
             mma16816(sc[2 * np + 1], qf[kt], b2, b3);
         }
     }
 
-    // scale, mask, online softmax (log2 domain)
     const int tig = lane & 3;
     float mx0 = kNegInf, mx1 = kNegInf;
 #pragma unroll
     for (int n = 0; n < NT; n++) {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            int key = key_tile0 + kb + n * 8 + 2 * tig + (e & 1);
+            int key = key_tile0 + n * 8 + 2 * tig + (e & 1);
             int end = (e < 2) ? end0 : end1;
             float v = sc[n][e] * scale_log2;
             sc[n][e] = (key < end) ? v : kNegInf;
@@ -380,7 +525,6 @@ __device__ __forceinline__ void warp_tile(const Smem<D> &s, int st, int kb, cons
         ws.o[d][2] *= al1; ws.o[d][3] *= al1;
     }
 
-    // O += P V
 #pragma unroll
     for (int ks = 0; ks < NT / 2; ks++) {
         unsigned pa[4];
@@ -390,140 +534,89 @@ __device__ __forceinline__ void warp_tile(const Smem<D> &s, int st, int kb, cons
         pa[3] = pack_half2(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < D / 16; dp++) {
-            int row = kb + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            int row = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
             int ch = 2 * dp + (lane >> 4);
             unsigned b0, b1, b2, b3;
-            ldsm_x4_t(b0, b1, b2, b3, V + row * D + ((ch ^ (row & 7)) << 3));
+            ldsm_x4_t(b0, b1, b2, b3, V + swz<D>(row, ch));
             mma16816(ws.o[2 * dp], pa, b0, b1);
             mma16816(ws.o[2 * dp + 1], pa, b2, b3);
         }
     }
 }
 
-template <int D, int NT>
-__device__ __forceinline__ void warp_state_init(WarpState<D, NT> &ws)
+// Key-tile pipeline of a row item over [key0, key_hi): every warp owns 16
+// rows and consumes every tile.  Warps without valid rows only help load.
+template <int D>
+__device__ __forceinline__ void row_pipeline(Smem<D> &s, const KeySrc &src, int key0, int key_hi,
+                                             const unsigned (&qf)[D / 16][4], RowState<D> &ws, int end0,
+                                             int end1, bool active, float scale_log2, unsigned *flags)
 {
-#pragma unroll
-    for (int d = 0; d < D / 8; d++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
-    ws.m[0] = ws.m[1] = kNegInf;
-    ws.l[0] = ws.l[1] = 0.f;
-}
-
-// Run the key-tile pipeline over [key0, key_hi) for this CTA's warps.
-// ROWS: each warp owns 16 rows and all 64 keys of a tile (NT = 8);
-// otherwise the warps share one padded row block and split each tile's keys
-// (NT = 2, warp w takes keys 16w..16w+15).
-template <int D, bool ROWS>
-__device__ __forceinline__ void run_pipeline(Smem<D> &s, const KeySrc &src, int key0, int key_hi,
-                                             const unsigned (&qf)[D / 16][4],
-                                             WarpState<D, ROWS ? 8 : 2> &ws, int end0, int end1,
-                                             float scale_log2, unsigned *flags)
-{
-    constexpr int NT = ROWS ? 8 : 2;
-    const int warp = threadIdx.x >> 5;
-    int n_tiles = (key_hi > key0) ? (key_hi - key0 + kTileK - 1) / kTileK : 0;
-    // prologue was issued by the caller (so that Q loads overlap it)
+    constexpr int S = Smem<D>::kStagesC;
+    const int n_tiles = (key_hi > key0) ? (key_hi - key0 + kTileK - 1) / kTileK : 0;
     for (int j = 0; j < n_tiles; j++) {
-        cp_async_wait<kStages - 2>();
+        cp_async_wait<S - 2>();
         __syncthreads();
-        int jn = j + kStages - 1;
-        if (jn < n_tiles) load_tile<D>(s, jn % kStages, src, key0 + jn * kTileK, key_hi, flags);
+        int jn = j + S - 1;
+        if (jn < n_tiles) load_tile<D>(s, jn % S, src, key0 + jn * kTileK, key_hi, flags);
         cp_async_commit();
-        warp_tile<D, NT>(s, j % kStages, ROWS ? 0 : warp * 16, qf, ws, key0 + j * kTileK, end0, end1, scale_log2);
+        if (active) row_tile<D>(s.ck(j % S), s.cv(j % S), qf, ws, key0 + j * kTileK, end0, end1, scale_log2);
     }
     cp_async_wait<0>();
     __syncthreads();
 }
 
 template <int D>
-__device__ __forceinline__ void issue_prologue(Smem<D> &s, const KeySrc &src, int key0, int key_hi, unsigned *flags)
+__device__ __forceinline__ void row_prologue(Smem<D> &s, const KeySrc &src, int key0, int key_hi, unsigned *flags)
 {
-    int n_tiles = (key_hi > key0) ? (key_hi - key0 + kTileK - 1) / kTileK : 0;
+    constexpr int S = Smem<D>::kStagesC;
+    const int n_tiles = (key_hi > key0) ? (key_hi - key0 + kTileK - 1) / kTileK : 0;
 #pragma unroll
-    for (int j = 0; j < kStages - 1; j++) {
+    for (int j = 0; j < S - 1; j++) {
         if (j < n_tiles) load_tile<D>(s, j, src, key0 + j * kTileK, key_hi, flags);
         cp_async_commit();
     }
 }
 
-// ----------------------------------------------------------------------------- merge (relay fusion)
-__device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int h)
-{
-    return ((size_t)part * p.max_q_total + r) * p.H + h;
-}
-
-// Merge every partial of (b, h) into the output: the convex combination of
-// the parts weighted by their softmax mass.  Called by all threads of the CTA
-// that completed the pair.
 template <int D>
-__device__ void merge_pair(const Params &p, const Smem<D> &s, int b, int h)
+__device__ __forceinline__ void load_q_rows(unsigned (&qf)[D / 16][4], const __half *qa, const __half *qb)
 {
-    const int r0 = s.qo[b], r1 = s.qo[b + 1];
-    const int ql = r1 - r0;
-    const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
-    int n_ctx = 0;
-    if (has_ctx(p.mode)) n_ctx = req_info(p, b, ql).ns;
-    constexpr int RPP = kThreads / D;    // rows per pass (1 for D=128, 2 for D=64)
-    const int d = threadIdx.x % D;
-    for (int rr = threadIdx.x / D; rr < ql; rr += RPP) {
-        int r = r0 + rr;
-        float M = kNegInf;
-        for (int j = 0; j < n_sys + n_ctx; j++) {
-            int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-            M = fmaxf(M, __ldcg(p.part_lse + part_row(p, part, r, h)));
-        }
-        float W = 0.f, acc = 0.f;
-        if (M != kNegInf) {
-            for (int j = 0; j < n_sys + n_ctx; j++) {
-                int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-                size_t pr = part_row(p, part, r, h);
-                float w = ex2(__ldcg(p.part_lse + pr) - M);
-                W += w;
-                acc += w * __ldcg(p.part_o + pr * D + d);
-            }
-        }
-        float o = (W > 0.f) ? acc / W : 0.f;
-        float lse2 = (W > 0.f) ? M + lg2(W) : kNegInf;
-        size_t orow = ((size_t)b * p.Lq + rr) * p.H + h;
-        if (p.mode == MODE_FUSED || p.mode == MODE_BASELINE) {
-            p.out[orow * D + d] = __float2half_rn(o);
-            if (p.lse_out && d == 0) p.lse_out[orow] = lse2 * 0.69314718055994531f;
-        } else {
-            p.o_f32[orow * D + d] = o;
-            if (d == 0) p.lse_f32[orow] = lse2 * 0.69314718055994531f;
-        }
+    const int tig = threadIdx.x & 3;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; kt++) {
+        int c = kt * 16 + 2 * tig;
+        qf[kt][0] = qa ? ld_u32(qa + c) : 0u;
+        qf[kt][1] = qb ? ld_u32(qb + c) : 0u;
+        qf[kt][2] = qa ? ld_u32(qa + c + 8) : 0u;
+        qf[kt][3] = qb ? ld_u32(qb + c + 8) : 0u;
     }
 }
 
-// Count the item's arrival for (b, h); returns true to the one thread whose
-// increment completed the pair.
-__device__ __forceinline__ bool arrive(const Params &p, int b, int h, int target)
-{
-    unsigned old = atomicAdd(&p.arrive[b * p.H + h], 1u);
-    if ((int)old + 1 == target) {
-        p.arrive[b * p.H + h] = 0;   // every arrival is in: reset for the next call
-        return true;
-    }
-    return false;
-}
-
+// Write one warp's partial rows (normalised output, log2-sum-exp).
 template <int D>
-__device__ __forceinline__ int pair_target(const Params &p, const Smem<D> &s, int b)
+__device__ __forceinline__ void write_row_partials(const Params &p, const RowState<D> &ws, int part, int h, int rA,
+                                                   bool vA, int rB, bool vB)
 {
-    const int r0 = s.qo[b], r1 = s.qo[b + 1];
-    int t = 0;
-    if (r1 <= r0) return 0;
-    if (has_sys(p.mode)) t += p.R_sys * ((r1 - 1) / kTileM - r0 / kTileM + 1);
-    if (has_ctx(p.mode)) {
-        ReqInfo ri = req_info(p, b, r1 - r0);
-        t += ri.ns * ri.mt;
+    const int tig = threadIdx.x & 3;
+    float l0 = ws.l[0], l1 = ws.l[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+        if (!(half ? vB : vA)) continue;
+        float l = half ? l1 : l0, m = ws.m[half];
+        float inv = l > 0.f ? 1.f / l : 0.f;
+        size_t pr = part_row(p, part, half ? rB : rA, h);
+        float *po = p.part_o + pr * D;
+#pragma unroll
+        for (int n = 0; n < D / 8; n++)
+            __stcg(reinterpret_cast<float2 *>(po + n * 8 + 2 * tig),
+                   make_float2(ws.o[n][2 * half] * inv, ws.o[n][2 * half + 1] * inv));
+        if (tig == 0) __stcg(p.part_lse + pr, l > 0.f ? m + lg2(l) : kNegInf);
     }
-    return t;
 }
 
-// ----------------------------------------------------------------------------- items
 template <int D>
 __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
 {
@@ -532,16 +625,15 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     const int rho = (item / T) % p.R_sys;
     const int h = item / (T * p.R_sys);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, tig = lane & 3;
+    const int g = lane >> 2;
 
     KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.H, h, 0};
     const int key0 = rho * p.sys_range;
-    int key_hi = key0 + p.sys_range;
-    if (key_hi > p.Ls) key_hi = p.Ls;
-    issue_prologue<D>(s, src, key0, key_hi, p.ctrl);
+    const int key_hi = min(key0 + p.sys_range, p.Ls);
+    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
-    // Q fragments: rows tau*64 + 16*warp + {g, g+8}
-    const int rA = tau * kTileM + warp * 16 + g, rB = rA + 8;
+    const int rW = tau * kTileM + warp * 16;
+    const int rA = rW + g, rB = rA + 8;
     const __half *qa = nullptr, *qb = nullptr;
     if (rA < Mtot) {
         int b = find_owner(s.qo, p.B, rA);
@@ -552,263 +644,412 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
         qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + h) * D;
     }
     unsigned qf[D / 16][4];
+    load_q_rows<D>(qf, qa, qb);
+    RowState<D> ws;
 #pragma unroll
-    for (int kt = 0; kt < D / 16; kt++) {
-        int c = kt * 16 + 2 * tig;
-        qf[kt][0] = qa ? ld_u32(qa + c) : 0u;
-        qf[kt][1] = qb ? ld_u32(qb + c) : 0u;
-        qf[kt][2] = qa ? ld_u32(qa + c + 8) : 0u;
-        qf[kt][3] = qb ? ld_u32(qb + c + 8) : 0u;
-    }
-    WarpState<D, 8> ws;
-    warp_state_init(ws);
-    run_pipeline<D, true>(s, src, key0, key_hi, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
-
-    // partial for rows rA, rB
-    float l0 = ws.l[0], l1 = ws.l[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int part = rho;
+    for (int d = 0; d < D / 8; d++)
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-        int r = half ? rB : rA;
-        if (r >= Mtot) continue;
-        float l = half ? l1 : l0, m = ws.m[half];
-        float inv = l > 0.f ? 1.f / l : 0.f;
-        size_t pr = part_row(p, part, r, h);
-        float *po = p.part_o + pr * D;
-#pragma unroll
-        for (int n = 0; n < D / 8; n++) {
-            float2 v = make_float2(ws.o[n][2 * half] * inv, ws.o[n][2 * half + 1] * inv);
-            __stcg(reinterpret_cast<float2 *>(po + n * 8 + 2 * tig), v);
-        }
-        if (tig == 0) __stcg(p.part_lse + pr, l > 0.f ? m + lg2(l) : kNegInf);
-    }
+        for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
+    ws.m[0] = ws.m[1] = kNegInf;
+    ws.l[0] = ws.l[1] = 0.f;
+    const bool active = rW < Mtot;
+    row_pipeline<D>(s, src, key0, key_hi, qf, ws, key_hi, key_hi, active, p.scale_log2, p.ctrl);
+    if (active) write_row_partials<D>(p, ws, rho, h, rA, rA < Mtot, rB, rB < Mtot);
     __threadfence();
     __syncthreads();
 
-    // arrivals for every request with rows in this tile
+    // arrivals of every request with rows in this tile
     const int r0 = tau * kTileM;
     const int r1 = min(Mtot, r0 + kTileM);
     const int bf = find_owner(s.qo, p.B, r0), bl = find_owner(s.qo, p.B, r1 - 1);
     if (threadIdx.x == 0) s.n_merge = 0;
     __syncthreads();
     for (int b = bf + threadIdx.x; b <= bl; b += kThreads) {
-        if (s.qo[b + 1] > s.qo[b] && arrive(p, b, h, pair_target(p, s, b))) {
+        if (s.qo[b + 1] > s.qo[b] && arrive(p, b, h, pair_target(p, s.qo, b))) {
             int k = atomicAdd(&s.n_merge, 1);
             s.merge_b[k] = b;
         }
     }
     __syncthreads();
-    if (s.n_merge > 0) {
+    const int nm = s.n_merge;
+    if (nm > 0) {
         __threadfence();
-        for (int k = 0; k < s.n_merge; k++) merge_pair<D>(p, s, s.merge_b[k], h);
+        // one warp per completed pair
+        for (int k = warp; k < nm; k += kWarps) merge_pair<D, 32>(p, s.qo, s.merge_b[k], h, lane);
     }
     __syncthreads();
 }
 
-// Context item for a request with several query rows (causal within the context).
+// Context item of a request with several query rows (causal within the context).
 template <int D>
 __device__ void mq_item(const Params &p, Smem<D> &s, int local)
 {
     const int b = find_owner(s.mq, p.B, local);
     const int ql = s.qo[b + 1] - s.qo[b];
-    ReqInfo ri = req_info(p, b, ql);
+    const ReqInfo ri = req_info(p, b, ql);
     int j = local - s.mq[b];
     const int mtile = j % ri.mt;
     j /= ri.mt;
     const int split = j % ri.ns;
     const int h = j / ri.ns;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, tig = lane & 3;
-    const int n_ctx = p.ctx_lens[b];
+    const int g = lane >> 2;
+    const int n_ctx = ri.n_ctx;
 
     KeySrc src{p.k_cache, p.v_cache, p.block_tables + (size_t)b * p.max_blocks, p.prefix_ids, p.n_prefix,
                p.H, h, p.num_blocks};
-    // visible keys of row i: prefix + max(0, n - ql + 1 + i)
-    auto vis = [&](int i) {
+    auto vis = [&](int i) {   // keys row i may see: prefix + max(0, n - ql + 1 + i)
         int v = n_ctx - ql + 1 + i;
         v = v < 0 ? 0 : (v > n_ctx ? n_ctx : v);
         return p.n_prefix + v;
     };
     const int key0 = split * ri.split;
     const int last_row = min(ql, (mtile + 1) * kTileM) - 1;
-    int key_hi = min(key0 + ri.split, vis(last_row));
-    issue_prologue<D>(s, src, key0, key_hi, p.ctrl);
+    const int key_hi = min(key0 + ri.split, vis(last_row));
+    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
-    const int iA = mtile * kTileM + warp * 16 + g, iB = iA + 8;
+    const int iW = mtile * kTileM + warp * 16;
+    const int iA = iW + g, iB = iA + 8;
     const __half *qa = iA < ql ? p.q + (((size_t)b * p.Lq + iA) * p.H + h) * D : nullptr;
     const __half *qb = iB < ql ? p.q + (((size_t)b * p.Lq + iB) * p.H + h) * D : nullptr;
     unsigned qf[D / 16][4];
-#pragma unroll
-    for (int kt = 0; kt < D / 16; kt++) {
-        int c = kt * 16 + 2 * tig;
-        qf[kt][0] = qa ? ld_u32(qa + c) : 0u;
-        qf[kt][1] = qb ? ld_u32(qb + c) : 0u;
-        qf[kt][2] = qa ? ld_u32(qa + c + 8) : 0u;
-        qf[kt][3] = qb ? ld_u32(qb + c + 8) : 0u;
-    }
+    load_q_rows<D>(qf, qa, qb);
     const int endA = iA < ql ? min(key0 + ri.split, vis(iA)) : 0;
     const int endB = iB < ql ? min(key0 + ri.split, vis(iB)) : 0;
-    WarpState<D, 8> ws;
-    warp_state_init(ws);
-    run_pipeline<D, true>(s, src, key0, key_hi, qf, ws, endA, endB, p.scale_log2, p.ctrl);
-
-    float l0 = ws.l[0], l1 = ws.l[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int part = p.ctx_base + split;
+    RowState<D> ws;
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-        int i = half ? iB : iA;
-        if (i >= ql) continue;
-        float l = half ? l1 : l0, m = ws.m[half];
-        float inv = l > 0.f ? 1.f / l : 0.f;
-        size_t pr = part_row(p, part, s.qo[b] + i, h);
-        float *po = p.part_o + pr * D;
+    for (int d = 0; d < D / 8; d++)
 #pragma unroll
-        for (int n = 0; n < D / 8; n++) {
-            float2 v = make_float2(ws.o[n][2 * half] * inv, ws.o[n][2 * half + 1] * inv);
-            __stcg(reinterpret_cast<float2 *>(po + n * 8 + 2 * tig), v);
-        }
-        if (tig == 0) __stcg(p.part_lse + pr, l > 0.f ? m + lg2(l) : kNegInf);
-    }
+        for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
+    ws.m[0] = ws.m[1] = kNegInf;
+    ws.l[0] = ws.l[1] = 0.f;
+    const bool active = iW < ql;
+    row_pipeline<D>(s, src, key0, key_hi, qf, ws, endA, endB, active, p.scale_log2, p.ctrl);
+    if (active) write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, s.qo[b] + iB, iB < ql);
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s, b)) ? 1 : 0;
+    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s.qo, b)) ? 1 : 0;
     __syncthreads();
     if (s.n_merge) {
         __threadfence();
-        merge_pair<D>(p, s, b, h);
+        merge_pair<D, kThreads>(p, s.qo, b, h, threadIdx.x);
     }
     __syncthreads();
 }
 
-// Context item for a decode request (one query row).
+// ============================================================================= phase 2: decode items
+struct DecItem {
+    int id;          // queue index, or -1 when the queue is exhausted
+    int b, h, split;
+    int p0, np;      // first page and page count of the item
+    int pp;          // prefix pages of the request's key sequence
+    int n_ctx;
+};
+
 template <int D>
-__device__ void dec_item(const Params &p, Smem<D> &s, int local)
+__device__ __forceinline__ DecItem dec_item(const Params &p, const Smem<D> &s, int id, int n_dec)
 {
-    const int b = find_owner(s.dec, p.B, local);
-    ReqInfo ri = req_info(p, b, 1);
-    const int j = local - s.dec[b];
-    const int split = j % ri.ns;
-    const int h = j / ri.ns;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    DecItem it;
+    it.id = -1;
+    it.b = it.h = it.split = it.p0 = it.np = it.pp = it.n_ctx = 0;
+    if (id >= n_dec) return it;
+    it.id = id;
+    it.b = find_owner(s.dec, p.B, id);
+    const ReqInfo ri = req_info(p, it.b, 1);
+    const int j = id - s.dec[it.b];
+    it.split = j % ri.ns;
+    it.h = j / ri.ns;
+    it.p0 = it.split * ri.tps;
+    it.np = min(ri.tps, ri.pages - it.p0);
+    if (it.np < 0) it.np = 0;
+    it.pp = ri.pp;
+    it.n_ctx = ri.n_ctx;
+    return it;
+}
+
+// Physical block and valid rows of page `pg` of the item's key sequence.
+__device__ __forceinline__ int page_block(const Params &p, const DecItem &it, int pg, int &rows)
+{
+    int blk;
+    if (pg < it.pp) {
+        blk = p.prefix_ids[pg];
+        rows = min(kBlock, p.n_prefix - pg * kBlock);
+    } else {
+        blk = p.block_tables[(size_t)it.b * p.max_blocks + (pg - it.pp)];
+        rows = min(kBlock, it.n_ctx - (pg - it.pp) * kBlock);
+    }
+    return blk;
+}
+
+__device__ __forceinline__ int page_rows(const Params &p, const DecItem &it, int pg)
+{
+    return pg < it.pp ? min(kBlock, p.n_prefix - pg * kBlock) : min(kBlock, it.n_ctx - (pg - it.pp) * kBlock);
+}
+
+// One lane's share of staging page `pg` (16 rows of K and V) into the warp's
+// ring slot; rows past the page's valid rows, or a bad block, are zero-filled.
+template <int D>
+__device__ __forceinline__ void load_page(const Params &p, __half *K, __half *V, const DecItem &it, int pg,
+                                          int lane)
+{
+    constexpr int CPR = D / 8;
+    constexpr int PER = kBlock * CPR / 32;
+    int rows;
+    int blk = page_block(p, it, pg, rows);
+    bool ok = blk >= 0 && blk < p.num_blocks;
+    if (!ok && lane == 0) atomicOr(&p.ctrl[CTRL_FLAGS], FLAG_BAD_BLOCK);
+    const size_t base = (((size_t)(ok ? blk : 0) * p.H + it.h) * kBlock) * D;
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int c = lane + k * 32;
+        int row = c / CPR, ch = c % CPR;
+        bool valid = ok && row < rows;
+        size_t off = base + (size_t)row * D + ch * 8;
+        int dst = swz<D>(row, ch);
+        cp_async16(K + dst, valid ? p.k_cache + off : p.k_cache, valid);
+        cp_async16(V + dst, valid ? p.v_cache + off : p.v_cache, valid);
+    }
+}
+
+template <int D>
+struct DecState {
+    float o[D / 16][4];   // O^T accumulators: lane (g, tig=0) holds d = 16*mt + g (c0) and +8 (c2)
+    float m;              // running max (log2 domain), uniform across the warp
+    float l;              // lane partial of the normaliser
+};
+
+// One warp, one page: S^T = K q (16 keys on M, the query in column 0 of N),
+// online softmax, O^T += V^T P.
+template <int D>
+__device__ __forceinline__ void dec_page(const __half *K, const __half *V, const unsigned (&qb)[D / 16][2],
+                                         DecState<D> &st, int valid_rows, float scale_log2)
+{
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
-
-    KeySrc src{p.k_cache, p.v_cache, p.block_tables + (size_t)b * p.max_blocks, p.prefix_ids, p.n_prefix,
-               p.H, h, p.num_blocks};
-    const int key0 = split * ri.split;
-    const int key_hi = min(key0 + ri.split, ri.nkeys);
-    issue_prologue<D>(s, src, key0, key_hi, p.ctrl);
-
-    // the one real query row sits in row 0 of the padded 16-row block
-    const __half *qrow = p.q + ((size_t)b * p.Lq * p.H + h) * D;
-    unsigned qf[D / 16][4];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kt = 0; kt < D / 16; kt++) {
-        int c = kt * 16 + 2 * tig;
-        qf[kt][0] = (g == 0) ? ld_u32(qrow + c) : 0u;
-        qf[kt][1] = 0u;
-        qf[kt][2] = (g == 0) ? ld_u32(qrow + c + 8) : 0u;
-        qf[kt][3] = 0u;
+        unsigned a[4];
+        int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+        int ch = 2 * kt + (lane >> 4);
+        ldsm_x4(a[0], a[1], a[2], a[3], K + swz<D>(row, ch));
+        mma16816(acc, a, qb[kt][0], qb[kt][1]);
     }
-    WarpState<D, 2> ws;
-    warp_state_init(ws);
-    run_pipeline<D, false>(s, src, key0, key_hi, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
-
-    // combine the four warps' states of row 0
-    float l0 = ws.l[0];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    if (g == 0) {
+    // column 0 of S^T lives in lanes with tig == 0: key g in acc[0], key g+8 in acc[2]
+    float s0 = (tig == 0 && g < valid_rows) ? acc[0] * scale_log2 : kNegInf;
+    float s1 = (tig == 0 && g + 8 < valid_rows) ? acc[2] * scale_log2 : kNegInf;
+    float mx = fmaxf(s0, s1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mx = __shfl_sync(0xffffffffu, mx, 0);
+    const float mn = fmaxf(st.m, mx);
+    const float mu = (mn == kNegInf) ? 0.f : mn;
+    if (mn != st.m) {     // warp-uniform: rescale only when the running max moves
+        const float al = ex2(st.m - mu);
+        st.l *= al;
 #pragma unroll
-        for (int n = 0; n < D / 8; n++) {
-            s.red_o[warp][n * 8 + 2 * tig] = ws.o[n][0];
-            s.red_o[warp][n * 8 + 2 * tig + 1] = ws.o[n][1];
-        }
-        if (tig == 0) {
-            s.red_m[warp] = ws.m[0];
-            s.red_l[warp] = l0;
-        }
-    }
-    __syncthreads();
-    const int part = p.ctx_base + split;
-    const size_t pr = part_row(p, part, s.qo[b], h);
-    if (threadIdx.x < D) {
-        const int d = threadIdx.x;
-        float M = kNegInf;
+        for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
-        for (int w = 0; w < kWarps; w++) M = fmaxf(M, s.red_m[w]);
-        float L = 0.f, acc = 0.f;
-        if (M != kNegInf) {
+            for (int e = 0; e < 4; e++) st.o[mt][e] *= al;
+        st.m = mn;
+    }
+    const float p0 = ex2(s0 - mu), p1 = ex2(s1 - mu);
+    st.l += p0 + p1;
+    // B operand P[16 keys x 8]: lanes 0..3 (column 0) need keys 2t, 2t+1 (b0)
+    // and 2t+8, 2t+9 (b1); key k's weight sits in lane 4*(k%8), p0 or p1.
+    const unsigned pk = pack_half2(p0, p1);
+    const unsigned x = __shfl_sync(0xffffffffu, pk, (lane & 3) * 8);
+    const unsigned y = __shfl_sync(0xffffffffu, pk, (lane & 3) * 8 + 4);
+    unsigned b0 = __byte_perm(x, y, 0x5410);     // (x.lo, y.lo)
+    unsigned b1 = __byte_perm(x, y, 0x7632);     // (x.hi, y.hi)
+    if (g != 0) b0 = b1 = 0u;
 #pragma unroll
-            for (int w = 0; w < kWarps; w++) {
-                float c = ex2(s.red_m[w] - M);
-                L += c * s.red_l[w];
-                acc += c * s.red_o[w][d];
-            }
-        }
-        __stcg(p.part_o + pr * D + d, L > 0.f ? acc / L : 0.f);
-        if (d == 0) __stcg(p.part_lse + pr, L > 0.f ? M + lg2(L) : kNegInf);
+    for (int mt = 0; mt < D / 16; mt++) {
+        unsigned a[4];
+        int row = (lane & 7) + ((lane >> 4) << 3);
+        int ch = 2 * mt + ((lane >> 3) & 1);
+        ldsm_x4_t(a[0], a[1], a[2], a[3], V + swz<D>(row, ch));
+        mma16816(st.o[mt], a, b0, b1);
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s, b)) ? 1 : 0;
-    __syncthreads();
-    if (s.n_merge) {
-        __threadfence();
-        merge_pair<D>(p, s, b, h);
-    }
-    __syncthreads();
 }
 
-// ----------------------------------------------------------------------------- persistent kernel
+// Finish a decode item: write its partial and count its arrival; the warp that
+// completes the pair merges it.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) relay_kernel(const Params p)
+__device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem &it, DecState<D> &st)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    float L = st.l;
+    L += __shfl_xor_sync(0xffffffffu, L, 4);
+    L += __shfl_xor_sync(0xffffffffu, L, 8);
+    L += __shfl_xor_sync(0xffffffffu, L, 16);
+    L = __shfl_sync(0xffffffffu, L, 0);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const size_t pr = part_row(p, p.ctx_base + it.split, s.qo[it.b], it.h);
+    if (tig == 0) {
+        float *po = p.part_o + pr * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            __stcg(po + 16 * mt + g, st.o[mt][0] * inv);
+            __stcg(po + 16 * mt + g + 8, st.o[mt][2] * inv);
+        }
+    }
+    if (lane == 0) __stcg(p.part_lse + pr, L > 0.f ? st.m + lg2(L) : kNegInf);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = arrive(p, it.b, it.h, pair_target(p, s.qo, it.b)) ? 1 : 0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence();
+        merge_pair<D, 32>(p, s.qo, it.b, it.h, lane);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void dec_load_q(const Params &p, const DecItem &it, unsigned (&qb)[D / 16][2])
+{
+    const int lane = threadIdx.x & 31;
+    const __half *q = p.q + ((size_t)it.b * p.Lq * p.H + it.h) * D;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; kt++) {
+        // B fragment of q in column 0: rows k = 2*tig, 2*tig+1 (b0) and +8 (b1), lanes 0..3
+        int c = kt * 16 + 2 * (lane & 3);
+        qb[kt][0] = lane < 4 ? ld_u32(q + c) : 0u;
+        qb[kt][1] = lane < 4 ? ld_u32(q + c + 8) : 0u;
+    }
+}
+
+// Phase 2 for one warp: pull decode items until the queue is empty, streaming
+// pages through the warp's ring and prefetching across item boundaries.
+template <int D>
+__device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
+{
+    constexpr int S = Smem<D>::kStagesW;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    auto fetch = [&]() {
+        int id = 0;
+        if (lane == 0) id = (int)atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
+        id = __shfl_sync(0xffffffffu, id, 0);
+        return dec_item<D>(p, s, id, n_dec);
+    };
+
+    DecItem cur = fetch();
+    if (cur.id < 0) return;
+    DecItem nxt = dec_item<D>(p, s, n_dec, n_dec);   // empty
+    bool nxt_fetched = false;
+    bool load_on_nxt = false;     // the loader has moved on to `nxt`
+    int load_pg = 0;              // next page (relative) of the item being loaded
+    int issued = 0, computed = 0;
+
+    auto fill = [&]() {
+        while (issued - computed < S - 1) {
+            const DecItem &li = load_on_nxt ? nxt : cur;
+            if (load_pg < li.np) {
+                int st = issued % S;
+                load_page<D>(p, s.wk(warp, st), s.wv(warp, st), li, li.p0 + load_pg, lane);
+                cp_async_commit();
+                load_pg++;
+                issued++;
+            } else if (!load_on_nxt) {
+                if (!nxt_fetched) {
+                    nxt = fetch();
+                    nxt_fetched = true;
+                }
+                if (nxt.id < 0) break;
+                load_on_nxt = true;
+                load_pg = 0;
+            } else {
+                break;
+            }
+        }
+    };
+
+    fill();
+    for (;;) {
+        unsigned qb[D / 16][2];
+        dec_load_q<D>(p, cur, qb);
+        DecState<D> st;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) st.o[mt][e] = 0.f;
+        st.m = kNegInf;
+        st.l = 0.f;
+        for (int j = 0; j < cur.np; j++) {
+            cp_async_wait_dyn(issued - computed - 1);
+            __syncwarp();
+            const int stg = computed % S;
+            dec_page<D>(s.wk(warp, stg), s.wv(warp, stg), qb, st, page_rows(p, cur, cur.p0 + j), p.scale_log2);
+            __syncwarp();
+            computed++;
+            fill();
+        }
+        if (!nxt_fetched) {     // the ring still held pages of this item: fetch the next one now
+            nxt = fetch();
+            nxt_fetched = true;
+        }
+        dec_epilogue<D>(p, s, cur, st);
+        if (nxt.id < 0) break;
+        // nxt becomes current; its pages already issued stay in flight
+        if (!load_on_nxt) load_pg = 0;
+        cur = nxt;
+        nxt_fetched = false;
+        load_on_nxt = false;
+        fill();
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+}
+
+// ============================================================================= persistent kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(smem_raw);
 
     build_schedule<D>(p, s);
     if (s.bad) {
-        if (threadIdx.x == 0) atomicOr(&p.ctrl[0], (unsigned)s.bad);
+        if (threadIdx.x == 0) atomicOr(&p.ctrl[CTRL_FLAGS], (unsigned)s.bad);
         return;    // counters untouched: nothing was scheduled
     }
     const int Mtot = s.qo[p.B];
     const int T = (Mtot + kTileM - 1) / kTileM;
     const int n_sys = has_sys(p.mode) ? p.H * p.R_sys * T : 0;
-    const int n_mq = s.mq[p.B];
+    const int n_rows = n_sys + s.mq[p.B];
     const int n_dec = s.dec[p.B];
-    const int total = n_sys + n_mq + n_dec;
 
+    // phase 1: row items, the whole CTA per item
     for (;;) {
-        if (threadIdx.x == 0) s.item = (int)atomicAdd(&p.ctrl[1], 1u);
+        if (threadIdx.x == 0) s.item = (int)atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u);
         __syncthreads();
         const int item = s.item;
         __syncthreads();
-        if (item >= total) break;
+        if (item >= n_rows) break;
         if (item < n_sys) sys_item<D>(p, s, item, Mtot);
-        else if (item < n_sys + n_mq) mq_item<D>(p, s, item - n_sys);
-        else dec_item<D>(p, s, item - n_sys - n_mq);
+        else mq_item<D>(p, s, item - n_sys);
     }
-    // the last CTA out resets the work counters for the next launch
+    // phase 2: decode items, each warp on its own
+    if (n_dec > 0) decode_phase<D>(p, s, n_dec);
+    __syncthreads();
+
+    // the last CTA out resets the queues for the next launch
     if (threadIdx.x == 0) {
         __threadfence();
-        unsigned done = atomicAdd(&p.ctrl[2], 1u);
+        unsigned done = atomicAdd(&p.ctrl[CTRL_DONE], 1u);
         if (done == gridDim.x - 1) {
-            p.ctrl[1] = 0u;
-            p.ctrl[2] = 0u;
+            p.ctrl[CTRL_ROW_ITEMS] = 0u;
+            p.ctrl[CTRL_DEC_ITEMS] = 0u;
+            p.ctrl[CTRL_DONE] = 0u;
             __threadfence();
         }
     }
 }
 
-// ----------------------------------------------------------------------------- stand-alone relay fusion
+// ============================================================================= stand-alone relay fusion
 // out = a*o_sys + (1-a)*o_ctx, a = e^lse_sys / (e^lse_sys + e^lse_ctx).
 template <int D>
 __global__ void __launch_bounds__(256) fuse_kernel(int B, int Lq, int H, const float *__restrict__ o_sys,
@@ -842,10 +1083,7 @@ __global__ void __launch_bounds__(256) fuse_kernel(int B, int Lq, int H, const f
             r = make_float4(a * x.x + c * y.x, a * x.y + c * y.y, a * x.z + c * y.z, a * x.w + c * y.w);
             lse2 = M + lg2(ws + wc);
         }
-        __half2 h0 = __floats2half2_rn(r.x, r.y), h1 = __floats2half2_rn(r.z, r.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<unsigned *>(&h0);
-        pk.y = *reinterpret_cast<unsigned *>(&h1);
+        uint2 pk = make_uint2(pack_half2(r.x, r.y), pack_half2(r.z, r.w));
         *reinterpret_cast<uint2 *>(out + row * D + d) = pk;
         if (lse_out && d == 0) lse_out[row] = lse2 * kLn2;
     }
