@@ -255,9 +255,11 @@ def run_relay(args):
     case = build_case(args, rank)
     g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
                                               "ctx_lens")}
+    g["q_lens"] = None if case.q_lens is None else case.q_lens.to(dev)
+    mq = case.total_q() if case.q_lens is not None else 0
     rows = case.total_q()
     dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
-                           sys_range=args.sys_range)
+                           sys_range=args.sys_range, max_q_total=mq)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -265,8 +267,8 @@ def run_relay(args):
 
     def step():
         relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
-                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims,
-                                     stream=stream)
+                                     g["block_tables"], g["ctx_lens"], g["q_lens"], out=out, workspace=ws,
+                                     dims=dims, stream=stream)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
@@ -308,13 +310,13 @@ def run_relay(args):
     # non-relay baseline: same requests, system KV re-read per request from the paged pool
     kp, vp, ids = synth.with_system_in_pool(case)
     kp, vp, ids = kp.to(dev), vp.to(dev), ids.to(dev)
-    dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks)
+    dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks, max_q_total=mq)
     ws_b = relay.make_workspace(dims_b, dev)
     out_b = torch.empty_like(out)
 
     def base_step():
-        relay.relay_baseline_decode(g["q"], kp, vp, ids, case.Ls, g["block_tables"], g["ctx_lens"], out=out_b,
-                                    workspace=ws_b, dims=dims_b, stream=stream)
+        relay.relay_baseline_decode(g["q"], kp, vp, ids, case.Ls, g["block_tables"], g["ctx_lens"], g["q_lens"],
+                                    out=out_b, workspace=ws_b, dims=dims_b, stream=stream)
     ms_b, _ = timed(base_step, max(5, args.steps // 2), args.warmup)
     del kp, vp
 
@@ -322,6 +324,8 @@ def run_relay(args):
     hq = case.q.pin_memory()
     hbt = case.block_tables.pin_memory()
     hcl = case.ctx_lens.pin_memory()
+    hql = None if case.q_lens is None else case.q_lens.pin_memory()
+    dql = None if hql is None else torch.empty_like(g["q_lens"])
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dq, dbt, dcl = torch.empty_like(g["q"]), torch.empty_like(g["block_tables"]), torch.empty_like(g["ctx_lens"])
 
@@ -329,13 +333,15 @@ def run_relay(args):
         dq.copy_(hq, non_blocking=True)
         dbt.copy_(hbt, non_blocking=True)
         dcl.copy_(hcl, non_blocking=True)
-        relay.relay_attention_decode(dq, g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"], dbt, dcl, out=out,
+        if dql is not None:
+            dql.copy_(hql, non_blocking=True)
+        relay.relay_attention_decode(dq, g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"], dbt, dcl, dql, out=out,
                                      workspace=ws, dims=dims, stream=stream)
         hout.copy_(out, non_blocking=True)
     ms_e, _ = timed(e2e_step, args.steps, args.warmup)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(sum(ms_e) / len(ms_e), world, dev)
-    h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4
+    h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4 + (0 if hql is None else hql.numel() * 4)
     d2h = hout.numel() * hout.element_size()
 
     cpu = None
@@ -382,15 +388,16 @@ def run_profile(args):
     case = build_case(args, 0)
     g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
                                               "ctx_lens")}
+    ql = None if case.q_lens is None else case.q_lens.to(dev)
     dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
-                           sys_range=args.sys_range)
+                           sys_range=args.sys_range, max_q_total=case.total_q() if ql is not None else 0)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(args.profile):
         flush.zero_()
         relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
-                                     g["block_tables"], g["ctx_lens"], out=out, workspace=ws, dims=dims)
+                                     g["block_tables"], g["ctx_lens"], ql, out=out, workspace=ws, dims=dims)
     torch.cuda.synchronize(dev)
     print(json.dumps({"profile_launches": args.profile, "workload": case.wl.name,
                       "algorithmic_bytes_per_launch": algorithmic_bytes(case)}))

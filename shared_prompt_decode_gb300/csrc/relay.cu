@@ -84,6 +84,7 @@ struct Plan {
     int Mtot = 0;
     int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
     int n_parts = 0, ctx_base = 0, n_prefix = 0;
+    int tps_min = 32, tps_max = 32;
     size_t off_arrive = 0, off_part_o = 0, off_part_lse = 0, total = 0;
 };
 
@@ -119,13 +120,21 @@ Plan make_plan(const relay_dims_t *d, int mode)
         if (mode == MODE_FUSED && d->Ls == 0) pl.R_sys = 0;
     }
     if (ctx) {
-        // context splits per request: decode rows split pages (prefix pages
-        // + context pages) into ctx_split/16-page items; multi-row requests
-        // use splits of at least ctx_split keys, so the page count bounds both
+        // Context splits per request.  A decode request's pages (prefix
+        // pages + context pages) go to items of tps pages, tps chosen on the
+        // device in [tps_min, tps_max] (fixed when ctx_split is given); a
+        // multi-row request uses splits of at least ctx_split keys.  tps_min
+        // keeps every request at <= kMaxCtxParts partials, which bounds the
+        // workspace.
+        constexpr int kMaxCtxParts = 32;
         pl.ctx_split = d->ctx_split > 0 ? d->ctx_split : kAutoCtxSplit;
-        int max_pages = (pl.n_prefix + kBlock - 1) / kBlock + d->max_blocks_per_seq;
-        int pages_per_split = pl.ctx_split / kBlock;
-        pl.C_max = std::max(1, (max_pages + pages_per_split - 1) / pages_per_split);
+        const int max_pages = (pl.n_prefix + kBlock - 1) / kBlock + d->max_blocks_per_seq;
+        pl.tps_max = std::min(pl.ctx_split / kBlock, 32);    // a decode item holds <= 32 pages
+        pl.tps_min = d->ctx_split > 0 ? pl.tps_max
+                                      : std::min(pl.tps_max, std::max(2, (max_pages + kMaxCtxParts - 1) / kMaxCtxParts));
+        const int c_dec = (max_pages + pl.tps_min - 1) / pl.tps_min;
+        const int c_mq = (pl.n_prefix + d->max_blocks_per_seq * kBlock + pl.ctx_split - 1) / pl.ctx_split;
+        pl.C_max = std::max(1, std::max(c_dec, c_mq));
     }
     pl.ctx_base = sys ? pl.R_sys : 0;
     pl.n_parts = (sys ? pl.R_sys : 0) + (ctx ? pl.C_max : 0);
@@ -175,6 +184,8 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.sys_range = pl.sys_range;
     p.ctx_split = pl.ctx_split;
     p.ctx_base = pl.ctx_base;
+    p.tps_min = pl.tps_min;
+    p.tps_max = pl.tps_max;
     p.mode = mode;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

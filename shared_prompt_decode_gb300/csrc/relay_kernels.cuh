@@ -40,12 +40,19 @@
 
 namespace relay {
 
+#ifndef RELAY_WARPS
+#define RELAY_WARPS 8           // warps per CTA (one CTA per SM)
+#endif
+#ifndef RELAY_RING_KB
+#define RELAY_RING_KB 192       // shared memory for K/V staging
+#endif
+
 constexpr int kBlock = 16;      // paged block size (tokens)
-constexpr int kWarps = 8;
+constexpr int kWarps = RELAY_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileK = 64;      // keys per stage in phase 1
 constexpr int kTileM = 16 * kWarps;   // query rows per phase-1 item
-constexpr int kRingBytes = 192 * 1024;
+constexpr int kRingBytes = RELAY_RING_KB * 1024;
 constexpr int kMaxB = 512;
 
 enum Mode : int { MODE_FUSED = 0, MODE_SYS = 1, MODE_CTX = 2, MODE_BASELINE = 3 };
@@ -72,6 +79,7 @@ struct Params {
     float *part_o;                    // [n_parts][max_q_total][H][D]
     float *part_lse;                  // [n_parts][max_q_total][H]  (log2 domain)
     int R_sys, sys_range, ctx_split, ctx_base;   // ctx_base: first partial slot of context parts
+    int tps_min, tps_max;             // pages per decode item: bounds of the adaptive choice
     int mode;
 };
 
@@ -85,8 +93,14 @@ struct Smem {
     alignas(128) unsigned char ring[kRingBytes];
     int qo[kMaxB + 1];        // exclusive prefix of query rows
     int mq[kMaxB + 1];        // exclusive prefix of multi-row context items
-    int dec[kMaxB + 1];       // exclusive prefix of decode context items
-    int warp_tot[3][kWarps];
+    int dec[kMaxB + 1];       // exclusive prefix of decode items over the decode order
+    int nctx[kMaxB];          // context lengths (validated)
+    short order[kMaxB];       // decode requests, longest item first
+    signed char dcls[kMaxB];  // largest item of a decode request in pages (-1: not a decode request)
+    int cls_cnt[33];
+    int n_dec_req;
+    int tps;                  // pages per decode item chosen for this launch
+    int warp_tot[kWarps];
     int item;
     int bad;
     int n_merge;
@@ -199,27 +213,28 @@ __device__ __forceinline__ bool has_ctx(int mode) { return mode != MODE_SYS; }
 // Context work of one request.
 //   decode request (one query row): its key sequence is cut into pages --
 //     ceil(n_prefix/16) prefix pages then ceil(n_ctx/16) context pages -- and
-//     the pages into splits of ctx_split/16 pages (one warp item each);
+//     the pages into ns nearly equal splits of at most ctx_split/16 pages
+//     (one warp item each; split j covers pages [j*pages/ns, (j+1)*pages/ns));
 //   multi-row request: keys [0, n_prefix + n_ctx) in splits of `split` keys,
 //     rows in tiles of kTileM (one CTA item per split and row tile).
 struct ReqInfo {
     int ql, n_ctx;
     int pp;        // prefix pages (decode)
     int pages;     // total pages (decode)
-    int tps;       // pages per split (decode)
+    int tps;       // most pages per split (decode)
     int split;     // keys per split (multi-row)
     int ns;        // splits
     int mt;        // row tiles (multi-row), 1 for decode
 };
 
-__device__ __forceinline__ ReqInfo req_info(const Params &p, int b, int ql)
+__device__ __forceinline__ ReqInfo req_info(const Params &p, int n_ctx, int ql, int tps)
 {
     ReqInfo r;
     r.ql = ql;
-    r.n_ctx = p.ctx_lens[b];
+    r.n_ctx = n_ctx;
     r.pp = (p.n_prefix + kBlock - 1) / kBlock;
     r.pages = r.pp + (r.n_ctx + kBlock - 1) / kBlock;
-    r.tps = p.ctx_split / kBlock;
+    r.tps = tps;                 // at most 32: a decode item holds one page per lane
     if (ql <= 1) {
         r.split = p.ctx_split;
         r.ns = (r.pages + r.tps - 1) / r.tps;
@@ -237,66 +252,145 @@ __device__ __forceinline__ ReqInfo req_info(const Params &p, int b, int ql)
     return r;
 }
 
-// Per-CTA prefix sums over the batch (B <= kMaxB, two entries per thread).
+// Exclusive prefix sum over the batch of per-request values v[k] (request
+// tid*PER + k), written to out[0..n] (out[n] = total).
+template <int D, int PER>
+__device__ __forceinline__ void block_scan(const int (&v)[PER], int *out, int n, Smem<D> &s)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int loc = 0;
+#pragma unroll
+    for (int k = 0; k < PER; k++) loc += v[k];
+    int inc = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += t;
+    }
+    if (lane == 31) s.warp_tot[warp] = inc;
+    __syncthreads();
+    int base = inc - loc;
+    for (int j = 0; j < warp; j++) base += s.warp_tot[j];
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int b = tid * PER + k;
+        if (b < n) out[b] = base;
+        base += v[k];
+    }
+    if (tid == kThreads - 1) out[n] = base;
+    __syncthreads();
+}
+
+// Per-CTA schedule over the batch (B <= kMaxB, PER requests per thread):
+// row prefix qo, multi-row item prefix mq, and the decode queue.
+//   * Pages per decode item: between tps_min and tps_max, chosen so that the
+//     decode queue holds about kItemsPerWarp items per warp of the grid (fine
+//     enough for the dynamic queue to balance, coarse enough to keep the
+//     per-item cost small).
+//   * Decode requests are ordered longest item first (their largest split in
+//     pages, descending; ties by request index), so the queue ends with the
+//     shortest items and the warps finish together.
+// Every CTA computes the same schedule from the same inputs.
 template <int D>
 __device__ void build_schedule(const Params &p, Smem<D> &s)
 {
     constexpr int PER = (kMaxB + kThreads - 1) / kThreads;
+    constexpr int kClasses = 33;                  // item sizes 0..32 pages
+    constexpr int kItemsPerWarp = 8;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int cnt[3][PER];
-    int loc[3] = {0, 0, 0};
+    int vq[PER], vm[PER], vp[PER], nn[PER];
     unsigned flags = 0;
+    if (tid < kClasses) s.cls_cnt[tid] = 0;
+    if (tid == 0) s.bad = 0;
+    const int pp = (p.n_prefix + kBlock - 1) / kBlock;
 #pragma unroll
     for (int k = 0; k < PER; k++) {
-        int b = tid * PER + k;
-        int c0 = 0, c1 = 0, c2 = 0;
+        const int b = tid * PER + k;
+        int ql = 0, n = 0, m = 0, pg = 0;
         if (b < p.B) {
-            int ql = p.q_lens ? p.q_lens[b] : p.Lq;
-            int n = p.ctx_lens ? p.ctx_lens[b] : 0;
+            ql = p.q_lens ? p.q_lens[b] : p.Lq;
+            n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
             if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
-            if (has_ctx(p.mode) && (n < 0 || n > p.max_blocks * kBlock)) { flags |= FLAG_BAD_CTX_LEN; ql = 0; }
-            c0 = ql;
-            if (has_ctx(p.mode) && ql > 0) {
-                ReqInfo r = req_info(p, b, ql);
-                if (ql > 1) c1 = p.H * r.ns * r.mt; else c2 = p.H * r.ns;
+            if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
+            if (has_ctx(p.mode) && ql > 1) {
+                const ReqInfo r = req_info(p, n, ql, p.tps_max);
+                m = p.H * r.ns * r.mt;
             }
+            if (has_ctx(p.mode) && ql == 1) pg = p.H * (pp + (n + kBlock - 1) / kBlock);
         }
-        cnt[0][k] = c0; cnt[1][k] = c1; cnt[2][k] = c2;
-        loc[0] += c0; loc[1] += c1; loc[2] += c2;
+        vq[k] = ql;
+        vm[k] = m;
+        vp[k] = pg;
+        nn[k] = n;
     }
-    int inc[3] = {loc[0], loc[1], loc[2]};
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-#pragma unroll
-        for (int a = 0; a < 3; a++) {
-            int v = __shfl_up_sync(0xffffffffu, inc[a], off);
-            if (lane >= off) inc[a] += v;
-        }
-    }
-    if (lane == 31)
-        for (int a = 0; a < 3; a++) s.warp_tot[a][warp] = inc[a];
-    if (tid == 0) s.bad = 0;
     __syncthreads();
     if (flags) atomicOr(&s.bad, (int)flags);
-    int base[3];
-    for (int a = 0; a < 3; a++) {
-        int w = 0;
-        for (int j = 0; j < warp; j++) w += s.warp_tot[a][j];
-        base[a] = w + inc[a] - loc[a];
+    block_scan<D, PER>(vq, s.qo, p.B, s);
+    block_scan<D, PER>(vm, s.mq, p.B, s);
+    block_scan<D, PER>(vp, s.dec, p.B, s);        // s.dec[B]: decode pages over all heads
+    if (tid == 0) {
+        const long long want = (long long)gridDim.x * kWarps * kItemsPerWarp;
+        int t = (int)((s.dec[p.B] + want - 1) / want);
+        s.tps = max(p.tps_min, min(p.tps_max, t));
     }
-    int *arr[3] = {s.qo, s.mq, s.dec};
+    __syncthreads();
+    const int tps = s.tps;
+    // decode class of every request: its largest item in pages (-1: not decode)
 #pragma unroll
     for (int k = 0; k < PER; k++) {
-        int b = tid * PER + k;
-        if (b < p.B)
-            for (int a = 0; a < 3; a++) {
-                arr[a][b] = base[a];
-                base[a] += cnt[a][k];
+        const int b = tid * PER + k;
+        if (b < p.B) {
+            s.nctx[b] = nn[k];
+            int c = -1;
+            if (has_ctx(p.mode) && vq[k] == 1) {
+                const ReqInfo r = req_info(p, nn[k], 1, tps);
+                c = (r.pages + r.ns - 1) / r.ns;
+                atomicAdd(&s.cls_cnt[c], 1);
             }
+            s.dcls[b] = (signed char)c;
+        }
     }
-    if (tid == kThreads - 1)    // the last thread's running sums are the totals
-        for (int a = 0; a < 3; a++) arr[a][p.B] = base[a];
     __syncthreads();
+    // counting sort of decode requests: class descending, request index ascending
+    if (warp == 0) {
+        // start position of classes 32..1 (lanes 0..31), then class 0
+        const int v = kClasses - 1 - lane;
+        const int cnt = s.cls_cnt[v];
+        int inc = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += t;
+        }
+        const int c0 = s.cls_cnt[0];
+        __syncwarp();
+        s.cls_cnt[v] = inc - cnt;
+        if (lane == 31) {
+            s.cls_cnt[0] = inc;
+            s.n_dec_req = inc + c0;
+        }
+        __syncwarp();
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            const int c = b < p.B ? s.dcls[b] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, c);
+            const int base = c >= 0 ? s.cls_cnt[c] : 0;
+            if (c >= 0) s.order[base + __popc(same & ((1u << lane) - 1u))] = (short)b;
+            __syncwarp();
+            if (c >= 0 && lane == __ffs(same) - 1) s.cls_cnt[c] = base + __popc(same);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // decode items per sorted position
+    int dv[PER];
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        const int pos = tid * PER + k;
+        dv[k] = 0;
+        if (pos < s.n_dec_req) dv[k] = p.H * req_info(p, s.nctx[s.order[pos]], 1, tps).ns;
+    }
+    block_scan<D, PER>(dv, s.dec, s.n_dec_req, s);
     if (tid == 0 && s.qo[p.B] > p.max_q_total) s.bad |= FLAG_Q_TOTAL;
     __syncthreads();
 }
@@ -312,13 +406,13 @@ __device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int
 // threads (a warp or the CTA); thread t of the team handles D/32 adjacent
 // elements of row (t/32) + k*(TEAM/32).
 template <int D, int TEAM>
-__device__ void merge_pair(const Params &p, const int *qo, int b, int h, int t)
+__device__ void merge_pair(const Params &p, const int *qo, const int *nctx, int tps, int b, int h, int t)
 {
     constexpr int V = D / 32;
     constexpr float kLn2 = 0.69314718055994531f;
     const int r0 = qo[b], ql = qo[b + 1] - qo[b];
     const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
-    const int n_ctx = has_ctx(p.mode) ? req_info(p, b, ql).ns : 0;
+    const int n_ctx = has_ctx(p.mode) ? req_info(p, nctx[b], ql, tps).ns : 0;
     const int n = n_sys + n_ctx;
     const int d0 = (t & 31) * V;
     for (int rr = t >> 5; rr < ql; rr += TEAM / 32) {
@@ -380,14 +474,14 @@ __device__ __forceinline__ bool arrive(const Params &p, int b, int h, int target
     return false;
 }
 
-__device__ __forceinline__ int pair_target(const Params &p, const int *qo, int b)
+__device__ __forceinline__ int pair_target(const Params &p, const int *qo, const int *nctx, int tps, int b)
 {
     const int r0 = qo[b], r1 = qo[b + 1];
     int t = 0;
     if (r1 <= r0) return 0;
     if (has_sys(p.mode)) t += p.R_sys * ((r1 - 1) / kTileM - r0 / kTileM + 1);
     if (has_ctx(p.mode)) {
-        ReqInfo ri = req_info(p, b, r1 - r0);
+        ReqInfo ri = req_info(p, nctx[b], r1 - r0, tps);
         t += ri.ns * ri.mt;
     }
     return t;
@@ -456,13 +550,13 @@ struct RowState {
     float m[2], l[2];
 };
 
-// One warp: 16 query rows (A fragments in qf) against the 64 keys of a staged
-// tile.  Lane state: rows g and g+8.
-template <int D>
-__device__ __forceinline__ void row_tile(const __half *K, const __half *V, const unsigned (&qf)[D / 16][4],
+// One warp: 16 query rows (A fragments in qf) against keys [kb, kb + 8*NT)
+// of a staged tile.  Lane state: rows g and g+8.
+template <int D, int NT>
+__device__ __forceinline__ void row_tile(const __half *K, const __half *V, int kb, const unsigned (&qf)[D / 16][4],
                                          RowState<D> &ws, int key_tile0, int end0, int end1, float scale_log2)
 {
-    constexpr int NT = kTileK / 8;
+    static_assert(NT % 2 == 0 || NT == 1, "key sub-range of 8, 16, 32 or 64 keys");
     const int lane = threadIdx.x & 31;
     float sc[NT][4];
 #pragma unroll
@@ -470,16 +564,29 @@ __device__ __forceinline__ void row_tile(const __half *K, const __half *V, const
 #pragma unroll
         for (int e = 0; e < 4; e++) sc[n][e] = 0.f;
 
+    if constexpr (NT == 1) {
 #pragma unroll
-    for (int kt = 0; kt < D / 16; kt++) {
-#pragma unroll
-        for (int np = 0; np < NT / 2; np++) {
-            int row = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-            int ch = 2 * kt + ((lane >> 3) & 1);
+        for (int kp = 0; kp < D / 32; kp++) {
+            // four 8x8 blocks: keys kb..kb+7, d-chunks 4kp .. 4kp+3
+            int row = kb + (lane & 7);
+            int ch = 4 * kp + (lane >> 3);
             unsigned b0, b1, b2, b3;
             ldsm_x4(b0, b1, b2, b3, K + swz<D>(row, ch));
-            mma16816(sc[2 * np], qf[kt], b0, b1);
-            mma16816(sc[2 * np + 1], qf[kt], b2, b3);
+            mma16816(sc[0], qf[2 * kp], b0, b1);
+            mma16816(sc[0], qf[2 * kp + 1], b2, b3);
+        }
+    } else {
+#pragma unroll
+        for (int kt = 0; kt < D / 16; kt++) {
+#pragma unroll
+            for (int np = 0; np < NT / 2; np++) {
+                int row = kb + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                int ch = 2 * kt + ((lane >> 3) & 1);
+                unsigned b0, b1, b2, b3;
+                ldsm_x4(b0, b1, b2, b3, K + swz<D>(row, ch));
+                mma16816(sc[2 * np], qf[kt], b0, b1);
+                mma16816(sc[2 * np + 1], qf[kt], b2, b3);
+            }
         }
     }
 
@@ -489,7 +596,7 @@ __device__ __forceinline__ void row_tile(const __half *K, const __half *V, const
     for (int n = 0; n < NT; n++) {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            int key = key_tile0 + n * 8 + 2 * tig + (e & 1);
+            int key = key_tile0 + kb + n * 8 + 2 * tig + (e & 1);
             int end = (e < 2) ? end0 : end1;
             float v = sc[n][e] * scale_log2;
             sc[n][e] = (key < end) ? v : kNegInf;
@@ -525,29 +632,55 @@ __device__ __forceinline__ void row_tile(const __half *K, const __half *V, const
         ws.o[d][2] *= al1; ws.o[d][3] *= al1;
     }
 
-#pragma unroll
-    for (int ks = 0; ks < NT / 2; ks++) {
+    if constexpr (NT == 1) {
+        // one k-step of 16 keys whose upper 8 weights are zero; the V rows
+        // of those 8 keys are read (they lie inside the staged tile) but
+        // multiplied by zero, and they are finite (zero-filled or real data)
         unsigned pa[4];
-        pa[0] = pack_half2(sc[2 * ks][0], sc[2 * ks][1]);
-        pa[1] = pack_half2(sc[2 * ks][2], sc[2 * ks][3]);
-        pa[2] = pack_half2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-        pa[3] = pack_half2(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+        pa[0] = pack_half2(sc[0][0], sc[0][1]);
+        pa[1] = pack_half2(sc[0][2], sc[0][3]);
+        pa[2] = 0u;
+        pa[3] = 0u;
+        const int kb16 = kb & ~15;
+        const int hi = kb & 8;     // our 8 keys are rows kb16+hi .. +7 of the 16-key step
+        if (hi) {                  // move our weights to the upper half of the step
+            pa[2] = pa[0]; pa[3] = pa[1]; pa[0] = 0u; pa[1] = 0u;
+        }
 #pragma unroll
         for (int dp = 0; dp < D / 16; dp++) {
-            int row = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            int row = kb16 + (lane & 7) + (((lane >> 3) & 1) << 3);
             int ch = 2 * dp + (lane >> 4);
             unsigned b0, b1, b2, b3;
             ldsm_x4_t(b0, b1, b2, b3, V + swz<D>(row, ch));
             mma16816(ws.o[2 * dp], pa, b0, b1);
             mma16816(ws.o[2 * dp + 1], pa, b2, b3);
         }
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < NT / 2; ks++) {
+            unsigned pa[4];
+            pa[0] = pack_half2(sc[2 * ks][0], sc[2 * ks][1]);
+            pa[1] = pack_half2(sc[2 * ks][2], sc[2 * ks][3]);
+            pa[2] = pack_half2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+            pa[3] = pack_half2(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; dp++) {
+                int row = kb + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                int ch = 2 * dp + (lane >> 4);
+                unsigned b0, b1, b2, b3;
+                ldsm_x4_t(b0, b1, b2, b3, V + swz<D>(row, ch));
+                mma16816(ws.o[2 * dp], pa, b0, b1);
+                mma16816(ws.o[2 * dp + 1], pa, b2, b3);
+            }
+        }
     }
 }
 
-// Key-tile pipeline of a row item over [key0, key_hi): every warp owns 16
-// rows and consumes every tile.  Warps without valid rows only help load.
-template <int D>
-__device__ __forceinline__ void row_pipeline(Smem<D> &s, const KeySrc &src, int key0, int key_hi,
+// Key-tile pipeline of a row item over [key0, key_hi): each warp owns 16 rows
+// and keys [kb, kb + 8*NT) of every tile.  Warps without valid rows only help
+// load.
+template <int D, int NT>
+__device__ __forceinline__ void row_pipeline(Smem<D> &s, const KeySrc &src, int key0, int key_hi, int kb,
                                              const unsigned (&qf)[D / 16][4], RowState<D> &ws, int end0,
                                              int end1, bool active, float scale_log2, unsigned *flags)
 {
@@ -559,7 +692,7 @@ __device__ __forceinline__ void row_pipeline(Smem<D> &s, const KeySrc &src, int 
         int jn = j + S - 1;
         if (jn < n_tiles) load_tile<D>(s, jn % S, src, key0 + jn * kTileK, key_hi, flags);
         cp_async_commit();
-        if (active) row_tile<D>(s.ck(j % S), s.cv(j % S), qf, ws, key0 + j * kTileK, end0, end1, scale_log2);
+        if (active) row_tile<D, NT>(s.ck(j % S), s.cv(j % S), kb, qf, ws, key0 + j * kTileK, end0, end1, scale_log2);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -617,13 +750,91 @@ __device__ __forceinline__ void write_row_partials(const Params &p, const RowSta
     }
 }
 
+// Warp roles of a row item with `rows` valid rows: RG groups of 16 rows, and
+// when the rows fill fewer than all warps, KG groups that split each tile's
+// 64 keys (their softmax states are combined at the end of the item).
+struct RowRoles {
+    int KG, RGp, rg, kg;
+    bool active;
+};
+
+__device__ __forceinline__ RowRoles row_roles(int rows)
+{
+    RowRoles r;
+    const int RG = (rows + 15) / 16;
+    int np2 = 1;
+    while (np2 < RG) np2 <<= 1;
+    r.KG = min(kWarps / np2, kTileK / 8);
+    r.RGp = kWarps / r.KG;
+    const int warp = threadIdx.x >> 5;
+    r.rg = warp % r.RGp;
+    r.kg = warp / r.RGp;
+    r.active = r.rg < RG && r.kg < r.KG;
+    return r;
+}
+
+template <int D>
+__device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0, int key_hi, const RowRoles &rr,
+                                         const unsigned (&qf)[D / 16][4], RowState<D> &ws, int end0, int end1,
+                                         float scale_log2, unsigned *flags)
+{
+    const int kpk = kTileK / rr.KG;          // keys per key group
+    const int kb = rr.kg * kpk;
+    switch (rr.KG) {
+    case 1: row_pipeline<D, 8>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+    case 2: row_pipeline<D, 4>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+    case 4: row_pipeline<D, 2>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+    default: row_pipeline<D, 1>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+    }
+    if (rr.KG == 1) return;
+    // combine the key groups' states into the kg == 0 warps (ring is idle now)
+    constexpr int PL = D / 2 + 4;            // floats per lane
+    float *red = reinterpret_cast<float *>(s.ring);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (rr.active && rr.kg > 0) {
+        float *mine = red + warp * PL * 32;
+#pragma unroll
+        for (int n = 0; n < D / 8; n++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) mine[(n * 4 + e) * 32 + lane] = ws.o[n][e];
+        mine[(D / 2 + 0) * 32 + lane] = ws.m[0];
+        mine[(D / 2 + 1) * 32 + lane] = ws.m[1];
+        mine[(D / 2 + 2) * 32 + lane] = ws.l[0];
+        mine[(D / 2 + 3) * 32 + lane] = ws.l[1];
+    }
+    __syncthreads();
+    if (rr.active && rr.kg == 0) {
+        for (int k = 1; k < rr.KG; k++) {
+            const float *oth = red + (warp + k * rr.RGp) * PL * 32;
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                const float mo = oth[(D / 2 + half) * 32 + lane];
+                const float lo = oth[(D / 2 + 2 + half) * 32 + lane];
+                const float M = fmaxf(ws.m[half], mo);
+                const float mu = (M == kNegInf) ? 0.f : M;
+                const float a = ex2(ws.m[half] - mu), c = ex2(mo - mu);
+                ws.l[half] = ws.l[half] * a + lo * c;
+                ws.m[half] = M;
+#pragma unroll
+                for (int n = 0; n < D / 8; n++) {
+                    ws.o[n][2 * half] = ws.o[n][2 * half] * a + oth[(n * 4 + 2 * half) * 32 + lane] * c;
+                    ws.o[n][2 * half + 1] = ws.o[n][2 * half + 1] * a + oth[(n * 4 + 2 * half + 1) * 32 + lane] * c;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
 template <int D>
 __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
 {
+    // heads vary fastest: CTAs that run concurrently read whole [H, D] rows of
+    // the system cache together instead of one head's 256-byte slivers
     const int T = (Mtot + kTileM - 1) / kTileM;
-    const int tau = item % T;
-    const int rho = (item / T) % p.R_sys;
-    const int h = item / (T * p.R_sys);
+    const int h = item % p.H;
+    const int tau = (item / p.H) % T;
+    const int rho = item / (p.H * T);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2;
 
@@ -632,7 +843,8 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     const int key_hi = min(key0 + p.sys_range, p.Ls);
     row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
-    const int rW = tau * kTileM + warp * 16;
+    const RowRoles rr = row_roles(min(kTileM, Mtot - tau * kTileM));
+    const int rW = tau * kTileM + rr.rg * 16;
     const int rA = rW + g, rB = rA + 8;
     const __half *qa = nullptr, *qb = nullptr;
     if (rA < Mtot) {
@@ -652,9 +864,8 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
         for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
-    const bool active = rW < Mtot;
-    row_pipeline<D>(s, src, key0, key_hi, qf, ws, key_hi, key_hi, active, p.scale_log2, p.ctrl);
-    if (active) write_row_partials<D>(p, ws, rho, h, rA, rA < Mtot, rB, rB < Mtot);
+    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
+    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, rho, h, rA, rA < Mtot, rB, rB < Mtot);
     __threadfence();
     __syncthreads();
 
@@ -665,7 +876,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     if (threadIdx.x == 0) s.n_merge = 0;
     __syncthreads();
     for (int b = bf + threadIdx.x; b <= bl; b += kThreads) {
-        if (s.qo[b + 1] > s.qo[b] && arrive(p, b, h, pair_target(p, s.qo, b))) {
+        if (s.qo[b + 1] > s.qo[b] && arrive(p, b, h, pair_target(p, s.qo, s.nctx, s.tps, b))) {
             int k = atomicAdd(&s.n_merge, 1);
             s.merge_b[k] = b;
         }
@@ -675,7 +886,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     if (nm > 0) {
         __threadfence();
         // one warp per completed pair
-        for (int k = warp; k < nm; k += kWarps) merge_pair<D, 32>(p, s.qo, s.merge_b[k], h, lane);
+        for (int k = warp; k < nm; k += kWarps) merge_pair<D, 32>(p, s.qo, s.nctx, s.tps, s.merge_b[k], h, lane);
     }
     __syncthreads();
 }
@@ -686,7 +897,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
 {
     const int b = find_owner(s.mq, p.B, local);
     const int ql = s.qo[b + 1] - s.qo[b];
-    const ReqInfo ri = req_info(p, b, ql);
+    const ReqInfo ri = req_info(p, s.nctx[b], ql, s.tps);
     int j = local - s.mq[b];
     const int mtile = j % ri.mt;
     j /= ri.mt;
@@ -708,7 +919,8 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     const int key_hi = min(key0 + ri.split, vis(last_row));
     row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
-    const int iW = mtile * kTileM + warp * 16;
+    const RowRoles rr = row_roles(min(kTileM, ql - mtile * kTileM));
+    const int iW = mtile * kTileM + rr.rg * 16;
     const int iA = iW + g, iB = iA + 8;
     const __half *qa = iA < ql ? p.q + (((size_t)b * p.Lq + iA) * p.H + h) * D : nullptr;
     const __half *qb = iB < ql ? p.q + (((size_t)b * p.Lq + iB) * p.H + h) * D : nullptr;
@@ -723,80 +935,85 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
         for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
-    const bool active = iW < ql;
-    row_pipeline<D>(s, src, key0, key_hi, qf, ws, endA, endB, active, p.scale_log2, p.ctrl);
-    if (active) write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, s.qo[b] + iB, iB < ql);
+    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
+    if (rr.active && rr.kg == 0)
+        write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, s.qo[b] + iB, iB < ql);
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s.qo, b)) ? 1 : 0;
+    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s.qo, s.nctx, s.tps, b)) ? 1 : 0;
     __syncthreads();
     if (s.n_merge) {
         __threadfence();
-        merge_pair<D, kThreads>(p, s.qo, b, h, threadIdx.x);
+        merge_pair<D, kThreads>(p, s.qo, s.nctx, s.tps, b, h, threadIdx.x);
     }
     __syncthreads();
 }
 
 // ============================================================================= phase 2: decode items
+// A decode item, decoded by every lane of the warp.  Lane j also holds the
+// physical block of the item's page j (fetched when the item is decoded, so
+// the page loads never wait on a block-table lookup) and lanes 0..3 hold the
+// query as the B operand of S^T = K q.
+template <int D>
 struct DecItem {
     int id;          // queue index, or -1 when the queue is exhausted
     int b, h, split;
     int p0, np;      // first page and page count of the item
     int pp;          // prefix pages of the request's key sequence
     int n_ctx;
+    int blk;         // lane j: block of page p0 + j
+    unsigned qb[D / 16][2];
 };
 
 template <int D>
-__device__ __forceinline__ DecItem dec_item(const Params &p, const Smem<D> &s, int id, int n_dec)
+__device__ __forceinline__ void dec_item(const Params &p, const Smem<D> &s, int id, int n_dec, DecItem<D> &it)
 {
-    DecItem it;
+    const int lane = threadIdx.x & 31;
     it.id = -1;
-    it.b = it.h = it.split = it.p0 = it.np = it.pp = it.n_ctx = 0;
-    if (id >= n_dec) return it;
+    it.np = 0;
+    if (id >= n_dec) return;
     it.id = id;
-    it.b = find_owner(s.dec, p.B, id);
-    const ReqInfo ri = req_info(p, it.b, 1);
-    const int j = id - s.dec[it.b];
+    const int pos = find_owner(s.dec, s.n_dec_req, id);
+    it.b = s.order[pos];
+    it.n_ctx = s.nctx[it.b];
+    const ReqInfo ri = req_info(p, it.n_ctx, 1, s.tps);
+    const int j = id - s.dec[pos];
     it.split = j % ri.ns;
     it.h = j / ri.ns;
-    it.p0 = it.split * ri.tps;
-    it.np = min(ri.tps, ri.pages - it.p0);
-    if (it.np < 0) it.np = 0;
+    it.p0 = it.split * ri.pages / ri.ns;
+    it.np = (it.split + 1) * ri.pages / ri.ns - it.p0;
     it.pp = ri.pp;
-    it.n_ctx = ri.n_ctx;
-    return it;
-}
-
-// Physical block and valid rows of page `pg` of the item's key sequence.
-__device__ __forceinline__ int page_block(const Params &p, const DecItem &it, int pg, int &rows)
-{
-    int blk;
-    if (pg < it.pp) {
-        blk = p.prefix_ids[pg];
-        rows = min(kBlock, p.n_prefix - pg * kBlock);
-    } else {
-        blk = p.block_tables[(size_t)it.b * p.max_blocks + (pg - it.pp)];
-        rows = min(kBlock, it.n_ctx - (pg - it.pp) * kBlock);
+    it.blk = -1;
+    if (lane < it.np) {
+        const int pg = it.p0 + lane;
+        it.blk = pg < it.pp ? p.prefix_ids[pg] : p.block_tables[(size_t)it.b * p.max_blocks + (pg - it.pp)];
     }
-    return blk;
+    const __half *q = p.q + ((size_t)it.b * p.Lq * p.H + it.h) * D;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; kt++) {
+        // column 0 of the B operand: rows k = 2*tig, 2*tig+1 (b0) and +8 (b1), lanes 0..3
+        const int c = kt * 16 + 2 * (lane & 3);
+        it.qb[kt][0] = lane < 4 ? ld_u32(q + c) : 0u;
+        it.qb[kt][1] = lane < 4 ? ld_u32(q + c + 8) : 0u;
+    }
 }
 
-__device__ __forceinline__ int page_rows(const Params &p, const DecItem &it, int pg)
+__device__ __forceinline__ int page_rows(const Params &p, int pp, int n_ctx, int pg)
 {
-    return pg < it.pp ? min(kBlock, p.n_prefix - pg * kBlock) : min(kBlock, it.n_ctx - (pg - it.pp) * kBlock);
+    return pg < pp ? min(kBlock, p.n_prefix - pg * kBlock) : min(kBlock, n_ctx - (pg - pp) * kBlock);
 }
 
-// One lane's share of staging page `pg` (16 rows of K and V) into the warp's
+// One lane's share of staging page j of the item (16 rows of K and V) into a
 // ring slot; rows past the page's valid rows, or a bad block, are zero-filled.
 template <int D>
-__device__ __forceinline__ void load_page(const Params &p, __half *K, __half *V, const DecItem &it, int pg,
+__device__ __forceinline__ void load_page(const Params &p, __half *K, __half *V, const DecItem<D> &it, int j,
                                           int lane)
 {
     constexpr int CPR = D / 8;
     constexpr int PER = kBlock * CPR / 32;
-    int rows;
-    int blk = page_block(p, it, pg, rows);
-    bool ok = blk >= 0 && blk < p.num_blocks;
+    const int blk = __shfl_sync(0xffffffffu, it.blk, j);
+    const int rows = page_rows(p, it.pp, it.n_ctx, it.p0 + j);
+    const bool ok = blk >= 0 && blk < p.num_blocks;
     if (!ok && lane == 0) atomicOr(&p.ctrl[CTRL_FLAGS], FLAG_BAD_BLOCK);
     const size_t base = (((size_t)(ok ? blk : 0) * p.H + it.h) * kBlock) * D;
 #pragma unroll
@@ -877,7 +1094,7 @@ __device__ __forceinline__ void dec_page(const __half *K, const __half *V, const
 // Finish a decode item: write its partial and count its arrival; the warp that
 // completes the pair merges it.
 template <int D>
-__device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem &it, DecState<D> &st)
+__device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem<D> &it, DecState<D> &st)
 {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
@@ -900,77 +1117,69 @@ __device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem &i
     __threadfence();
     __syncwarp();
     int last = 0;
-    if (lane == 0) last = arrive(p, it.b, it.h, pair_target(p, s.qo, it.b)) ? 1 : 0;
+    if (lane == 0) last = arrive(p, it.b, it.h, pair_target(p, s.qo, s.nctx, s.tps, it.b)) ? 1 : 0;
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
         __threadfence();
-        merge_pair<D, 32>(p, s.qo, it.b, it.h, lane);
-    }
-}
-
-template <int D>
-__device__ __forceinline__ void dec_load_q(const Params &p, const DecItem &it, unsigned (&qb)[D / 16][2])
-{
-    const int lane = threadIdx.x & 31;
-    const __half *q = p.q + ((size_t)it.b * p.Lq * p.H + it.h) * D;
-#pragma unroll
-    for (int kt = 0; kt < D / 16; kt++) {
-        // B fragment of q in column 0: rows k = 2*tig, 2*tig+1 (b0) and +8 (b1), lanes 0..3
-        int c = kt * 16 + 2 * (lane & 3);
-        qb[kt][0] = lane < 4 ? ld_u32(q + c) : 0u;
-        qb[kt][1] = lane < 4 ? ld_u32(q + c + 8) : 0u;
+        merge_pair<D, 32>(p, s.qo, s.nctx, s.tps, it.b, it.h, lane);
     }
 }
 
 // Phase 2 for one warp: pull decode items until the queue is empty, streaming
-// pages through the warp's ring and prefetching across item boundaries.
+// pages through the warp's ring and prefetching across item boundaries.  The
+// item after the current one is decoded (block ids and query loads issued)
+// as soon as the current one starts, and the queue ticket after that is
+// requested at the same time, so no item start waits on memory.
 template <int D>
 __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    auto fetch = [&]() {
-        int id = 0;
-        if (lane == 0) id = (int)atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
-        id = __shfl_sync(0xffffffffu, id, 0);
-        return dec_item<D>(p, s, id, n_dec);
+    // the first ticket of every warp is static; later ones come from the queue
+    unsigned ticket = blockIdx.x * kWarps + warp;
+    auto request = [&]() {      // ask for a ticket; its value is read later
+        if (lane == 0) ticket = gridDim.x * kWarps + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
+    };
+    auto take = [&](DecItem<D> &it) {
+        int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
+        dec_item<D>(p, s, id, n_dec, it);
+        if (it.id >= 0) request();
     };
 
-    DecItem cur = fetch();
+    DecItem<D> cur, nxt;
+    take(cur);
     if (cur.id < 0) return;
-    DecItem nxt = dec_item<D>(p, s, n_dec, n_dec);   // empty
-    bool nxt_fetched = false;
+    take(nxt);
     bool load_on_nxt = false;     // the loader has moved on to `nxt`
     int load_pg = 0;              // next page (relative) of the item being loaded
     int issued = 0, computed = 0;
 
     auto fill = [&]() {
         while (issued - computed < S - 1) {
-            const DecItem &li = load_on_nxt ? nxt : cur;
-            if (load_pg < li.np) {
-                int st = issued % S;
-                load_page<D>(p, s.wk(warp, st), s.wv(warp, st), li, li.p0 + load_pg, lane);
-                cp_async_commit();
-                load_pg++;
-                issued++;
-            } else if (!load_on_nxt) {
-                if (!nxt_fetched) {
-                    nxt = fetch();
-                    nxt_fetched = true;
+            if (!load_on_nxt) {
+                if (load_pg < cur.np) {
+                    const int st = issued % S;
+                    load_page<D>(p, s.wk(warp, st), s.wv(warp, st), cur, load_pg, lane);
+                    cp_async_commit();
+                    load_pg++;
+                    issued++;
+                    continue;
                 }
                 if (nxt.id < 0) break;
                 load_on_nxt = true;
                 load_pg = 0;
-            } else {
-                break;
             }
+            if (load_pg >= nxt.np) break;
+            const int st = issued % S;
+            load_page<D>(p, s.wk(warp, st), s.wv(warp, st), nxt, load_pg, lane);
+            cp_async_commit();
+            load_pg++;
+            issued++;
         }
     };
 
     fill();
     for (;;) {
-        unsigned qb[D / 16][2];
-        dec_load_q<D>(p, cur, qb);
         DecState<D> st;
 #pragma unroll
         for (int mt = 0; mt < D / 16; mt++)
@@ -982,22 +1191,20 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
             cp_async_wait_dyn(issued - computed - 1);
             __syncwarp();
             const int stg = computed % S;
-            dec_page<D>(s.wk(warp, stg), s.wv(warp, stg), qb, st, page_rows(p, cur, cur.p0 + j), p.scale_log2);
+            dec_page<D>(s.wk(warp, stg), s.wv(warp, stg), cur.qb, st, page_rows(p, cur.pp, cur.n_ctx, cur.p0 + j),
+                        p.scale_log2);
             __syncwarp();
             computed++;
             fill();
         }
-        if (!nxt_fetched) {     // the ring still held pages of this item: fetch the next one now
-            nxt = fetch();
-            nxt_fetched = true;
-        }
         dec_epilogue<D>(p, s, cur, st);
         if (nxt.id < 0) break;
-        // nxt becomes current; its pages already issued stay in flight
+        // nxt becomes current (its pages already issued stay in flight), and
+        // the item after it is decoded now
         if (!load_on_nxt) load_pg = 0;
-        cur = nxt;
-        nxt_fetched = false;
         load_on_nxt = false;
+        cur = nxt;
+        take(nxt);
         fill();
     }
     cp_async_wait<0>();
@@ -1020,17 +1227,16 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     const int T = (Mtot + kTileM - 1) / kTileM;
     const int n_sys = has_sys(p.mode) ? p.H * p.R_sys * T : 0;
     const int n_rows = n_sys + s.mq[p.B];
-    const int n_dec = s.dec[p.B];
+    const int n_dec = s.dec[s.n_dec_req];
 
-    // phase 1: row items, the whole CTA per item
-    for (;;) {
-        if (threadIdx.x == 0) s.item = (int)atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u);
-        __syncthreads();
-        const int item = s.item;
-        __syncthreads();
-        if (item >= n_rows) break;
+    // phase 1: row items, the whole CTA per item (the first one is static)
+    for (int item = blockIdx.x; item < n_rows;) {
         if (item < n_sys) sys_item<D>(p, s, item, Mtot);
         else mq_item<D>(p, s, item - n_sys);
+        if (threadIdx.x == 0) s.item = (int)(gridDim.x + atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u));
+        __syncthreads();
+        item = s.item;
+        __syncthreads();
     }
     // phase 2: decode items, each warp on its own
     if (n_dec > 0) decode_phase<D>(p, s, n_dec);
