@@ -8,7 +8,10 @@ shapes, through the C ABI of librelay.
 Prints ONE JSON line (rank 0).  `value` is tokens/s over the whole job (a
 token = one query row of one request, all heads), measured with CUDA events
 around each step's kernel on device-resident inputs, L2 flushed between
-steps.  `e2e` repeats the measurement through the public API with the
+steps: a 256 MB buffer is written and then a second 256 MB buffer read, so
+each step starts with L2 holding clean, unrelated lines (a write-only flush
+would leave ~128 MB of dirty lines whose write-back the next step would pay).
+The step itself is replayed from a CUDA graph.  `e2e` repeats the measurement through the public API with the
 step's per-request inputs (q, block tables, lengths) copied from pinned host
 memory and the output copied back inside the timed region; the KV caches are
 persistent device state, as in a serving system.  `--impl reference` times
@@ -181,7 +184,8 @@ def algorithmic_bytes(case):
 def workload_config(case, args):
     return {"workload": case.wl.name, "B": case.B, "H": case.H, "D": case.D, "Ls": case.Ls,
             "Lq": case.Lq, "query_rows": case.total_q(), "ctx_tokens": int(case.ctx_lens.sum()),
-            "block_size": 16, "seed": args.seed, "l2": "flushed between steps (256 MB write)",
+            "block_size": 16, "seed": args.seed,
+            "l2": "flushed between steps: 256 MB written, then another 256 MB read (L2 clean and cold)",
             "parallelism": f"replicas x{args.world} (independent batches)"}
 
 
@@ -262,17 +266,36 @@ def run_relay(args):
                            sys_range=args.sys_range, max_q_total=mq)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
+
+    def as_graph(fn):
+        """Capture one call of fn (after two eager calls) and return a replay function."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        return graph.replay
 
     def step():
         relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
                                      g["block_tables"], g["ctx_lens"], g["q_lens"], out=out, workspace=ws,
-                                     dims=dims, stream=stream)
+                                     dims=dims)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             fn()
         torch.cuda.synchronize(dev)
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -281,7 +304,7 @@ def run_relay(args):
         torch.cuda.synchronize(dev)
         w0 = time.perf_counter()
         for i in range(steps):
-            flush.zero_()
+            flush()
             starts[i].record(stream)
             fn()
             ends[i].record(stream)
@@ -291,8 +314,9 @@ def run_relay(args):
         ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         return ms, wall
 
+    step_graph = as_graph(step)
     with ClockSampler(local) as clk:
-        ms, wall = timed(step, args.steps, args.warmup)
+        ms, wall = timed(step_graph, args.steps, args.warmup)
     clocks = clk.summary()
     mean_ms = max_over_ranks(sum(ms) / len(ms), world, dev)
     value = world * rows / (mean_ms * 1e-3)
@@ -316,8 +340,8 @@ def run_relay(args):
 
     def base_step():
         relay.relay_baseline_decode(g["q"], kp, vp, ids, case.Ls, g["block_tables"], g["ctx_lens"], g["q_lens"],
-                                    out=out_b, workspace=ws_b, dims=dims_b, stream=stream)
-    ms_b, _ = timed(base_step, max(5, args.steps // 2), args.warmup)
+                                    out=out_b, workspace=ws_b, dims=dims_b)
+    ms_b, _ = timed(as_graph(base_step), max(5, args.steps // 2), args.warmup)
     del kp, vp
 
     # end to end through the public API, host buffers, copies inside the timed region
@@ -362,14 +386,14 @@ def run_relay(args):
         "algorithmic_bytes_per_step": abytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "relay_kernel<128> (one launch per step)",
+                     "kernel": "relay_kernel<128> + merge_kernel<128> (two launches per step, one graph)",
                      "peak_source": f"{peaks['source']} copy bandwidth (burst)"},
         "nonrelay_baseline": {"kernel": "relay_baseline_decode (system KV re-read per request)",
                               "step_us": 1e3 * base_mean, "tokens_per_s": rows / (base_mean * 1e-3),
                               "relay_speedup": base_mean / statistics.mean(ms)},
         "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -393,9 +417,11 @@ def run_profile(args):
                            sys_range=args.sys_range, max_q_total=case.total_q() if ql is not None else 0)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(args.profile):
-        flush.zero_()
+        flush_w.zero_()
+        flush_r.sum()
         relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"],
                                      g["block_tables"], g["ctx_lens"], ql, out=out, workspace=ws, dims=dims)
     torch.cuda.synchronize(dev)

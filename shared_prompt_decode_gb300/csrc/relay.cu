@@ -85,7 +85,7 @@ struct Plan {
     int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
     int n_parts = 0, ctx_base = 0, n_prefix = 0;
     int tps_min = 32, tps_max = 32;
-    size_t off_arrive = 0, off_part_o = 0, off_part_lse = 0, total = 0;
+    size_t off_sched = 0, off_part_o = 0, off_part_lse = 0, total = 0;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -138,9 +138,9 @@ Plan make_plan(const relay_dims_t *d, int mode)
     }
     pl.ctx_base = sys ? pl.R_sys : 0;
     pl.n_parts = (sys ? pl.R_sys : 0) + (ctx ? pl.C_max : 0);
-    pl.off_arrive = 256;
-    size_t arrive_bytes = ((size_t)d->B * d->H * sizeof(unsigned) + 255) / 256 * 256;
-    pl.off_part_o = pl.off_arrive + arrive_bytes;
+    pl.off_sched = 256;
+    size_t sched_bytes = ((size_t)(2 * d->B + 2) * sizeof(int) + 255) / 256 * 256;
+    pl.off_part_o = pl.off_sched + sched_bytes;
     size_t rows = (size_t)pl.n_parts * pl.Mtot * d->H;
     pl.off_part_lse = pl.off_part_o + (rows * d->D * sizeof(float) + 255) / 256 * 256;
     pl.total = pl.off_part_lse + (rows * sizeof(float) + 255) / 256 * 256;
@@ -177,7 +177,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.scale_log2 = scale_log2_of(d);
     p.n_prefix = pl.n_prefix;
     p.ctrl = reinterpret_cast<unsigned *>(base);
-    p.arrive = reinterpret_cast<unsigned *>(base + pl.off_arrive);
+    p.sched = reinterpret_cast<int *>(base + pl.off_sched);
     p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
     p.part_lse = reinterpret_cast<float *>(base + pl.off_part_lse);
     p.R_sys = pl.R_sys;
@@ -195,6 +195,26 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         relay_kernel<64><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
+
+    // merge kernel: one warp per (row, head), launched as a programmatic
+    // dependent so that its launch overlaps the first kernel's tail
+    const long long warps = (long long)pl.Mtot * d->H;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + kWarps - 1) / kWarps));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = d->D == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128>, p)
+                                : cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RELAY_ERR_CUDA;
+    }
     return RELAY_OK;
 }
 

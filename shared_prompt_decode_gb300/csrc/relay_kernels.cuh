@@ -30,9 +30,11 @@
 //   output as O^T = V^T P, so a single query row wastes no MMA rows.
 //
 // Every item writes one fp32 partial result (normalised output and its
-// log2-sum-exp).  The item whose arrival completes a (request, head) pair
-// merges all of that pair's partials: the relay fusion, generalised to any
-// number of parts, as a convex combination weighted by softmax mass.
+// log2-sum-exp) and moves on: no fence, no counter, no waiting.  A second,
+// small kernel, launched as a programmatic dependent of the first, merges
+// every row's partials: the relay fusion, generalised to any number of parts
+// (system ranges and context splits), as a convex combination weighted by
+// softmax mass.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -75,7 +77,7 @@ struct Params {
     float *lse_out;                   // nullable
     float *o_f32, *lse_f32;           // sys-only / ctx-only outputs
     unsigned *ctrl;                   // see CTRL_*
-    unsigned *arrive;                 // [B*H] arrival counters
+    int *sched;                       // schedule handed to the merge kernel: [tps, qo[0..B], nctx[0..B-1]]
     float *part_o;                    // [n_parts][max_q_total][H][D]
     float *part_lse;                  // [n_parts][max_q_total][H]  (log2 domain)
     int R_sys, sys_range, ctx_split, ctx_base;   // ctx_base: first partial slot of context parts
@@ -103,8 +105,6 @@ struct Smem {
     int warp_tot[kWarps];
     int item;
     int bad;
-    int n_merge;
-    int merge_b[kTileM];
 
     __device__ __half *ck(int st) { return reinterpret_cast<__half *>(ring + st * kStageC); }
     __device__ __half *cv(int st) { return ck(st) + kTileK * D; }
@@ -401,90 +401,91 @@ __device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int
     return ((size_t)part * p.max_q_total + r) * p.H + h;
 }
 
-// Merge every partial of (b, h) into the output: the convex combination of
-// the parts weighted by their softmax mass.  Executed by a team of TEAM
-// threads (a warp or the CTA); thread t of the team handles D/32 adjacent
-// elements of row (t/32) + k*(TEAM/32).
-template <int D, int TEAM>
-__device__ void merge_pair(const Params &p, const int *qo, const int *nctx, int tps, int b, int h, int t)
+// Merge the partials of one output row (compact row r = row i of request b,
+// head h) into the output: the convex combination of the parts weighted by
+// their softmax mass.  One warp; lane k loads the log-sum-exp of part k (one
+// round trip), then the parts' output rows are loaded eight at a time with
+// all eight loads in flight together.  Lane t handles D/32 adjacent elements.
+template <int D>
+__device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx)
 {
     constexpr int V = D / 32;
+    constexpr int CH = 8;
     constexpr float kLn2 = 0.69314718055994531f;
-    const int r0 = qo[b], ql = qo[b + 1] - qo[b];
-    const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
-    const int n_ctx = has_ctx(p.mode) ? req_info(p, nctx[b], ql, tps).ns : 0;
+    const int lane = threadIdx.x & 31;
     const int n = n_sys + n_ctx;
-    const int d0 = (t & 31) * V;
-    for (int rr = t >> 5; rr < ql; rr += TEAM / 32) {
-        const int r = r0 + rr;
-        float M = kNegInf;
-        for (int j = 0; j < n; j++) {
-            int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-            M = fmaxf(M, __ldcg(p.part_lse + part_row(p, part, r, h)));
-        }
-        float W = 0.f, acc[V];
+    const int d0 = lane * V;
+    float M = kNegInf, W = 0.f, acc[V];
 #pragma unroll
-        for (int v = 0; v < V; v++) acc[v] = 0.f;
-        if (M != kNegInf) {
-            for (int j = 0; j < n; j++) {
-                int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-                size_t pr = part_row(p, part, r, h);
-                float w = ex2(__ldcg(p.part_lse + pr) - M);
-                W += w;
-                const float *src = p.part_o + pr * D + d0;
-                if constexpr (V == 4) {
-                    float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+    for (int v = 0; v < V; v++) acc[v] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        const int cnt = min(32, n - j0);
+        float lk = kNegInf;      // lane k: log-sum-exp of part j0 + k
+        if (lane < cnt) {
+            const int j = j0 + lane;
+            const int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
+            lk = __ldcg(p.part_lse + part_row(p, part, r, h));
+        }
+        float mk = lk;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+        if (mk == kNegInf) continue;
+        const float Mn = fmaxf(M, mk);
+        const float sc = ex2(M - Mn);          // rescale what was merged so far
+        W *= sc;
+#pragma unroll
+        for (int v = 0; v < V; v++) acc[v] *= sc;
+        M = Mn;
+        const float wk = ex2(lk - M);
+        for (int c0 = 0; c0 < cnt; c0 += CH) {
+            float x[CH][V];
+#pragma unroll
+            for (int k = 0; k < CH; k++) {
+                const int j = j0 + c0 + k;
+                if (c0 + k < cnt) {
+                    const int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
+                    const float *src = p.part_o + part_row(p, part, r, h) * D + d0;
+                    if constexpr (V == 4) {
+                        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                        x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
+                    } else {
+                        const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                        x[k][0] = t.x; x[k][1] = t.y;
+                    }
                 } else {
-                    float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
-                    acc[0] += w * x.x; acc[1] += w * x.y;
+#pragma unroll
+                    for (int v = 0; v < V; v++) x[k][v] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < CH; k++) {
+                const float w = __shfl_sync(0xffffffffu, wk, (c0 + k) & 31);
+                if (c0 + k < cnt) {
+                    W += w;
+#pragma unroll
+                    for (int v = 0; v < V; v++) acc[v] += w * x[k][v];
                 }
             }
         }
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        const float lse = W > 0.f ? (M + lg2(W)) * kLn2 : kNegInf;
-        const size_t orow = ((size_t)b * p.Lq + rr) * p.H + h;
-        if (p.mode == MODE_FUSED || p.mode == MODE_BASELINE) {
-            __half *dst = p.out + orow * D + d0;
-            if constexpr (V == 4) {
-                uint2 pk = make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
-                *reinterpret_cast<uint2 *>(dst) = pk;
-            } else {
-                *reinterpret_cast<unsigned *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
-            }
-            if (p.lse_out && (t & 31) == 0) p.lse_out[orow] = lse;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const float lse = W > 0.f ? (M + lg2(W)) * kLn2 : kNegInf;
+    const size_t orow = ((size_t)b * p.Lq + i) * p.H + h;
+    if (p.mode == MODE_FUSED || p.mode == MODE_BASELINE) {
+        __half *dst = p.out + orow * D + d0;
+        if constexpr (V == 4) {
+            *reinterpret_cast<uint2 *>(dst) =
+                make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
         } else {
-            float *dst = p.o_f32 + orow * D + d0;
-#pragma unroll
-            for (int v = 0; v < V; v++) dst[v] = acc[v] * inv;
-            if ((t & 31) == 0) p.lse_f32[orow] = lse;
+            *reinterpret_cast<unsigned *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
         }
+        if (p.lse_out && lane == 0) p.lse_out[orow] = lse;
+    } else {
+        float *dst = p.o_f32 + orow * D + d0;
+#pragma unroll
+        for (int v = 0; v < V; v++) dst[v] = acc[v] * inv;
+        if (lane == 0) p.lse_f32[orow] = lse;
     }
-}
-
-// Count one arrival for (b, h); true for the caller whose increment completed
-// the pair (it then resets the counter for the next call).
-__device__ __forceinline__ bool arrive(const Params &p, int b, int h, int target)
-{
-    unsigned old = atomicAdd(&p.arrive[b * p.H + h], 1u);
-    if ((int)old + 1 == target) {
-        p.arrive[b * p.H + h] = 0;
-        return true;
-    }
-    return false;
-}
-
-__device__ __forceinline__ int pair_target(const Params &p, const int *qo, const int *nctx, int tps, int b)
-{
-    const int r0 = qo[b], r1 = qo[b + 1];
-    int t = 0;
-    if (r1 <= r0) return 0;
-    if (has_sys(p.mode)) t += p.R_sys * ((r1 - 1) / kTileM - r0 / kTileM + 1);
-    if (has_ctx(p.mode)) {
-        ReqInfo ri = req_info(p, nctx[b], r1 - r0, tps);
-        t += ri.ns * ri.mt;
-    }
-    return t;
 }
 
 // ============================================================================= phase 1: row items
@@ -866,29 +867,6 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     ws.l[0] = ws.l[1] = 0.f;
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, rho, h, rA, rA < Mtot, rB, rB < Mtot);
-    __threadfence();
-    __syncthreads();
-
-    // arrivals of every request with rows in this tile
-    const int r0 = tau * kTileM;
-    const int r1 = min(Mtot, r0 + kTileM);
-    const int bf = find_owner(s.qo, p.B, r0), bl = find_owner(s.qo, p.B, r1 - 1);
-    if (threadIdx.x == 0) s.n_merge = 0;
-    __syncthreads();
-    for (int b = bf + threadIdx.x; b <= bl; b += kThreads) {
-        if (s.qo[b + 1] > s.qo[b] && arrive(p, b, h, pair_target(p, s.qo, s.nctx, s.tps, b))) {
-            int k = atomicAdd(&s.n_merge, 1);
-            s.merge_b[k] = b;
-        }
-    }
-    __syncthreads();
-    const int nm = s.n_merge;
-    if (nm > 0) {
-        __threadfence();
-        // one warp per completed pair
-        for (int k = warp; k < nm; k += kWarps) merge_pair<D, 32>(p, s.qo, s.nctx, s.tps, s.merge_b[k], h, lane);
-    }
-    __syncthreads();
 }
 
 // Context item of a request with several query rows (causal within the context).
@@ -938,15 +916,6 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0)
         write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, s.qo[b] + iB, iB < ql);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s.n_merge = arrive(p, b, h, pair_target(p, s.qo, s.nctx, s.tps, b)) ? 1 : 0;
-    __syncthreads();
-    if (s.n_merge) {
-        __threadfence();
-        merge_pair<D, kThreads>(p, s.qo, s.nctx, s.tps, b, h, threadIdx.x);
-    }
-    __syncthreads();
 }
 
 // ============================================================================= phase 2: decode items
@@ -1091,8 +1060,7 @@ __device__ __forceinline__ void dec_page(const __half *K, const __half *V, const
     }
 }
 
-// Finish a decode item: write its partial and count its arrival; the warp that
-// completes the pair merges it.
+// Finish a decode item: write its partial (normalised output, log2-sum-exp).
 template <int D>
 __device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem<D> &it, DecState<D> &st)
 {
@@ -1114,15 +1082,6 @@ __device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem<D>
         }
     }
     if (lane == 0) __stcg(p.part_lse + pr, L > 0.f ? st.m + lg2(L) : kNegInf);
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = arrive(p, it.b, it.h, pair_target(p, s.qo, s.nctx, s.tps, it.b)) ? 1 : 0;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-        __threadfence();
-        merge_pair<D, 32>(p, s.qo, s.nctx, s.tps, it.b, it.h, lane);
-    }
 }
 
 // Phase 2 for one warp: pull decode items until the queue is empty, streaming
@@ -1219,6 +1178,12 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(smem_raw);
 
     build_schedule<D>(p, s);
+    if (blockIdx.x == 0) {
+        // hand the schedule to the merge kernel; tps < 0 tells it to do nothing
+        for (int k = threadIdx.x; k <= p.B; k += kThreads) p.sched[1 + k] = s.qo[k];
+        for (int k = threadIdx.x; k < p.B; k += kThreads) p.sched[2 + p.B + k] = s.nctx[k];
+        if (threadIdx.x == 0) p.sched[0] = s.bad ? -1 : s.tps;
+    }
     if (s.bad) {
         if (threadIdx.x == 0) atomicOr(&p.ctrl[CTRL_FLAGS], (unsigned)s.bad);
         return;    // counters untouched: nothing was scheduled
@@ -1241,6 +1206,8 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     // phase 2: decode items, each warp on its own
     if (n_dec > 0) decode_phase<D>(p, s, n_dec);
     __syncthreads();
+    // this CTA's partials are written: the merge kernel may be launched
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // the last CTA out resets the queues for the next launch
     if (threadIdx.x == 0) {
@@ -1253,6 +1220,31 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
             __threadfence();
         }
     }
+}
+
+// ============================================================================= merge kernel
+// One warp per (row, head): combines the row's system partials and context
+// partials.  Launched as a programmatic dependent of relay_kernel: it waits
+// for that grid (and its memory) before reading anything it wrote.
+template <int D>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
+{
+    __shared__ int qo[kMaxB + 1];
+    __shared__ int nctx[kMaxB];
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    const int tps = p.sched[0];
+    if (tps < 0) return;                 // the producer rejected its inputs
+    for (int k = threadIdx.x; k <= p.B; k += blockDim.x) qo[k] = p.sched[1 + k];
+    for (int k = threadIdx.x; k < p.B; k += blockDim.x) nctx[k] = p.sched[2 + p.B + k];
+    __syncthreads();
+    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int r = w / p.H, h = w % p.H;
+    if (r >= qo[p.B]) return;
+    const int b = find_owner(qo, p.B, r);
+    const int ql = qo[b + 1] - qo[b];
+    const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
+    const int n_ctx = has_ctx(p.mode) ? req_info(p, nctx[b], ql, tps).ns : 0;
+    merge_row<D>(p, r, b, r - qo[b], h, n_sys, n_ctx);
 }
 
 // ============================================================================= stand-alone relay fusion
