@@ -102,8 +102,9 @@ typedef struct {
 } relay_dims_t;
 
 /* Bytes of workspace any entry point below needs for `dims` (0 if `dims` is
- * invalid).  The workspace holds fp32 partial results of the work items and
- * a few counters.  It must be zero-filled once when first allocated (or by
+ * invalid).  The workspace holds fp32 partial results of the work items, the
+ * schedule handed from the first kernel to the merge kernel, and the work
+ * queue counters.  It must be zero-filled once when first allocated (or by
  * relay_workspace_init); every call leaves its counters at zero again.
  * Calls that share one workspace must be ordered (same stream, or events). */
 size_t relay_workspace_size(const relay_dims_t *dims);
@@ -140,12 +141,16 @@ relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const fl
                           const float *o_ctx, const float *lse_ctx, const int32_t *q_lens,
                           void *out, float *lse_out, relay_stream_t stream);
 
-/* All three steps in ONE launch: a persistent grid works through system
- * items (one head, a range of system keys, 64 query rows) and context items
- * (one request, one head, a range of its context); each item leaves an fp32
- * partial result with its log-sum-exp, and the item that completes a
- * (request, head) merges all of that pair's partials into `out` (fp16) and
- * `lse_out` (fp32 natural log, nullable). */
+/* All three steps, queued as two kernels on `stream` (the second launched
+ * as a programmatic dependent of the first, so both fit in one CUDA graph):
+ *  1. a persistent grid (one CTA per SM) works through system items (one
+ *     head, a range of system keys, up to 128 query rows of the batch: the
+ *     system KV is streamed once per batch) and context items (one request,
+ *     one head, a range of its paged context); each item writes an fp32
+ *     partial result and its log-sum-exp to the workspace;
+ *  2. a merge kernel combines each (row, head)'s partials -- the system
+ *     ranges and the context splits -- into `out` (fp16) and `lse_out` (fp32
+ *     natural log, nullable): the relay fusion, over any number of parts. */
 relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
                                       const void *sys_k, const void *sys_v,
                                       const void *k_cache, const void *v_cache,
