@@ -172,6 +172,39 @@ relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q,
                                      const int32_t *q_lens, void *out, float *lse_out,
                                      void *ws, size_t ws_bytes, relay_stream_t stream);
 
+/* Maximum scratch of relay_attention_decode_noalloc, in bytes. */
+#define RELAY_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* relay_attention_decode for callers that cannot allocate device memory at
+ * the point of the call -- for example a serving process whose own pool
+ * allocator owns all device memory and forbids outside allocations, or a
+ * latency-critical decode loop that must not reach cudaMalloc (which can
+ * synchronise the device).  The paper has no counterpart: this is a
+ * packaging of the same computation.
+ *
+ * Same arguments as relay_attention_decode except the workspace: the
+ * scratch (partials, schedule, queue counters) lives in one fixed buffer of
+ * RELAY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library keeps until the process exits.  Nothing is allocated or
+ * freed, by the library or by any library it calls.
+ *  - Shapes whose workspace (relay_workspace_size) exceeds the buffer are
+ *    rejected with RELAY_ERR_WORKSPACE before anything is queued.
+ *  - The first call on a device looks up the buffer's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call queues a zero-fill of the buffer's counter header, then the
+ *    two kernels.  All calls share the one buffer, which keeps the last
+ *    call's contents: calls that may overlap on the GPU (other streams, other
+ *    host threads) race and must be serialised by the caller.
+ *  - Device-side check flags land in the shared buffer and are cleared by the
+ *    next call; callers that need relay_device_status use
+ *    relay_attention_decode with their own workspace. */
+relay_status_t relay_attention_decode_noalloc(const relay_dims_t *dims, const void *q,
+                                              const void *sys_k, const void *sys_v,
+                                              const void *k_cache, const void *v_cache,
+                                              const int32_t *block_tables, const int32_t *ctx_lens,
+                                              const int32_t *q_lens, void *out, float *lse_out,
+                                              relay_stream_t stream);
+
 /* Read and clear the device-side check flags of a workspace.  SYNCHRONOUS:
  * waits for `stream`.  *flags_out (host pointer, nullable) receives the
  * RELAY_FLAG_* mask.  Returns RELAY_ERR_DEVICE_CHECK if any flag was set. */
