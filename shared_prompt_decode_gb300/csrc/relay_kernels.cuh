@@ -53,7 +53,10 @@ constexpr int kBlock = 16;      // paged block size (tokens)
 constexpr int kWarps = RELAY_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileK = 64;      // keys per stage in phase 1
-constexpr int kTileM = 16 * kWarps;   // query rows per phase-1 item
+constexpr int kRowWarps = kWarps / 2;         // warps of a row team (phase-1 items); two teams per CTA
+constexpr int kTeams = kWarps / kRowWarps;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kTileM = 16 * kRowWarps;        // query rows per phase-1 item
 constexpr int kRingBytes = RELAY_RING_KB * 1024;
 constexpr int kMaxB = 512;
 
@@ -87,8 +90,12 @@ struct Params {
 
 template <int D>
 struct Smem {
+    // row team t's ring is the t-th half of the staging memory, which holds
+    // the decode rings of the team's own warps, so a team that moves on to
+    // decode items never disturbs the other team's row item
     static constexpr int kStageC = kTileK * D * 2 * 2;        // bytes of one phase-1 stage (K + V)
-    static constexpr int kStagesC = kRingBytes / kStageC < 8 ? kRingBytes / kStageC : 8;   // phase-1 ring depth
+    static constexpr int kRowRing = kRingBytes / kTeams;
+    static constexpr int kStagesC = kRowRing / kStageC < 8 ? kRowRing / kStageC : 8;   // phase-1 ring depth
     static constexpr int kStageW = kBlock * D * 2 * 2;        // bytes of one page (K + V)
     static constexpr int kStagesW =
         kRingBytes / (kWarps * kStageW) < 6 ? kRingBytes / (kWarps * kStageW) : 6;   // per-warp ring depth
@@ -103,11 +110,11 @@ struct Smem {
     int n_dec_req;
     int tps;                  // pages per decode item chosen for this launch
     int warp_tot[kWarps];
-    int item;
+    int item[kTeams];
     int bad;
 
-    __device__ __half *ck(int st) { return reinterpret_cast<__half *>(ring + st * kStageC); }
-    __device__ __half *cv(int st) { return ck(st) + kTileK * D; }
+    __device__ __half *ck(int team, int st) { return reinterpret_cast<__half *>(ring + team * kRowRing + st * kStageC); }
+    __device__ __half *cv(int team, int st) { return ck(team, st) + kTileK * D; }
     __device__ __half *wk(int w, int st) { return reinterpret_cast<__half *>(ring + (w * kStagesW + st) * kStageW); }
     __device__ __half *wv(int w, int st) { return wk(w, st) + kBlock * D; }
 };
@@ -187,6 +194,14 @@ __device__ __forceinline__ unsigned ld_u32(const __half *p)
 }
 
 #define kNegInf (-__int_as_float(0x7f800000))
+
+// index of this thread's row team, and the team's barrier (named barrier
+// 1 + team over the team's kRowThreads threads; the other team goes on)
+__device__ __forceinline__ int team_of() { return (threadIdx.x >> 5) / kRowWarps; }
+__device__ __forceinline__ void team_sync()
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(1 + team_of()), "n"(kRowThreads) : "memory");
+}
 
 // swizzled element offset of (row, 16-byte chunk) in a [rows][D] fp16 tile
 template <int D>
@@ -528,12 +543,12 @@ __device__ __forceinline__ void load_tile(Smem<D> &s, int st, const KeySrc &src,
                                           unsigned *flags)
 {
     constexpr int CPR = D / 8;                      // 16-byte chunks per row
-    constexpr int PER = kTileK * CPR / kThreads;    // chunks per thread
-    const int tid = threadIdx.x;
-    __half *K = s.ck(st), *V = s.cv(st);
+    constexpr int PER = kTileK * CPR / kRowThreads; // chunks per team thread
+    const int tid = threadIdx.x % kRowThreads;
+    __half *K = s.ck(team_of(), st), *V = s.cv(team_of(), st);
 #pragma unroll
     for (int k = 0; k < PER; k++) {
-        int c = tid + k * kThreads;
+        int c = tid + k * kRowThreads;
         int key = c / CPR, ch = c % CPR;
         int t = key0 + key;
         size_t off = 0;
@@ -689,14 +704,16 @@ __device__ __forceinline__ void row_pipeline(Smem<D> &s, const KeySrc &src, int 
     const int n_tiles = (key_hi > key0) ? (key_hi - key0 + kTileK - 1) / kTileK : 0;
     for (int j = 0; j < n_tiles; j++) {
         cp_async_wait<S - 2>();
-        __syncthreads();
+        team_sync();
         int jn = j + S - 1;
         if (jn < n_tiles) load_tile<D>(s, jn % S, src, key0 + jn * kTileK, key_hi, flags);
         cp_async_commit();
-        if (active) row_tile<D, NT>(s.ck(j % S), s.cv(j % S), kb, qf, ws, key0 + j * kTileK, end0, end1, scale_log2);
+        if (active)
+            row_tile<D, NT>(s.ck(team_of(), j % S), s.cv(team_of(), j % S), kb, qf, ws, key0 + j * kTileK, end0, end1,
+                            scale_log2);
     }
     cp_async_wait<0>();
-    __syncthreads();
+    team_sync();
 }
 
 template <int D>
@@ -765,9 +782,9 @@ __device__ __forceinline__ RowRoles row_roles(int rows)
     const int RG = (rows + 15) / 16;
     int np2 = 1;
     while (np2 < RG) np2 <<= 1;
-    r.KG = min(kWarps / np2, kTileK / 8);
-    r.RGp = kWarps / r.KG;
-    const int warp = threadIdx.x >> 5;
+    r.KG = min(kRowWarps / np2, kTileK / 8);
+    r.RGp = kRowWarps / r.KG;
+    const int warp = (threadIdx.x >> 5) % kRowWarps;
     r.rg = warp % r.RGp;
     r.kg = warp / r.RGp;
     r.active = r.rg < RG && r.kg < r.KG;
@@ -790,8 +807,8 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
     if (rr.KG == 1) return;
     // combine the key groups' states into the kg == 0 warps (ring is idle now)
     constexpr int PL = D / 2 + 4;            // floats per lane
-    float *red = reinterpret_cast<float *>(s.ring);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float *red = reinterpret_cast<float *>(s.ring + team_of() * Smem<D>::kRowRing);
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) % kRowWarps;
     if (rr.active && rr.kg > 0) {
         float *mine = red + warp * PL * 32;
 #pragma unroll
@@ -803,7 +820,7 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
         mine[(D / 2 + 2) * 32 + lane] = ws.l[0];
         mine[(D / 2 + 3) * 32 + lane] = ws.l[1];
     }
-    __syncthreads();
+    team_sync();
     if (rr.active && rr.kg == 0) {
         for (int k = 1; k < rr.KG; k++) {
             const float *oth = red + (warp + k * rr.RGp) * PL * 32;
@@ -824,7 +841,7 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
             }
         }
     }
-    __syncthreads();
+    team_sync();
 }
 
 template <int D>
@@ -1194,14 +1211,19 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     const int n_rows = n_sys + s.mq[p.B];
     const int n_dec = s.dec[s.n_dec_req];
 
-    // phase 1: row items, the whole CTA per item (the first one is static)
-    for (int item = blockIdx.x; item < n_rows;) {
-        if (item < n_sys) sys_item<D>(p, s, item, Mtot);
-        else mq_item<D>(p, s, item - n_sys);
-        if (threadIdx.x == 0) s.item = (int)(gridDim.x + atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u));
-        __syncthreads();
-        item = s.item;
-        __syncthreads();
+    // phase 1: row items, two independent row teams per CTA (first items
+    // static); a team with no row item starts on decode items at once
+    {
+        const int team = team_of();
+        const bool leader = (threadIdx.x % kRowThreads) == 0;
+        for (int item = blockIdx.x + team * gridDim.x; item < n_rows;) {
+            if (item < n_sys) sys_item<D>(p, s, item, Mtot);
+            else mq_item<D>(p, s, item - n_sys);
+            if (leader) s.item[team] = (int)(kTeams * gridDim.x + atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u));
+            team_sync();
+            item = s.item[team];
+            team_sync();
+        }
     }
     // phase 2: decode items, each warp on its own
     if (n_dec > 0) decode_phase<D>(p, s, n_dec);
