@@ -186,6 +186,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.ctx_base = pl.ctx_base;
     p.tps_min = pl.tps_min;
     p.tps_max = pl.tps_max;
+    p.c_max = pl.C_max;
     p.mode = mode;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -85,6 +85,7 @@ struct Params {
     float *part_lse;                  // [n_parts][max_q_total][H]  (log2 domain)
     int R_sys, sys_range, ctx_split, ctx_base;   // ctx_base: first partial slot of context parts
     int tps_min, tps_max;             // pages per decode item: bounds of the adaptive choice
+    int c_max;                        // context partial slots per row (workspace layout)
     int mode;
 };
 
@@ -311,7 +312,7 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
 {
     constexpr int PER = (kMaxB + kThreads - 1) / kThreads;
     constexpr int kClasses = 33;                  // item sizes 0..32 pages
-    constexpr int kItemsPerWarp = 8;
+    constexpr int kItemsPerWarp = 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int vq[PER], vm[PER], vp[PER], nn[PER];
     unsigned flags = 0;
@@ -422,7 +423,8 @@ __device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int
 // round trip), then the parts' output rows are loaded eight at a time with
 // all eight loads in flight together.  Lane t handles D/32 adjacent elements.
 template <int D>
-__device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx)
+__device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx,
+                          bool have_lk0 = false, float lk0 = 0.f)
 {
     constexpr int V = D / 32;
     constexpr int CH = 8;
@@ -436,7 +438,9 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
     for (int j0 = 0; j0 < n; j0 += 32) {
         const int cnt = min(32, n - j0);
         float lk = kNegInf;      // lane k: log-sum-exp of part j0 + k
-        if (lane < cnt) {
+        if (j0 == 0 && have_lk0) {
+            lk = lane < cnt ? lk0 : kNegInf;
+        } else if (lane < cnt) {
             const int j = j0 + lane;
             const int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
             lk = __ldcg(p.part_lse + part_row(p, part, r, h));
@@ -1111,15 +1115,20 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // the first ticket of every warp is static; later ones come from the queue
+    // The first two tickets of every warp are static (no warp starts by
+    // queueing on the counter with all the others); later ones come from the
+    // queue, requested one item ahead.
+    const unsigned n_w = gridDim.x * kWarps;
     unsigned ticket = blockIdx.x * kWarps + warp;
+    int taken = 0;
     auto request = [&]() {      // ask for a ticket; its value is read later
-        if (lane == 0) ticket = gridDim.x * kWarps + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
+        if (lane == 0) ticket = 2 * n_w + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
     };
     auto take = [&](DecItem<D> &it) {
         int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
         dec_item<D>(p, s, id, n_dec, it);
-        if (it.id >= 0) request();
+        if (++taken == 1) ticket = n_w + blockIdx.x * kWarps + warp;
+        else if (it.id >= 0) request();
     };
 
     DecItem<D> cur, nxt;
@@ -1254,6 +1263,32 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     __shared__ int qo[kMaxB + 1];
     __shared__ int nctx[kMaxB];
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (p.q_lens == nullptr) {
+        // every request has Lq rows: row r is row r % Lq of request r / Lq, so
+        // no schedule table is needed; the request's context length, the
+        // split size and the log-sum-exps of every slot the row may use are
+        // loaded together (one round trip)
+        const int lane = threadIdx.x & 31;
+        const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const int r = w / p.H, h = w % p.H;
+        if (r >= p.B * p.Lq) return;
+        const int b = r / p.Lq;
+        const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
+        const int ncand = n_sys + (has_ctx(p.mode) ? p.c_max : 0);
+        if (ncand <= 32) {
+            float lk = kNegInf;
+            if (lane < ncand) {
+                const int part = lane < n_sys ? lane : p.ctx_base + (lane - n_sys);
+                lk = __ldcg(p.part_lse + part_row(p, part, r, h));
+            }
+            const int tps = __ldcg(p.sched);
+            const int nc = has_ctx(p.mode) ? __ldg(p.ctx_lens + b) : 0;
+            if (tps < 0) return;
+            const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
+            merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, true, lk);
+            return;
+        }
+    }
     const int tps = p.sched[0];
     if (tps < 0) return;                 // the producer rejected its inputs
     for (int k = threadIdx.x; k <= p.B; k += blockDim.x) qo[k] = p.sched[1 + k];
