@@ -12,7 +12,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "librelay.so")
 SOURCES = [os.path.join(CSRC, "relay.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "relay_kernels.cuh"), os.path.join(INCLUDE, "relay.h")]
+DEPS = SOURCES + [os.path.join(CSRC, "relay_kernels.cuh"), os.path.join(CSRC, "sys_tc.cuh"),
+                  os.path.join(INCLUDE, "relay.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -14,6 +14,7 @@
 
 #include "relay.h"
 #include "relay_kernels.cuh"
+#include "sys_tc.cuh"
 
 namespace {
 
@@ -28,6 +29,11 @@ struct DevInfo {
     int sms = 0;
     int occ64 = 0, occ128 = 0;
 };
+
+// Batches with more query rows per head than this run the system step on the
+// tensor cores (tcgen05), where it is compute-bound; below it the step stays
+// inside the streaming kernel, where it is memory-bound and overlaps context.
+constexpr int kTcMinRows = 256;
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -56,6 +62,11 @@ relay_status_t device_info(const DevInfo **out)
             return RELAY_ERR_CUDA;
         }
         if (d.occ64 < 1 || d.occ128 < 1) return RELAY_ERR_CUDA;
+        if (cudaFuncSetAttribute(tc::sys_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemTC) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return RELAY_ERR_CUDA;
+        }
         d.ready = true;
     }
     *out = &d;
@@ -85,6 +96,7 @@ struct Plan {
     int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
     int n_parts = 0, ctx_base = 0, n_prefix = 0;
     int tps_min = 32, tps_max = 32;
+    bool tc = false;          // system step on the tensor-core kernel
     size_t off_sched = 0, off_part_o = 0, off_part_lse = 0, total = 0;
 };
 
@@ -98,7 +110,17 @@ Plan make_plan(const relay_dims_t *d, int mode)
     const bool sys = mode == MODE_FUSED || mode == MODE_SYS;
     const bool ctx = mode != MODE_SYS;
     pl.n_prefix = mode == MODE_BASELINE ? d->Ls : 0;
-    if (sys) {
+    pl.tc = sys && d->D == 128 && d->Ls > 0 && pl.Mtot > kTcMinRows;
+    if (pl.tc) {
+        // enough (head, 128-row tile, key range) items for ~4 waves of CTAs,
+        // ranges of at least 2048 keys so the partials stay small
+        const int tiles = (pl.Mtot + tc::kRowsTC - 1) / tc::kRowsTC;
+        int r = (4 * kGridTarget + d->H * tiles - 1) / (d->H * tiles);
+        r = std::max(1, std::min(r, d->Ls / 2048));
+        int range = d->sys_range > 0 ? d->sys_range : round_up((d->Ls + r - 1) / r, kTileK);
+        pl.sys_range = range;
+        pl.R_sys = (d->Ls + range - 1) / range;
+    } else if (sys) {
         if (d->Ls > 0) {
             int range = d->sys_range;
             if (range == 0) {
@@ -187,9 +209,33 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.tps_min = pl.tps_min;
     p.tps_max = pl.tps_max;
     p.c_max = pl.C_max;
+    p.skip_sys = pl.tc ? 1 : 0;
     p.mode = mode;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.tc) {
+        // system partials from the tensor cores: one CTA per (head, tile, range)
+        tc::TcParams t{};
+        t.B = d->B;
+        t.Lq = d->Lq;
+        t.H = d->H;
+        t.Ls = d->Ls;
+        t.max_q_total = pl.Mtot;
+        t.scale_log2 = p.scale_log2;
+        t.q = p.q;
+        t.sys_k = p.sys_k;
+        t.sys_v = p.sys_v;
+        t.q_lens = p.q_lens;
+        t.flags = p.ctrl;
+        t.part_o = p.part_o;
+        t.part_lse = p.part_lse;
+        t.R = pl.R_sys;
+        t.range = pl.sys_range;
+        const long long tiles = (pl.Mtot + tc::kRowsTC - 1) / tc::kRowsTC;
+        const long long items = tiles * d->H * pl.R_sys;
+        tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(t);
+        if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
+    }
     if (d->D == 128) {
         relay_kernel<128><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
     } else {

@@ -86,6 +86,7 @@ struct Params {
     int R_sys, sys_range, ctx_split, ctx_base;   // ctx_base: first partial slot of context parts
     int tps_min, tps_max;             // pages per decode item: bounds of the adaptive choice
     int c_max;                        // context partial slots per row (workspace layout)
+    int skip_sys;                     // system partials come from the tensor-core kernel
     int mode;
 };
 
@@ -1216,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     }
     const int Mtot = s.qo[p.B];
     const int T = (Mtot + kTileM - 1) / kTileM;
-    const int n_sys = has_sys(p.mode) ? p.H * p.R_sys * T : 0;
+    const int n_sys = (has_sys(p.mode) && !p.skip_sys) ? p.H * p.R_sys * T : 0;
     const int n_rows = n_sys + s.mq[p.B];
     const int n_dec = s.dec[s.n_dec_req];
 

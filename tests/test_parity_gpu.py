@@ -312,3 +312,32 @@ def test_device_checks_flag_bad_values(what):
     ws2 = ws if relay.workspace_size(dims2) <= ws.numel() else relay.make_workspace(dims2)
     out2, lse2 = T.run_fused(case2, ws=ws2)
     T.check_full(case2, out2, lse2)
+
+
+# ----------------------------------------------------------------------------- tensor-core system step
+# Batches with more than 256 query rows per head run the system step on the
+# tcgen05 kernel (128-row tiles, 64-key tiles); ragged rows and keys on purpose.
+TC_CASES = [
+    ("rows257_keys1000", 257, 1, 1000, None),
+    ("rows300_keys64", 300, 1, 64, None),
+    ("rows600_keys4097", 150, 4, 4097, None),
+    ("chunks_qlens", 6, 128, 700, [128, 1, 77, 128, 3, 90]),
+]
+
+
+@pytest.mark.parametrize("name,B,Lq,Ls,ql", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_tensor_core_system_step(name, B, Lq, Ls, ql):
+    w = synth.Workload(name, B=B, H=3, D=128, Ls=Ls, ctx_dist=("uniform", 0, 48), value_scale=0.5, Lq=Lq)
+    case = synth.make_case(w, 31, q_lens=ql)
+    if ql is not None:
+        case.ctx_lens[:] = torch.maximum(case.ctx_lens, case.q_lens)
+        case = synth.make_case(w, 31, ctx_lens=[int(x) for x in case.ctx_lens], q_lens=ql)
+    assert case.total_q() > 256
+    o_s, l_s, o_c, l_c, out2, lse2 = T.run_split(case)
+    ref_s, refl_s = oracle.attention_full(case, "sys")
+    m = T.valid_mask(case)
+    T.check(o_s, ref_s, "o_sys", m)
+    T.check(l_s, refl_s, "lse_sys", m)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+    T.check_full(case, out2, lse2)
