@@ -79,6 +79,8 @@ typedef enum {
 #define RELAY_FLAG_BAD_CTX_LEN  2u  /* ctx_lens[b] outside [0, 16*max_blocks_per_seq] */
 #define RELAY_FLAG_BAD_BLOCK    4u  /* a block id outside [0, num_blocks) */
 #define RELAY_FLAG_Q_TOTAL      8u  /* sum of q_lens above max_q_total */
+#define RELAY_FLAG_WAIT_TIMEOUT 16u  /* a bounded wait inside the tensor-core system step gave up;
+                                       that call's outputs are not valid */
 
 /* Opaque CUDA stream (binary-compatible with cudaStream_t); NULL = legacy stream. */
 typedef struct CUstream_st *relay_stream_t;

@@ -5,6 +5,7 @@
 // (relay_device_status excepted), no state beyond a per-device cache of the
 // SM count and the kernels' occupancy.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <climits>
@@ -91,6 +92,41 @@ relay_status_t check_dims(const relay_dims_t *d)
     return RELAY_OK;
 }
 
+int tc_pairs(int Mtot) { return ((Mtot + tc::kRowsTC - 1) / tc::kRowsTC + 1) / 2; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library links only the CUDA runtime).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// sys_k or sys_v, [Ls][H][128] fp16, as a 3-D tensor (d, head, key) read in
+// {64, 1, 64} boxes with 128-byte swizzle; keys past Ls read as zero.
+bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)Ls};
+    const cuuint64_t strides[2] = {128 * sizeof(__half), (cuuint64_t)H * 128 * sizeof(__half)};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)tc::kKeysTC};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
     int Mtot = 0;
     int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
@@ -112,12 +148,26 @@ Plan make_plan(const relay_dims_t *d, int mode)
     pl.n_prefix = mode == MODE_BASELINE ? d->Ls : 0;
     pl.tc = sys && d->D == 128 && d->Ls > 0 && pl.Mtot > kTcMinRows;
     if (pl.tc) {
-        // enough (head, 128-row tile, key range) items for ~4 waves of CTAs,
-        // ranges of at least 2048 keys so the partials stay small
-        const int tiles = (pl.Mtot + tc::kRowsTC - 1) / tc::kRowsTC;
-        int r = (4 * kGridTarget + d->H * tiles - 1) / (d->H * tiles);
-        r = std::max(1, std::min(r, d->Ls / 2048));
-        int range = d->sys_range > 0 ? d->sys_range : round_up((d->Ls + r - 1) / r, kTileK);
+        // (head, tile pair, key range) items, one CTA each.  The number of
+        // ranges R minimises the makespan in waves of one CTA per SM times
+        // keys per range, ceil(n R / SMs) / R, among ranges of at least
+        // 2048 keys (so the partials stay small); the smallest R within 2%
+        // of the best wins.
+        const long long n = (long long)tc_pairs(pl.Mtot) * d->H;
+        const int r_cap = std::max(1, d->Ls / 2048);
+        double best = 1e30;
+        int r_best = 1;
+        for (int r = 1; r <= r_cap; r++) {
+            const double cost = (double)((n * r + kGridTarget - 1) / kGridTarget) / r;
+            if (cost < best) best = cost;
+        }
+        for (int r = 1; r <= r_cap; r++) {
+            if ((double)((n * r + kGridTarget - 1) / kGridTarget) / r <= best * 1.02) {
+                r_best = r;
+                break;
+            }
+        }
+        int range = d->sys_range > 0 ? d->sys_range : round_up((d->Ls + r_best - 1) / r_best, tc::kKeysTC);
         pl.sys_range = range;
         pl.R_sys = (d->Ls + range - 1) / range;
     } else if (sys) {
@@ -223,17 +273,18 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.max_q_total = pl.Mtot;
         t.scale_log2 = p.scale_log2;
         t.q = p.q;
-        t.sys_k = p.sys_k;
-        t.sys_v = p.sys_v;
         t.q_lens = p.q_lens;
         t.flags = p.ctrl;
         t.part_o = p.part_o;
         t.part_lse = p.part_lse;
         t.R = pl.R_sys;
         t.range = pl.sys_range;
-        const long long tiles = (pl.Mtot + tc::kRowsTC - 1) / tc::kRowsTC;
-        const long long items = tiles * d->H * pl.R_sys;
-        tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(t);
+        t.pairs = tc_pairs(pl.Mtot);
+        CUtensorMap tmK, tmV;
+        if (!encode_sys_map(&tmK, p.sys_k, d->H, d->Ls) || !encode_sys_map(&tmV, p.sys_v, d->H, d->Ls))
+            return RELAY_ERR_CUDA;
+        const long long items = (long long)t.pairs * d->H * pl.R_sys;
+        tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
     if (d->D == 128) {
