@@ -11,25 +11,32 @@
 //                   lives in TMEM lane t and is owned by thread t, so the
 //                   online softmax needs no cross-thread reduction
 //   warp 8          streams 64-key K and V stages in with TMA (128-byte
-//                   swizzle, zero fill past the end of the prompt)
-//   warp 9          owns TMEM and issues every MMA from one thread
+//                   swizzle, zero fill past the end of the prompt), K and V
+//                   on rings of their own
+//   warp 9          owns TMEM and issues the S MMAs from one thread
+//   warp 10         issues the PV MMAs from one thread
 // Per 64-key stage j and query tile:
-//   S = Q K^T        tcgen05.mma kind::f16, M=128 N=64, both operands K-major
-//                    in shared memory, fp32 into TMEM S buffer j % 2
-//   P = exp2(S - m)  by the tile's warpgroup, fp16, stored over the first 32
-//                    columns of the same S buffer
-//   O += P V         tcgen05.mma with P read from TMEM and V read from shared
-//                    memory in its natural [key][d] order (MN-major), so V is
-//                    never transposed
-// The MMA thread issues S(j) for both tiles before PV(j-1) of both, so each
-// warpgroup computes its softmax while the tensor cores run the other tile's
-// work.  An S buffer is rewritten only after the PV that read its P has
-// completed.  O is rescaled only when a row's running maximum grows by more
-// than 2^8 (P <= 256 otherwise, well inside fp16).  Every wait is bounded in
-// time; a wait that gives up raises RELAY_FLAG_WAIT_TIMEOUT and the CTA drains
-// its copies and MMAs before it frees TMEM and leaves.  Each row's result is
-// one fp32 partial (normalised output and log2-sum-exp), merged later with
-// the context partials.
+//   S = Q K^T        tcgen05.mma kind::f16, M=128 N=64, Q and K K-major in
+//                    shared memory, fp32 into TMEM S buffer j % 2
+//   P = exp2(S - m)  by the tile's warpgroup, fp16, into shared-memory P
+//                    buffer j % 2
+//   O += P V         tcgen05.mma, M=128 N=128: P and V from shared memory, V
+//                    in its natural [key][d] order (MN-major), never transposed
+// The S thread runs two stages ahead of the PV thread: S(j+2) is issued
+// while PV(j) is.  S and P are double-buffered, so every hand-off between an
+// MMA thread and a warpgroup has a full stage of slack: a warpgroup frees an
+// S buffer as soon as it has read it, and refills a P buffer once the PV two
+// stages back has completed.  A thread that has MMAs in flight waits for them
+// to drain before its next shared-memory read completes, so a barrier check
+// on the issuing thread empties the tensor pipe; with S and PV issued from
+// two threads, one thread's checks overlap the other's MMAs.
+// Each barrier signalled per stage has one instance per buffer, so that no
+// parity wait can be two phases behind.  O is rescaled only when a row's
+// running maximum grows by more than 2^8 (P <= 256 otherwise, well inside
+// fp16).  Every wait is bounded in time; a wait that gives up raises
+// RELAY_FLAG_WAIT_TIMEOUT and the CTA drains its copies and MMAs before it
+// frees TMEM and leaves.  Each row's result is one fp32 partial (normalised
+// output and log2-sum-exp), merged later with the context partials.
 #pragma once
 
 #include <cuda.h>
@@ -42,28 +49,32 @@ namespace tc {
 
 constexpr int kRowsTC = 128;          // query rows per tile (TMEM lanes)
 constexpr int kKeysTC = 64;           // keys per K/V stage
-constexpr int kStagesTC = 4;          // K/V ring depth
-constexpr int kWarpLoad = 8, kWarpMma = 9;
-constexpr int kThreadsTC = 320;
+constexpr int kStagesK = 3, kStagesV = 2;
+constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
+constexpr int kThreadsTC = 352;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // give up on a wait after 1 s
 
 // shared-memory map (byte offsets from a 1024-aligned base), D = 128
 constexpr int kHalfQ = kRowsTC * 128;             // one d-half of a Q tile: [128 rows][64 d] fp16 = 16 KB
 constexpr int kQTile = 2 * kHalfQ;                // 32 KB
+constexpr int kPBuf = kRowsTC * kKeysTC * 2;      // one P buffer: [128 rows][64 keys] fp16 = 16 KB
 constexpr int kHalfKV = kKeysTC * 128;            // one d-half of a K or V stage: [64 keys][64 d] = 8 KB
-constexpr int kStageBytes = 4 * kHalfKV;          // K half 0, K half 1, V half 0, V half 1
+constexpr int kStageBytes = 2 * kHalfKV;          // a K stage or a V stage: two d-halves
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + 2 * kQTile;
-constexpr int kOffBar = kOffStage + kStagesTC * kStageBytes;
-constexpr int kNumBars = 24;
+constexpr int kOffP = kOffQ + 2 * kQTile;         // [tile][buffer]
+constexpr int kOffK = kOffP + 4 * kPBuf;
+constexpr int kOffV = kOffK + kStagesK * kStageBytes;
+constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
+constexpr int kNumBars = 32;
 constexpr int kSmemTC = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
-constexpr int kTmemCols = 512;        // O tile 0 | O tile 1 | S tile 0 (2 x 64) | S tile 1 (2 x 64)
+// TMEM columns: O tile 0 | O tile 1 | S tile 0 (2 buffers) | S tile 1 (2 buffers)
+constexpr int kTmemCols = 512;
+constexpr unsigned kColO = 0, kColS = 256;
 
 // mbarrier slots
-constexpr int kBarKFull = 0, kBarVFull = 4, kBarEmpty = 8;    // per stage
-constexpr int kBarSFull = 12, kBarPFull = 16;                 // per (tile, S buffer)
-constexpr int kBarODone = 20;                                 // per tile
-constexpr int kBarQFull = 22, kBarFin = 23;
+constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6, kBarVEmpty = 8;       // per stage
+constexpr int kBarSFull = 10, kBarSFree = 14, kBarPFull = 18, kBarODone = 22;    // per (tile, buffer)
+constexpr int kBarQFull = 26, kBarFin = 27;
 
 // --------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count)
@@ -80,6 +91,16 @@ __device__ __forceinline__ bool mbar_try(unsigned bar, unsigned parity)
     return ok != 0;
 }
 
+// Non-blocking test of completion `parity`.
+__device__ __forceinline__ bool mbar_test(unsigned bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns()
 {
     unsigned long long t;
@@ -91,7 +112,7 @@ __device__ __forceinline__ unsigned long long global_ns()
 // role has raised *abort, or after kWaitNs, raising *abort itself.
 __device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity, volatile int *abort)
 {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
 #pragma unroll 1
@@ -244,6 +265,8 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
     return lo;
 }
 
+
+
 // blockIdx.x = (range * pairs + pair) * H + h.  tmK / tmV view sys_k / sys_v
 // as [Ls][H][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -254,7 +277,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     __shared__ unsigned tmem_base_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned sbase = (static_cast<unsigned>(__cvta_generic_to_shared(smem_raw)) + 1023u) & ~1023u;
+    const unsigned sraw = static_cast<unsigned>(__cvta_generic_to_shared(smem_raw));
+    const unsigned sbase = (sraw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (sbase - sraw);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (unsigned)i; };
     volatile int *abort_p = &abort_sh;
 
@@ -281,35 +306,40 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int key_hi = min(key0 + p.range, p.Ls);
     const int n_tiles = key_hi > key0 ? (key_hi - key0 + kKeysTC - 1) / kKeysTC : 0;
 
-    if (warp == kWarpMma) {
+    if (warp == kWarpMmaS) {
         const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(&tmem_base_sh));
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst), "n"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
     if (tid == 0) {
-        for (int s = 0; s < kStagesTC; s++) {
+        for (int s = 0; s < kStagesK; s++) {
             mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < kStagesV; s++) {
             mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarEmpty + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
         }
-        for (int i = 0; i < 4; i++) {
+        for (int i = 0; i < 4; i++) {                // (tile, buffer)
             mbar_init(bar(kBarSFull + i), 1);
-            mbar_init(bar(kBarPFull + i), 4);        // one arrival per warp of the warpgroup
+            mbar_init(bar(kBarSFree + i), 4);        // one arrival per warp of the warpgroup
+            mbar_init(bar(kBarPFull + i), 4);
+            mbar_init(bar(kBarODone + i), 1);
         }
-        mbar_init(bar(kBarODone), 1);
-        mbar_init(bar(kBarODone + 1), 1);
         mbar_init(bar(kBarQFull), 256);
-        mbar_init(bar(kBarFin), 1);
+        mbar_init(bar(kBarFin), 2);                  // one commit from each MMA thread
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const unsigned tmem = tmem_base_sh;
-    auto tO = [&](int t) { return tmem + (unsigned)(t * 128); };
-    auto tS = [&](int t, int b) { return tmem + 256u + (unsigned)(t * 128 + b * 64); };
-    auto stage = [&](int s) { return sbase + kOffStage + (unsigned)(s * kStageBytes); };
+    auto tO = [&](int t) { return tmem + kColO + (unsigned)(t * 128); };
+    auto tS = [&](int t, int b) { return tmem + kColS + (unsigned)(t * 128 + b * 64); };
+    auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
+    auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
+    auto pbuf = [&](int t, int b) { return (unsigned)(kOffP + (t * 2 + b) * kPBuf); };
 
     if (warp < 8) {
         // ------------------------------------------------------------ softmax warpgroups
@@ -320,6 +350,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int r = tile * kRowsTC + row;
         const bool row_ok = wg < n_act && r < Mtot;
         {
+            // this row's query into the K-major, 128-byte-swizzled Q tile
             const __half *qrow = p.q;
             if (row_ok) {
                 const int b = owner_of(qo, p.B, r);
@@ -357,30 +388,36 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         s[32 + i] = __uint_as_float(c[i]);
                     }
                 }
-                float mt = kNegInf;
+                // S(j) is in registers: its buffer may take S(j+2)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarSFree + wg * 2 + b));
                 const int kbase = key0 + j * kKeysTC;
-                if (kbase + kKeysTC <= key_hi) {
+                if (kbase + kKeysTC > key_hi) {
 #pragma unroll
-                    for (int i = 0; i < 64; i++) {
-                        s[i] *= p.scale_log2;
-                        mt = fmaxf(mt, s[i]);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; i++) {
-                        s[i] = (kbase + i < key_hi) ? s[i] * p.scale_log2 : kNegInf;
-                        mt = fmaxf(mt, s[i]);
-                    }
+                    for (int i = 0; i < 64; i++)
+                        if (kbase + i >= key_hi) s[i] = kNegInf;
                 }
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) mx[i] = s[i];
+#pragma unroll
+                for (int i = 8; i < 64; i++) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
+                bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
                 // lazy rescale: only when this row's max grows by more than 8 (log2)
                 const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
+                bool rescaled = false;
                 if (__any_sync(0xffffffffu, grow)) {
                     const float mn = grow ? mt : m_run;
                     const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
                     if (j >= 1) {
-                        // O holds PV(0..j-1): wait for PV(j-1) before touching it
-                        ok = mbar_wait(bar(kBarODone + wg), (j - 1) & 1, abort_p);
+                        // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
+                        ok = mbar_wait(bar(kBarODone + wg * 2 + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
                         if (!__all_sync(0xffffffffu, ok)) break;
+                        pbuf_free = true;
                         tc_fence_after();
 #pragma unroll
                         for (int q4 = 0; q4 < 4; q4++) {
@@ -391,29 +428,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                             tmem_st32(tO(wg) + lane_off + q4 * 32, o);
                         }
+                        tmem_wait_st();
+                        rescaled = true;
                     }
                     l_run *= alpha;
                     m_run = mn;
                 }
                 const float mu = (m_run == kNegInf) ? 0.f : m_run;
                 unsigned pk[32];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 32; i++) {
-                    const float p0 = ex2(s[2 * i] - mu), p1 = ex2(s[2 * i + 1] - mu);
-                    l_run += p0 + p1;
+                    const float p0 = ex2(fmaf(s[2 * i], p.scale_log2, -mu));
+                    const float p1 = ex2(fmaf(s[2 * i + 1], p.scale_log2, -mu));
+                    ls[i & 3] += p0 + p1;
                     pk[i] = pack_half2(p0, p1);
                 }
-                tmem_st32(tS(wg, b) + lane_off, pk);
-                tmem_wait_st();
-                tc_fence_before();
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if (!pbuf_free) {
+                    ok = mbar_wait(bar(kBarODone + wg * 2 + b), ((j - 2) >> 1) & 1, abort_p);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                }
+                // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
+                unsigned char *pr = gbase + pbuf(wg, b);
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_async_smem();
+                if (rescaled) tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarPFull + wg * 2 + b));
                 done = j + 1;
             }
-            // the row's partial: normalised O and log2-sum-exp.  The last PVs
-            // are awaited on the single-shot barrier the MMA thread commits
-            // after its final MMA (a parity wait on ODone could not tell
-            // PV(n-1) done from PV(n-2) still running).
+            // the row's partial: normalised O and log2-sum-exp, once every MMA
+            // has completed (the single-shot barrier the MMA thread commits last)
             bool fin = done == n_tiles;
             if (fin && n_tiles > 0) fin = mbar_wait(bar(kBarFin), 0, abort_p);
             fin = __all_sync(0xffffffffu, fin);
@@ -444,78 +493,101 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
     } else if (warp == kWarpLoad) {
         // ------------------------------------------------------------ TMA producer
+        // K runs up to kStagesK stages ahead and V up to kStagesV, each as
+        // soon as its ring has room (polled, so neither ring holds up the other)
         if (lane == 0) {
-            int issued = 0;
-            for (int j = 0; j < n_tiles; j++) {
-                const int s = j % kStagesTC;
-                if (j >= kStagesTC && !mbar_wait(bar(kBarEmpty + s), ((j / kStagesTC) - 1) & 1, abort_p)) break;
-                const unsigned st = stage(s);
-                const int z = key0 + j * kKeysTC;
-                mbar_expect_tx(bar(kBarKFull + s), 2 * kHalfKV);
-                tma_load_3d(st, &tmK, 0, h, z, bar(kBarKFull + s));
-                tma_load_3d(st + kHalfKV, &tmK, 64, h, z, bar(kBarKFull + s));
-                mbar_expect_tx(bar(kBarVFull + s), 2 * kHalfKV);
-                tma_load_3d(st + 2 * kHalfKV, &tmV, 0, h, z, bar(kBarVFull + s));
-                tma_load_3d(st + 3 * kHalfKV, &tmV, 64, h, z, bar(kBarVFull + s));
-                issued = j + 1;
+            int jk = 0, jv = 0;
+            unsigned long long t_last = global_ns();
+            while ((jk < n_tiles || jv < n_tiles) && !*abort_p) {
+                bool progress = false;
+                if (jk < n_tiles &&
+                    (jk < kStagesK || mbar_test(bar(kBarKEmpty + jk % kStagesK), ((jk / kStagesK) - 1) & 1))) {
+                    const int s = jk % kStagesK, z = key0 + jk * kKeysTC;
+                    mbar_expect_tx(bar(kBarKFull + s), kStageBytes);
+                    tma_load_3d(kstage(s), &tmK, 0, h, z, bar(kBarKFull + s));
+                    tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, h, z, bar(kBarKFull + s));
+                    jk++;
+                    progress = true;
+                }
+                if (jv < n_tiles &&
+                    (jv < kStagesV || mbar_test(bar(kBarVEmpty + jv % kStagesV), ((jv / kStagesV) - 1) & 1))) {
+                    const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
+                    mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
+                    tma_load_3d(vstage(s), &tmV, 0, h, z, bar(kBarVFull + s));
+                    tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, h, z, bar(kBarVFull + s));
+                    jv++;
+                    progress = true;
+                }
+                if (progress) {
+                    t_last = global_ns();
+                } else if (global_ns() - t_last > kWaitNs) {
+                    *abort_p = 1;
+                    break;
+                }
             }
             // no copy may still be in flight when the CTA leaves
-            for (int s = 0; s < kStagesTC && s < issued; s++) {
-                const int js = s + ((issued - 1 - s) / kStagesTC) * kStagesTC;
-                mbar_drain(bar(kBarKFull + s), (js / kStagesTC) & 1);
-                mbar_drain(bar(kBarVFull + s), (js / kStagesTC) & 1);
-            }
+            for (int s = 0; s < kStagesK && s < jk; s++)
+                mbar_drain(bar(kBarKFull + s), ((s + ((jk - 1 - s) / kStagesK) * kStagesK) / kStagesK) & 1);
+            for (int s = 0; s < kStagesV && s < jv; s++)
+                mbar_drain(bar(kBarVFull + s), ((s + ((jv - 1 - s) / kStagesV) * kStagesV) / kStagesV) & 1);
         }
-    } else {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMmaS) {
+        // ------------------------------------------------------------ S = Q K^T
         if (lane == 0) {
-            const uint32_t idS = idesc_f16(kRowsTC, kKeysTC), idO = idesc_f16(kRowsTC, 128, true);
+            const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
             bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
             tc_fence_after();
-            for (int j = 0; ok && j <= n_tiles; j++) {
-                if (j < n_tiles) {
-                    const int s = j % kStagesTC, b = j & 1;
-                    ok = mbar_wait(bar(kBarKFull + s), (j / kStagesTC) & 1, abort_p);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const unsigned kb = stage(s);
-                    for (int t = 0; t < n_act; t++) {
-                        // S buffer b held P(j-2): PV(j-2) must have read it
-                        if (j >= 2) {
-                            ok = mbar_wait(bar(kBarODone + t), (j - 2) & 1, abort_p);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
-#pragma unroll
-                        for (int kk = 0; kk < 8; kk++)
-                            umma_ss(tS(t, b), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
-                                    sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
-                        umma_commit(bar(kBarSFull + t * 2 + b));
-                    }
-                    if (!ok) break;
-                }
-                if (j >= 1) {
-                    const int jp = j - 1, sp = jp % kStagesTC, bp = jp & 1;
-                    ok = mbar_wait(bar(kBarVFull + sp), (jp / kStagesTC) & 1, abort_p);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const unsigned vb = stage(sp) + 2 * kHalfKV;
-                    for (int t = 0; t < n_act; t++) {
-                        ok = mbar_wait(bar(kBarPFull + t * 2 + bp), (jp >> 1) & 1, abort_p);
+            for (int j = 0; ok && j < n_tiles; j++) {
+                const int b = j & 1, sk = j % kStagesK;
+                ok = mbar_wait(bar(kBarKFull + sk), (j / kStagesK) & 1, abort_p);
+                if (!ok) break;
+                tc_fence_after();
+                const unsigned kb = kstage(sk);
+                for (int t = 0; t < n_act; t++) {
+                    if (j >= 2) {
+                        // S buffer b held S(j-2): its warpgroup must have read it
+                        ok = mbar_wait(bar(kBarSFree + t * 2 + b), ((j - 2) >> 1) & 1, abort_p);
                         if (!ok) break;
                         tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 4; kk++)
-                            umma_ts(tO(t), tS(t, bp) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
-                                    (jp > 0 || kk > 0));
-                        umma_commit(bar(kBarODone + t));
                     }
-                    if (!ok) break;
-                    umma_commit(bar(kBarEmpty + sp));
+                    const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++)
+                        umma_ss(tS(t, b), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
+                                sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
+                    umma_commit(bar(kBarSFull + t * 2 + b));
                 }
+                if (!ok) break;
+                umma_commit(bar(kBarKEmpty + sk));
             }
-            // every MMA issued so far has completed once this barrier fires
+            // every S MMA has completed once the final barrier fires
+            umma_commit(bar(kBarFin));
+            mbar_drain(bar(kBarFin), 0);
+        }
+    } else {
+        // ------------------------------------------------------------ O += P V
+        if (lane == 0) {
+            const uint32_t idO = idesc_f16(kRowsTC, 128, true);
+            bool ok = true;
+            for (int j = 0; ok && j < n_tiles; j++) {
+                const int b = j & 1, sv = j % kStagesV;
+                ok = mbar_wait(bar(kBarVFull + sv), (j / kStagesV) & 1, abort_p);
+                if (!ok) break;
+                const unsigned vb = vstage(sv);
+                for (int t = 0; t < n_act; t++) {
+                    ok = mbar_wait(bar(kBarPFull + t * 2 + b), (j >> 1) & 1, abort_p);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const unsigned pa = sbase + pbuf(t, b);
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++)
+                        umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
+                                (j > 0 || kk > 0));
+                    umma_commit(bar(kBarODone + t * 2 + b));
+                }
+                if (!ok) break;
+                umma_commit(bar(kBarVEmpty + sv));
+            }
             umma_commit(bar(kBarFin));
             mbar_drain(bar(kBarFin), 0);
         }
@@ -524,7 +596,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
-    if (warp == kWarpMma) {
+    if (warp == kWarpMmaS) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(kTmemCols) : "memory");
