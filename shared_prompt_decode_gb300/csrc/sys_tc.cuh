@@ -23,13 +23,13 @@
 //   O += P V         tcgen05.mma, M=128 N=128: P and V from shared memory, V
 //                    in its natural [key][d] order (MN-major), never transposed
 // The S thread runs two stages ahead of the PV thread: S(j+2) is issued
-// while PV(j) is.  S and P are double-buffered, so every hand-off between an
-// MMA thread and a warpgroup has a full stage of slack: a warpgroup frees an
-// S buffer as soon as it has read it, and refills a P buffer once the PV two
-// stages back has completed.  A thread that has MMAs in flight waits for them
-// to drain before its next shared-memory read completes, so a barrier check
-// on the issuing thread empties the tensor pipe; with S and PV issued from
-// two threads, one thread's checks overlap the other's MMAs.
+// while PV(j) is.  S and P are double-buffered.  A thread that has MMAs in
+// flight waits for them to drain before its next shared-memory read
+// completes, so every barrier check on an issuing thread empties the tensor
+// pipe.  The MMA threads therefore check one barrier per stage: READY(j),
+// raised by the warpgroups once P(j) is stored (so S(j) has been read, and
+// its S buffer may take S(j+2)) and once they have seen V(j) and K(j+2)
+// land; the two threads' checks overlap each other's MMAs.
 // Each barrier signalled per stage has one instance per buffer, so that no
 // parity wait can be two phases behind.  O is rescaled only when a row's
 // running maximum grows by more than 2^8 (P <= 256 otherwise, well inside
@@ -65,16 +65,16 @@ constexpr int kOffP = kOffQ + 2 * kQTile;         // [tile][buffer]
 constexpr int kOffK = kOffP + 4 * kPBuf;
 constexpr int kOffV = kOffK + kStagesK * kStageBytes;
 constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
-constexpr int kNumBars = 32;
+constexpr int kNumBars = 24;
 constexpr int kSmemTC = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 // TMEM columns: O tile 0 | O tile 1 | S tile 0 (2 buffers) | S tile 1 (2 buffers)
 constexpr int kTmemCols = 512;
 constexpr unsigned kColO = 0, kColS = 256;
 
 // mbarrier slots
-constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6, kBarVEmpty = 8;       // per stage
-constexpr int kBarSFull = 10, kBarSFree = 14, kBarPFull = 18, kBarODone = 22;    // per (tile, buffer)
-constexpr int kBarQFull = 26, kBarFin = 27;
+constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6, kBarVEmpty = 8;   // per stage
+constexpr int kBarSFull = 10, kBarReady = 12, kBarODone = 14;               // per buffer, both tiles
+constexpr int kBarQFull = 16, kBarFin = 17;
 
 // --------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count)
@@ -321,10 +321,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarVEmpty + s), 1);
         }
-        for (int i = 0; i < 4; i++) {                // (tile, buffer)
+        for (int i = 0; i < 2; i++) {                // per buffer
             mbar_init(bar(kBarSFull + i), 1);
-            mbar_init(bar(kBarSFree + i), 4);        // one arrival per warp of the warpgroup
-            mbar_init(bar(kBarPFull + i), 4);
+            mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
             mbar_init(bar(kBarODone + i), 1);
         }
         mbar_init(bar(kBarQFull), 256);
@@ -373,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int done = 0;
             for (int j = 0; j < n_tiles; j++) {
                 const int b = j & 1;
-                bool ok = mbar_wait(bar(kBarSFull + wg * 2 + b), (j >> 1) & 1, abort_p);
+                bool ok = mbar_wait(bar(kBarSFull + b), (j >> 1) & 1, abort_p);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 tc_fence_after();
                 float s[64];
@@ -388,10 +387,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         s[32 + i] = __uint_as_float(c[i]);
                     }
                 }
-                // S(j) is in registers: its buffer may take S(j+2)
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarSFree + wg * 2 + b));
                 const int kbase = key0 + j * kKeysTC;
                 if (kbase + kKeysTC > key_hi) {
 #pragma unroll
@@ -415,7 +410,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
                     if (j >= 1) {
                         // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
-                        ok = mbar_wait(bar(kBarODone + wg * 2 + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
+                        ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
                         if (!__all_sync(0xffffffffu, ok)) break;
                         pbuf_free = true;
                         tc_fence_after();
@@ -446,7 +441,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 if (!pbuf_free) {
-                    ok = mbar_wait(bar(kBarODone + wg * 2 + b), ((j - 2) >> 1) & 1, abort_p);
+                    ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
                     if (!__all_sync(0xffffffffu, ok)) break;
                 }
                 // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
@@ -456,9 +451,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
                         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 fence_async_smem();
-                if (rescaled) tc_fence_before();
+                // the MMA threads check only READY: V(j) and K(j+2) must have landed
+                ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
+                if (ok && j + 2 < n_tiles)
+                    ok = mbar_wait(bar(kBarKFull + (j + 2) % kStagesK), ((j + 2) / kStagesK) & 1, abort_p);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                tc_fence_before();   // S(j) loads (and a rescale's stores) before the MMAs that follow
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarPFull + wg * 2 + b));
+                if (lane == 0) mbar_arrive(bar(kBarReady + b));
                 done = j + 1;
             }
             // the row's partial: normalised O and log2-sum-exp, once every MMA
@@ -535,30 +535,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // ------------------------------------------------------------ S = Q K^T
         if (lane == 0) {
             const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
-            bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
-            tc_fence_after();
-            for (int j = 0; ok && j < n_tiles; j++) {
-                const int b = j & 1, sk = j % kStagesK;
-                ok = mbar_wait(bar(kBarKFull + sk), (j / kStagesK) & 1, abort_p);
-                if (!ok) break;
-                tc_fence_after();
-                const unsigned kb = kstage(sk);
+            auto issue_s = [&](int j) {              // S(j) of every tile into S buffer j % 2
+                const unsigned kb = kstage(j % kStagesK);
                 for (int t = 0; t < n_act; t++) {
-                    if (j >= 2) {
-                        // S buffer b held S(j-2): its warpgroup must have read it
-                        ok = mbar_wait(bar(kBarSFree + t * 2 + b), ((j - 2) >> 1) & 1, abort_p);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
                     const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
 #pragma unroll
                     for (int kk = 0; kk < 8; kk++)
-                        umma_ss(tS(t, b), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
+                        umma_ss(tS(t, j & 1), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
                                 sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
-                    umma_commit(bar(kBarSFull + t * 2 + b));
                 }
+                umma_commit(bar(kBarSFull + (j & 1)));
+                umma_commit(bar(kBarKEmpty + j % kStagesK));
+            };
+            bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
+            for (int j = 0; ok && j < n_tiles && j < 2; j++) {
+                ok = mbar_wait(bar(kBarKFull + j % kStagesK), (j / kStagesK) & 1, abort_p);
                 if (!ok) break;
-                umma_commit(bar(kBarKEmpty + sk));
+                tc_fence_after();
+                issue_s(j);
+            }
+            for (int j = 0; ok && j + 2 < n_tiles; j++) {
+                // READY(j): S(j) read (its buffer is free) and K(j+2) landed
+                ok = mbar_wait(bar(kBarReady + (j & 1)), (j >> 1) & 1, abort_p);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(j + 2);
             }
             // every S MMA has completed once the final barrier fires
             umma_commit(bar(kBarFin));
@@ -571,21 +572,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             bool ok = true;
             for (int j = 0; ok && j < n_tiles; j++) {
                 const int b = j & 1, sv = j % kStagesV;
-                ok = mbar_wait(bar(kBarVFull + sv), (j / kStagesV) & 1, abort_p);
+                // READY(j): P(j) stored and V(j) landed
+                ok = mbar_wait(bar(kBarReady + b), (j >> 1) & 1, abort_p);
                 if (!ok) break;
+                tc_fence_after();
                 const unsigned vb = vstage(sv);
                 for (int t = 0; t < n_act; t++) {
-                    ok = mbar_wait(bar(kBarPFull + t * 2 + b), (j >> 1) & 1, abort_p);
-                    if (!ok) break;
-                    tc_fence_after();
                     const unsigned pa = sbase + pbuf(t, b);
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++)
                         umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                 (j > 0 || kk > 0));
-                    umma_commit(bar(kBarODone + t * 2 + b));
                 }
-                if (!ok) break;
+                umma_commit(bar(kBarODone + b));
                 umma_commit(bar(kBarVEmpty + sv));
             }
             umma_commit(bar(kBarFin));
