@@ -44,7 +44,16 @@ import synth  # noqa: E402
 METRIC = "relay decode-attention step µs, tokens/s & HBM GB/s (% of 8 TB/s), Llama2-7B"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-KERNEL_SOURCES = ["shared_prompt_decode_gb300/csrc/relay.cu", "shared_prompt_decode_gb300/csrc/relay_kernels.cuh"]
+KERNEL_SOURCES = ["shared_prompt_decode_gb300/csrc/relay.cu", "shared_prompt_decode_gb300/csrc/relay_kernels.cuh",
+                  "shared_prompt_decode_gb300/csrc/sys_tc.cuh"]
+# The library runs the system step on the tcgen05 kernel, a third launch per
+# step, when D = 128, Ls > 0 and the batch holds more than this many query
+# rows per head (the dispatch rule of relay.cu).
+TC_MIN_ROWS = 256
+
+
+def launches_per_step(case):
+    return 3 if (case.D == 128 and case.Ls > 0 and case.total_q() > TC_MIN_ROWS) else 2
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -370,7 +379,7 @@ def run_relay(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=8)
+        cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=200)
 
     if rank != 0:
         return 0
@@ -386,14 +395,16 @@ def run_relay(args):
         "algorithmic_bytes_per_step": abytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "relay_kernel<128> + merge_kernel<128> (two launches per step, one graph)",
+                     "kernel": ("relay_kernel<128> + merge_kernel<128> (two launches per step, one graph)"
+                                if launches_per_step(case) == 2 else
+                                "sys_tc_kernel + relay_kernel<128> + merge_kernel<128> (three launches per step, one graph)"),
                      "peak_source": f"{peaks['source']} copy bandwidth (burst)"},
         "nonrelay_baseline": {"kernel": "relay_baseline_decode (system KV re-read per request)",
                               "step_us": 1e3 * base_mean, "tokens_per_s": rows / (base_mean * 1e-3),
                               "relay_speedup": base_mean / statistics.mean(ms)},
         "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step(case) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

@@ -49,7 +49,7 @@ namespace tc {
 
 constexpr int kRowsTC = 128;          // query rows per tile (TMEM lanes)
 constexpr int kKeysTC = 64;           // keys per K/V stage
-constexpr int kStagesK = 3, kStagesV = 2;
+constexpr int kStagesK = 3, kStagesV = 2;   // V stage j % 2 is freed by the O-done barrier of PV(j)
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // give up on a wait after 1 s
@@ -72,7 +72,7 @@ constexpr int kTmemCols = 512;
 constexpr unsigned kColO = 0, kColS = 256;
 
 // mbarrier slots
-constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6, kBarVEmpty = 8;   // per stage
+constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6;                  // per stage
 constexpr int kBarSFull = 10, kBarReady = 12, kBarODone = 14;               // per buffer, both tiles
 constexpr int kBarQFull = 16, kBarFin = 17;
 
@@ -241,6 +241,36 @@ __device__ __forceinline__ void tmem_st32(unsigned taddr, const unsigned (&r)[32
                  : "memory");
 }
 
+// packed fp32 pairs (two lanes of one 64-bit register)
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled region of 128-byte rows
 __device__ __forceinline__ unsigned sw_off(int r, int c) { return (unsigned)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -317,10 +347,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarKEmpty + s), 1);
         }
-        for (int s = 0; s < kStagesV; s++) {
-            mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarVEmpty + s), 1);
-        }
+        for (int s = 0; s < kStagesV; s++) mbar_init(bar(kBarVFull + s), 1);
         for (int i = 0; i < 2; i++) {                // per buffer
             mbar_init(bar(kBarSFull + i), 1);
             mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
@@ -395,11 +422,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 float mx[8];
 #pragma unroll
-                for (int i = 0; i < 8; i++) mx[i] = s[i];
-#pragma unroll
-                for (int i = 8; i < 64; i++) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-                const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                for (int k = 0; k < 8; k++) {
+                    mx[k] = max3f(s[k], s[8 + k], s[16 + k]);
+                    mx[k] = max3f(mx[k], s[24 + k], s[32 + k]);
+                    mx[k] = max3f(mx[k], s[40 + k], s[48 + k]);
+                    mx[k] = fmaxf(mx[k], s[56 + k]);
+                }
+                const float mraw = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
                 bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
                 // lazy rescale: only when this row's max grows by more than 8 (log2)
@@ -431,15 +460,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 const float mu = (m_run == kNegInf) ? 0.f : m_run;
                 unsigned pk[32];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nmu2 = f2_pack(-mu, -mu);
+                unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};     // pairs of +0.0f
 #pragma unroll
                 for (int i = 0; i < 32; i++) {
-                    const float p0 = ex2(fmaf(s[2 * i], p.scale_log2, -mu));
-                    const float p1 = ex2(fmaf(s[2 * i + 1], p.scale_log2, -mu));
-                    ls[i & 3] += p0 + p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nmu2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    ls[i & 3] = f2_add(ls[i & 3], f2_pack(p0, p1));
                     pk[i] = pack_half2(p0, p1);
                 }
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
+                    l_run += a0 + a1;
+                }
                 if (!pbuf_free) {
                     ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
                     if (!__all_sync(0xffffffffu, ok)) break;
@@ -509,8 +544,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     jk++;
                     progress = true;
                 }
-                if (jv < n_tiles &&
-                    (jv < kStagesV || mbar_test(bar(kBarVEmpty + jv % kStagesV), ((jv / kStagesV) - 1) & 1))) {
+                // V stage jv % 2 held V(jv-2): free once PV(jv-2) has completed
+                if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
                     const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
                     mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
                     tma_load_3d(vstage(s), &tmV, 0, h, z, bar(kBarVFull + s));
@@ -584,8 +619,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                 (j > 0 || kk > 0));
                 }
-                umma_commit(bar(kBarODone + b));
-                umma_commit(bar(kBarVEmpty + sv));
+                umma_commit(bar(kBarODone + b));      // also frees V stage sv for the producer
             }
             umma_commit(bar(kBarFin));
             mbar_drain(bar(kBarFin), 0);

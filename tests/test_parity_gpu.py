@@ -316,10 +316,14 @@ def test_device_checks_flag_bad_values(what):
 
 # ----------------------------------------------------------------------------- tensor-core system step
 # Batches with more than 256 query rows per head run the system step on the
-# tcgen05 kernel (128-row tiles, 64-key tiles); ragged rows and keys on purpose.
+# tcgen05 kernel (pairs of 128-row tiles, 64-key stages, S issued two stages
+# ahead of PV); ragged rows and keys on purpose, and ranges of 1, 2 and 3
+# stages, which take the pipeline's prologue-only and shortest-loop paths.
 TC_CASES = [
     ("rows257_keys1000", 257, 1, 1000, None),
     ("rows300_keys64", 300, 1, 64, None),
+    ("rows300_keys100", 300, 1, 100, None),
+    ("rows513_keys150", 171, 3, 150, None),
     ("rows600_keys4097", 150, 4, 4097, None),
     ("chunks_qlens", 6, 128, 700, [128, 1, 77, 128, 3, 90]),
 ]
