@@ -185,13 +185,13 @@ def build_case(args, rank):
 
 
 def algorithmic_bytes(case):
-    kv_tok = 2 * case.H * case.D * 2
+    kv_tok = 2 * case.Hkv * case.D * 2          # K and V of one token, every KV head
     rows = case.total_q()
     return case.Ls * kv_tok + int(case.ctx_lens.sum()) * kv_tok + 2 * rows * case.H * case.D * 2
 
 
 def workload_config(case, args):
-    return {"workload": case.wl.name, "B": case.B, "H": case.H, "D": case.D, "Ls": case.Ls,
+    return {"workload": case.wl.name, "B": case.B, "H": case.H, "Hkv": case.Hkv, "D": case.D, "Ls": case.Ls,
             "Lq": case.Lq, "query_rows": case.total_q(), "ctx_tokens": int(case.ctx_lens.sum()),
             "block_size": 16, "seed": args.seed,
             "l2": "flushed between steps: 256 MB written, then another 256 MB read (L2 clean and cold)",
@@ -271,7 +271,7 @@ def run_relay(args):
     g["q_lens"] = None if case.q_lens is None else case.q_lens.to(dev)
     mq = case.total_q() if case.q_lens is not None else 0
     rows = case.total_q()
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv, ctx_split=args.ctx_split,
                            sys_range=args.sys_range, max_q_total=mq)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])
@@ -343,7 +343,7 @@ def run_relay(args):
     # non-relay baseline: same requests, system KV re-read per request from the paged pool
     kp, vp, ids = synth.with_system_in_pool(case)
     kp, vp, ids = kp.to(dev), vp.to(dev), ids.to(dev)
-    dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks, max_q_total=mq)
+    dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks, max_q_total=mq, Hkv=case.Hkv)
     ws_b = relay.make_workspace(dims_b, dev)
     out_b = torch.empty_like(out)
 
@@ -424,7 +424,7 @@ def run_profile(args):
     g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
                                               "ctx_lens")}
     ql = None if case.q_lens is None else case.q_lens.to(dev)
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, ctx_split=args.ctx_split,
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv, ctx_split=args.ctx_split,
                            sys_range=args.sys_range, max_q_total=case.total_q() if ql is not None else 0)
     ws = relay.make_workspace(dims, dev)
     out = torch.empty_like(g["q"])

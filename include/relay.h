@@ -25,8 +25,8 @@
  *    says so).  All work is queued on `stream`; the calls return at once.
  *  - Layouts are contiguous, row-major:
  *      q, out             [B, Lq, H, D]            fp16
- *      sys_k, sys_v       [Ls, H, D]               fp16
- *      k_cache, v_cache   [num_blocks, H, 16, D]   fp16 (paged pool; one
+ *      sys_k, sys_v       [Ls, Hkv, D]             fp16
+ *      k_cache, v_cache   [num_blocks, Hkv, 16, D] fp16 (paged pool; one
  *                                                  head of one block is 16
  *                                                  contiguous rows of D)
  *      block_tables       [B, max_blocks_per_seq]  int32 (physical block of
@@ -39,6 +39,10 @@
  *      lse arrays         [B, Lq, H]               fp32, natural log
  *      o_sys, o_ctx       [B, Lq, H, D]            fp32
  *    q, out, sys_k, sys_v, k_cache, v_cache must be 16-byte aligned.
+ *  - Hkv KV heads serve H query heads (grouped-query attention; Hkv = H is
+ *    multi-head, Hkv = 1 multi-query): query head h reads KV head
+ *    h / (H / Hkv), i.e. each run of H / Hkv consecutive query heads shares
+ *    one KV head.
  *  - Query row i of request b is context position ctx_lens[b]-q_lens[b]+i;
  *    it sees the whole system prompt and context tokens
  *    t < max(0, ctx_lens[b] - q_lens[b] + 1 + i).  Rows i >= q_lens[b] of
@@ -101,6 +105,8 @@ typedef struct {
     int32_t sys_range;          /* system keys per work item; 0 = automatic;
                                    else a multiple of 64 */
     float scale;                /* softmax scale; <= 0 means 1/sqrt(D) */
+    int32_t Hkv;                /* KV heads of sys_k/sys_v and the pool; 0 means H
+                                   (multi-head); else H must be a multiple of it */
 } relay_dims_t;
 
 /* Bytes of workspace any entry point below needs for `dims` (0 if `dims` is

@@ -34,7 +34,7 @@ class _Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Lq", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("D", ctypes.c_int32), ("Ls", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
-                ("scale", ctypes.c_double)]
+                ("Hkv", ctypes.c_int32), ("scale", ctypes.c_double)]
 
 
 def build(force: bool = False) -> str:
@@ -99,10 +99,10 @@ def attention_rows(case, rows, part: str = "full", scale: float | None = None,
     rows = list(rows)
     n = len(rows)
     D = case.D
-    dims = _Dims(case.B, case.Lq, case.H, D, case.Ls, 16,
-                 (k_cache if k_cache is not None else case.k_cache).shape[0],
+    kc_ = k_cache if k_cache is not None else case.k_cache
+    dims = _Dims(case.B, case.Lq, case.H, D, case.Ls, 16, kc_.shape[0],
                  (block_tables if block_tables is not None else case.block_tables).shape[1],
-                 float(1.0 / math.sqrt(D)) if scale is None else float(scale))
+                 kc_.shape[1], float(1.0 / math.sqrt(D)) if scale is None else float(scale))
     rb = np.ascontiguousarray(np.array([r[0] for r in rows], dtype=np.int32))
     ri = np.ascontiguousarray(np.array([r[1] for r in rows], dtype=np.int32))
     rh = np.ascontiguousarray(np.array([r[2] for r in rows], dtype=np.int32))

@@ -12,7 +12,9 @@
  * causal attention):
  *
  *   for every request b, query row i < q_lens[b], head h:
- *     keys   = [ system keys 0..Ls-1 ;  context keys t = 0..v-1 ]
+ *     keys   = [ system keys 0..Ls-1 ;  context keys t = 0..v-1 ]  of KV head
+ *              h / (H / Hkv)   (grouped-query attention: H / Hkv consecutive
+ *              query heads share one KV head; Hkv = H is multi-head)
  *     v      = max(0, ctx_lens[b] - q_lens[b] + 1 + i)      (causal visibility:
  *              the query rows are the last q_lens[b] positions of the context)
  *     s_j    = scale * <q[b,i,h], k_j>
@@ -20,8 +22,8 @@
  *
  * Context key t of request b lives in the paged pool at block
  * block_tables[b][t / bs], row t % bs (PagedAttention block tables; the pool
- * layout is [num_blocks, H, bs, D]).  System keys live in a separate cache
- * [Ls, H, D] (atyun.com RelayAttention article, section "RelayAttention": a
+ * layout is [num_blocks, Hkv, bs, D]).  System keys live in a separate cache
+ * [Ls, Hkv, D] (atyun.com RelayAttention article, section "RelayAttention": a
  * separate cache for the system KVs, filled offline).
  *
  * A second set of entry points computes the method's three steps separately
@@ -47,6 +49,7 @@
 
 typedef struct {
     int32_t B, Lq, H, D, Ls, block_size, num_blocks, max_blocks;
+    int32_t Hkv;      /* KV heads of the caches; H is a multiple of Hkv */
     double scale;
 } oracle_dims_t;
 
@@ -124,9 +127,10 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
                           double *out, double *lse, int n_threads)
 {
     if (!dm || !out || !lse || n_rows < 0) return ORACLE_BAD_ARG;
-    const int B = dm->B, Lq = dm->Lq, H = dm->H, D = dm->D, Ls = dm->Ls;
+    const int B = dm->B, Lq = dm->Lq, H = dm->H, D = dm->D, Ls = dm->Ls, Hkv = dm->Hkv;
     const int bs = dm->block_size, MB = dm->max_blocks;
-    if (D <= 0 || H <= 0 || bs <= 0 || Ls < 0) return ORACLE_BAD_ARG;
+    if (D <= 0 || H <= 0 || bs <= 0 || Ls < 0 || Hkv <= 0 || H % Hkv != 0) return ORACLE_BAD_ARG;
+    const int group = H / Hkv;   /* query heads per KV head */
 
     /* Validate every row and every block id before computing anything. */
     for (int64_t r = 0; r < n_rows; r++) {
@@ -160,12 +164,13 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
 #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < n_rows; r++) {
             int b = row_b[r], i = row_i[r], h = row_h[r];
+            int hk = h / group;   /* the KV head this query head reads */
             int ql = q_lens ? q_lens[b] : Lq;
             int n = 0;
             if (part != PART_CTX) {
                 for (int t = 0; t < Ls; t++) {
-                    krows[n] = sys_k + ((int64_t)t * H + h) * D;
-                    vrows[n] = sys_v + ((int64_t)t * H + h) * D;
+                    krows[n] = sys_k + ((int64_t)t * Hkv + hk) * D;
+                    vrows[n] = sys_v + ((int64_t)t * Hkv + hk) * D;
                     n++;
                 }
             }
@@ -173,7 +178,7 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
                 int v = visible_ctx(ctx_lens[b], ql, i);
                 for (int t = 0; t < v; t++) {
                     int64_t blk = block_tables[(int64_t)b * MB + t / bs];
-                    int64_t row = (blk * H + h) * bs + t % bs;
+                    int64_t row = (blk * Hkv + hk) * bs + t % bs;
                     krows[n] = k_cache + row * D;
                     vrows[n] = v_cache + row * D;
                     n++;

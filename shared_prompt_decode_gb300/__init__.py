@@ -41,7 +41,7 @@ class Dims(ctypes.Structure):
                 ("D", ctypes.c_int32), ("Ls", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
                 ("max_q_total", ctypes.c_int32), ("ctx_split", ctypes.c_int32),
-                ("sys_range", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("sys_range", ctypes.c_int32), ("scale", ctypes.c_float), ("Hkv", ctypes.c_int32)]
 
     def __repr__(self):
         return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
@@ -114,10 +114,18 @@ def _need(t, name, dtype, device=None):
 
 
 def make_dims(q: torch.Tensor, Ls: int, num_blocks: int, max_blocks: int, scale: Optional[float] = None,
-              max_q_total: int = 0, ctx_split: int = 0, sys_range: int = 0) -> Dims:
+              max_q_total: int = 0, ctx_split: int = 0, sys_range: int = 0, Hkv: int = 0) -> Dims:
+    """Hkv: KV heads of the caches (0: as many as query heads)."""
     B, Lq, H, D = q.shape
     return Dims(B, Lq, H, D, Ls, 16, num_blocks, max_blocks, max_q_total, ctx_split, sys_range,
-                0.0 if scale is None else float(scale))
+                0.0 if scale is None else float(scale), Hkv)
+
+
+def _check_kv(dims: Dims, cache: torch.Tensor, name: str):
+    """The cache's head dimension (dim 1) must be the dims' KV heads."""
+    hkv = dims.Hkv if dims.Hkv > 0 else dims.H
+    if cache.dim() < 3 or cache.shape[1] != hkv:
+        raise ValueError(f"{name} has {cache.shape[1] if cache.dim() > 1 else '?'} KV heads, dims say {hkv}")
 
 
 def workspace_size(dims: Dims) -> int:
@@ -152,7 +160,9 @@ def relay_attention_decode(q, sys_k, sys_v, k_cache, v_cache, block_tables, ctx_
         _need(q_lens, "q_lens", torch.int32, dev)
     if dims is None:
         dims = make_dims(q, sys_k.shape[0], k_cache.shape[0], block_tables.shape[1], scale,
-                         max_q_total, ctx_split, sys_range)
+                         max_q_total, ctx_split, sys_range, k_cache.shape[1])
+    _check_kv(dims, sys_k, "sys_k")
+    _check_kv(dims, k_cache, "k_cache")
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.float16, dev)
@@ -173,7 +183,7 @@ def relay_sys_attn(q, sys_k, sys_v, q_lens=None, o_sys=None, lse_sys=None, works
     _need(sys_k, "sys_k", torch.float16, dev)
     _need(sys_v, "sys_v", torch.float16, dev)
     B, Lq, H, D = q.shape
-    dims = make_dims(q, sys_k.shape[0], 0, max_blocks, scale, max_q_total, 0, sys_range)
+    dims = make_dims(q, sys_k.shape[0], 0, max_blocks, scale, max_q_total, 0, sys_range, sys_k.shape[1])
     if o_sys is None:
         o_sys = torch.empty(B, Lq, H, D, dtype=torch.float32, device=dev)
     if lse_sys is None:
@@ -194,7 +204,8 @@ def relay_ctx_attn(q, k_cache, v_cache, block_tables, ctx_lens, q_lens=None, o_c
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
     B, Lq, H, D = q.shape
-    dims = make_dims(q, 0, k_cache.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0)
+    dims = make_dims(q, 0, k_cache.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0,
+                     k_cache.shape[1])
     if o_ctx is None:
         o_ctx = torch.empty(B, Lq, H, D, dtype=torch.float32, device=dev)
     if lse_ctx is None:
@@ -232,7 +243,9 @@ def relay_baseline_decode(q, k_pool, v_pool, sys_block_ids, Ls, block_tables, ct
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
     if dims is None:
-        dims = make_dims(q, Ls, k_pool.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0)
+        dims = make_dims(q, Ls, k_pool.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0,
+                         k_pool.shape[1])
+    _check_kv(dims, k_pool, "k_pool")
     if out is None:
         out = torch.empty_like(q)
     ws = _ws(dims, workspace, dev)
@@ -252,8 +265,8 @@ def device_status(workspace: torch.Tensor, stream=None) -> int:
     return int(flags.value)
 
 
-def algorithmic_bytes(B, H, D, Ls, ctx_lens, q_rows) -> int:
+def algorithmic_bytes(B, H, D, Ls, ctx_lens, q_rows, Hkv=None) -> int:
     """Bytes the relay step must move at minimum: the system KV once, every
-    request's context KV once, q read and out written (fp16)."""
-    kv_token = 2 * H * D * 2
+    request's context KV once (Hkv heads), q read and out written (fp16)."""
+    kv_token = 2 * (H if not Hkv else Hkv) * D * 2
     return Ls * kv_token + int(sum(int(n) for n in ctx_lens)) * kv_token + 2 * q_rows * H * D * 2

@@ -74,6 +74,9 @@ relay_status_t device_info(const DevInfo **out)
     return RELAY_OK;
 }
 
+// KV heads of the caches (0 in the dims means multi-head: H)
+int kv_heads(const relay_dims_t *d) { return d->Hkv > 0 ? d->Hkv : d->H; }
+
 relay_status_t check_dims(const relay_dims_t *d)
 {
     if (!d) return RELAY_ERR_INVALID_ARG;
@@ -82,6 +85,7 @@ relay_status_t check_dims(const relay_dims_t *d)
         d->sys_range < 0 || !(d->scale == d->scale))
         return RELAY_ERR_INVALID_ARG;
     if (d->ctx_split % kTileK || d->sys_range % kTileK) return RELAY_ERR_INVALID_ARG;
+    if (d->Hkv < 0 || (d->Hkv > 0 && d->H % d->Hkv != 0)) return RELAY_ERR_INVALID_ARG;
     if (d->D != 64 && d->D != 128) return RELAY_ERR_UNSUPPORTED;
     if (d->block_size != kBlock) return RELAY_ERR_UNSUPPORTED;
     if (d->B > kMaxB) return RELAY_ERR_UNSUPPORTED;
@@ -242,6 +246,8 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.B = d->B;
     p.Lq = d->Lq;
     p.H = d->H;
+    p.Hkv = kv_heads(d);
+    p.G = d->H / p.Hkv;
     p.Ls = d->Ls;
     p.num_blocks = d->num_blocks;
     p.max_blocks = d->max_blocks_per_seq;
@@ -269,6 +275,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.B = d->B;
         t.Lq = d->Lq;
         t.H = d->H;
+        t.G = p.G;
         t.Ls = d->Ls;
         t.max_q_total = pl.Mtot;
         t.scale_log2 = p.scale_log2;
@@ -281,7 +288,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.range = pl.sys_range;
         t.pairs = tc_pairs(pl.Mtot);
         CUtensorMap tmK, tmV;
-        if (!encode_sys_map(&tmK, p.sys_k, d->H, d->Ls) || !encode_sys_map(&tmV, p.sys_v, d->H, d->Ls))
+        if (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls))
             return RELAY_ERR_CUDA;
         const long long items = (long long)t.pairs * d->H * pl.R_sys;
         tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);

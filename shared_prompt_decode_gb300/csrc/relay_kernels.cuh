@@ -71,6 +71,7 @@ enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DONE = 2, CTRL_DEC_ITEMS = 3 };
 
 struct Params {
     int B, Lq, H, Ls, num_blocks, max_blocks, max_q_total;
+    int Hkv, G;                       // KV heads; query heads per KV head (query head h reads KV head h / G)
     float scale_log2;                 // softmax scale * log2(e)
     const __half *q, *sys_k, *sys_v, *k_cache, *v_cache;
     const int *block_tables, *ctx_lens, *q_lens;
@@ -514,7 +515,7 @@ struct KeySrc {
     const int *table;       // this request's block table row (paged) or nullptr (system cache)
     const int *prefix;      // baseline: system blocks
     int n_prefix;
-    int H, h, num_blocks;
+    int H, h, num_blocks;   // KV heads of the cache and the KV head read
 };
 
 // Element offset of key t's row; false (and a flag) for an out-of-range block.
@@ -861,7 +862,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2;
 
-    KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.H, h, 0};
+    KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.Hkv, h / p.G, 0};
     const int key0 = rho * p.sys_range;
     const int key_hi = min(key0 + p.sys_range, p.Ls);
     row_prologue<D>(s, src, key0, key_hi, p.ctrl);
@@ -908,7 +909,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     const int n_ctx = ri.n_ctx;
 
     KeySrc src{p.k_cache, p.v_cache, p.block_tables + (size_t)b * p.max_blocks, p.prefix_ids, p.n_prefix,
-               p.H, h, p.num_blocks};
+               p.Hkv, h / p.G, p.num_blocks};
     auto vis = [&](int i) {   // keys row i may see: prefix + max(0, n - ql + 1 + i)
         int v = n_ctx - ql + 1 + i;
         v = v < 0 ? 0 : (v > n_ctx ? n_ctx : v);
@@ -1006,7 +1007,7 @@ __device__ __forceinline__ void load_page(const Params &p, __half *K, __half *V,
     const int rows = page_rows(p, it.pp, it.n_ctx, it.p0 + j);
     const bool ok = blk >= 0 && blk < p.num_blocks;
     if (!ok && lane == 0) atomicOr(&p.ctrl[CTRL_FLAGS], FLAG_BAD_BLOCK);
-    const size_t base = (((size_t)(ok ? blk : 0) * p.H + it.h) * kBlock) * D;
+    const size_t base = (((size_t)(ok ? blk : 0) * p.Hkv + it.h / p.G) * kBlock) * D;
 #pragma unroll
     for (int k = 0; k < PER; k++) {
         int c = lane + k * 32;

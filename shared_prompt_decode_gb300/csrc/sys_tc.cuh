@@ -283,6 +283,7 @@ struct TcParams {
     float *part_o, *part_lse;        // partial slots: [part][max_q_total][H][128]
     int R, range;                    // key ranges of the system prompt
     int pairs;                       // tile pairs in the grid: ceil(ceil(max_q_total / 128) / 2)
+    int G;                           // query heads per KV head: head h reads KV head h / G
 };
 
 __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
@@ -298,7 +299,7 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 
 
 // blockIdx.x = (range * pairs + pair) * H + h.  tmK / tmV view sys_k / sys_v
-// as [Ls][H][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
+// as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
 __global__ void __launch_bounds__(kThreadsTC, 1)
     sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int h = blockIdx.x % p.H;
     const int pair = (blockIdx.x / p.H) % p.pairs;
     const int rho = blockIdx.x / (p.H * p.pairs);
+    const int hk = h / p.G;                          // KV head
     if (2 * pair >= T || rho >= p.R) return;        // the whole CTA leaves together
     const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
     const int key0 = rho * p.range;
@@ -539,8 +541,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     (jk < kStagesK || mbar_test(bar(kBarKEmpty + jk % kStagesK), ((jk / kStagesK) - 1) & 1))) {
                     const int s = jk % kStagesK, z = key0 + jk * kKeysTC;
                     mbar_expect_tx(bar(kBarKFull + s), kStageBytes);
-                    tma_load_3d(kstage(s), &tmK, 0, h, z, bar(kBarKFull + s));
-                    tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, h, z, bar(kBarKFull + s));
+                    tma_load_3d(kstage(s), &tmK, 0, hk, z, bar(kBarKFull + s));
+                    tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, hk, z, bar(kBarKFull + s));
                     jk++;
                     progress = true;
                 }
@@ -548,8 +550,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
                     const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
                     mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
-                    tma_load_3d(vstage(s), &tmV, 0, h, z, bar(kBarVFull + s));
-                    tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, h, z, bar(kBarVFull + s));
+                    tma_load_3d(vstage(s), &tmV, 0, hk, z, bar(kBarVFull + s));
+                    tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, hk, z, bar(kBarVFull + s));
                     jv++;
                     progress = true;
                 }

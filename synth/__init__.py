@@ -11,9 +11,10 @@ datasets are not used: the synthetic shapes below stand in for them.
 
 Layouts (all contiguous, row-major):
     q             [B, Lq, H, D]            fp16
-    sys_k, sys_v  [Ls, H, D]               fp16   shared system-prompt cache
+    sys_k, sys_v  [Ls, Hkv, D]             fp16   shared system-prompt cache
     k_cache,
-    v_cache       [num_blocks, H, 16, D]   fp16   paged context pool
+    v_cache       [num_blocks, Hkv, 16, D] fp16   paged context pool
+                  (Hkv KV heads; Hkv = H unless the workload is grouped-query)
     block_tables  [B, max_blocks]          int32  unused entries are -1
     ctx_lens      [B]                      int32  context tokens per request
     q_lens        [B]                      int32  query rows per request
@@ -47,6 +48,7 @@ class Workload:
     chunk_requests: int = 0  # the last `chunk_requests` requests carry Lq query rows, the rest 1
     pool_blocks: Optional[int] = None   # fixed pool size (else needed blocks + 10% spare)
     spare_frac: float = 0.10
+    Hkv: Optional[int] = None           # KV heads (None: H, multi-head)
 
 
 # The five workloads.  Context-length draws are integer and inclusive.
@@ -62,6 +64,16 @@ WORKLOADS = {
     "llama2_13b_mixed": Workload("llama2_13b_mixed", B=64, H=40, D=128, Ls=32768,
                                  ctx_dist=("uniform", 1, 4096), value_scale=0.5,
                                  Lq=128, chunk_requests=8),
+    # Grouped-query attention (not on the pages; all five workloads above are
+    # multi-head): the Llama-2-70B attention shape, 64 query heads over 8 KV
+    # heads, with the Llama-2-7B workload's batch, prompt and contexts; and
+    # small CPU-checkable grouped (2 KV heads) and multi-query (1) cases.
+    "llama2_70b_gqa": Workload("llama2_70b_gqa", B=32, H=64, D=128, Ls=2048,
+                               ctx_dist=("uniform", 64, 1024), value_scale=0.5, Hkv=8),
+    "tiny_gqa": Workload("tiny_gqa", B=4, H=8, D=64, Ls=256, ctx_dist=("uniform", 1, 64),
+                         value_scale=1.0, pool_blocks=32, Hkv=2),
+    "tiny_mqa": Workload("tiny_mqa", B=4, H=4, D=64, Ls=256, ctx_dist=("uniform", 1, 64),
+                         value_scale=1.0, pool_blocks=32, Hkv=1),
 }
 
 SWEEP_LS = (512, 1024, 2048, 4096, 8192, 16384)
@@ -96,6 +108,8 @@ class Case:
     def D(self): return self.q.shape[3]
     @property
     def Ls(self): return self.sys_k.shape[0]
+    @property
+    def Hkv(self): return self.k_cache.shape[1]
     @property
     def num_blocks(self): return self.k_cache.shape[0]
     @property
@@ -146,6 +160,8 @@ def make_case(wl, seed: int = 0, ctx_lens: Optional[list] = None, q_lens: Option
         wl = WORKLOADS[wl]
     g = torch.Generator().manual_seed(seed)
     B, H, D, Ls, Lq = wl.B, wl.H, wl.D, wl.Ls, wl.Lq
+    Hkv = H if wl.Hkv is None else wl.Hkv
+    assert H % Hkv == 0
     drawn = _draw_ctx_lens(wl, g)
     if ctx_lens is None:
         ctx_lens = drawn
@@ -164,10 +180,10 @@ def make_case(wl, seed: int = 0, ctx_lens: Optional[list] = None, q_lens: Option
         num_blocks = max(1, needed + int(math.ceil(wl.spare_frac * needed)))
 
     q = _randn_f16((B, Lq, H, D), g, wl.value_scale)
-    sys_k = _randn_f16((Ls, H, D), g, wl.value_scale)
-    sys_v = _randn_f16((Ls, H, D), g, wl.value_scale)
-    k_cache = _randn_f16((num_blocks, H, BLOCK_SIZE, D), g, wl.value_scale)
-    v_cache = _randn_f16((num_blocks, H, BLOCK_SIZE, D), g, wl.value_scale)
+    sys_k = _randn_f16((Ls, Hkv, D), g, wl.value_scale)
+    sys_v = _randn_f16((Ls, Hkv, D), g, wl.value_scale)
+    k_cache = _randn_f16((num_blocks, Hkv, BLOCK_SIZE, D), g, wl.value_scale)
+    v_cache = _randn_f16((num_blocks, Hkv, BLOCK_SIZE, D), g, wl.value_scale)
 
     perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
     block_tables = torch.full((B, max_blocks), -1, dtype=torch.int32)
@@ -220,7 +236,7 @@ def with_system_in_pool(case: Case):
     paged-attention system uses, where every request's table begins with the
     shared system blocks.  The tail of the last system block is NaN.
     """
-    Ls, H, D = case.Ls, case.H, case.D
+    Ls, H, D = case.Ls, case.Hkv, case.D
     n_sys = -(-Ls // BLOCK_SIZE)
     pad = n_sys * BLOCK_SIZE - Ls
     def to_blocks(x):

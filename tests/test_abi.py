@@ -40,14 +40,14 @@ def test_dims_layout_matches_header(relay, tmp_path):
     prog = tmp_path / "layout.c"
     prog.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "relay.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(relay_dims_t),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(relay_dims_t),"
         " offsetof(relay_dims_t, max_q_total), offsetof(relay_dims_t, sys_range),"
-        " offsetof(relay_dims_t, scale));return 0;}\n")
+        " offsetof(relay_dims_t, scale), offsetof(relay_dims_t, Hkv));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     D = relay.Dims
-    assert got == [ctypes.sizeof(D), D.max_q_total.offset, D.sys_range.offset, D.scale.offset]
+    assert got == [ctypes.sizeof(D), D.max_q_total.offset, D.sys_range.offset, D.scale.offset, D.Hkv.offset]
 
 
 def test_status_strings(relay):
@@ -58,7 +58,7 @@ def test_status_strings(relay):
 
 def _dims(relay, **kw):
     base = dict(B=32, Lq=1, H=32, D=128, Ls=2048, block_size=16, num_blocks=1200, max_blocks_per_seq=64,
-                max_q_total=0, ctx_split=0, sys_range=0, scale=0.0)
+                max_q_total=0, ctx_split=0, sys_range=0, scale=0.0, Hkv=0)
     base.update(kw)
     return relay.Dims(**base)
 
@@ -70,13 +70,16 @@ def test_workspace_size(relay):
     assert lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64))) > n
     assert lib.relay_workspace_size(None) == 0
     for bad in (dict(D=96), dict(block_size=32), dict(B=513), dict(H=0), dict(Lq=0), dict(Ls=-1),
-                dict(ctx_split=100), dict(sys_range=-64)):
+                dict(ctx_split=100), dict(sys_range=-64), dict(Hkv=-1), dict(Hkv=3), dict(Hkv=64)):
         assert lib.relay_workspace_size(ctypes.byref(_dims(relay, **bad))) == 0, bad
     # a bound on the total query rows shrinks the partial storage
     big = lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64, Lq=128, H=40, Ls=32768, max_blocks_per_seq=256)))
     small = lib.relay_workspace_size(ctypes.byref(_dims(relay, B=64, Lq=128, H=40, Ls=32768, max_blocks_per_seq=256,
                                                         max_q_total=1080)))
     assert small < big / 4
+    # grouped-query heads: any divisor of H, the partials stay per query head
+    for hkv in (1, 8, 32):
+        assert lib.relay_workspace_size(ctypes.byref(_dims(relay, Hkv=hkv))) == n
 
 
 FAKE = 0x7f0000000000      # never dereferenced: validation fails first
@@ -98,6 +101,7 @@ def test_host_validation(relay):
     assert _call_decode(relay, None) == relay.ERR_INVALID_ARG
     assert _call_decode(relay, _dims(relay, D=96)) == relay.ERR_UNSUPPORTED
     assert _call_decode(relay, _dims(relay, block_size=8)) == relay.ERR_UNSUPPORTED
+    assert _call_decode(relay, _dims(relay, Hkv=5)) == relay.ERR_INVALID_ARG   # 32 query heads, 5 KV heads
     assert _call_decode(relay, _dims(relay, B=1024)) == relay.ERR_UNSUPPORTED
     assert _call_decode(relay, d, q=None) == relay.ERR_INVALID_ARG
     assert _call_decode(relay, d, out=None) == relay.ERR_INVALID_ARG

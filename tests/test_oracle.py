@@ -209,6 +209,8 @@ def _relay_decomposed(oracle_lib, case):
     ("llama30b_sweep", dict(B=3, H=3, Ls=512)),
     ("llama2_7b_b256", dict(B=5, H=2, Ls=128)),
     ("llama2_13b_mixed", dict(B=6, H=2, Ls=256, Lq=8, chunk_requests=2, ctx_dist=("uniform", 1, 96))),
+    ("tiny_gqa", {}),
+    ("tiny_mqa", dict(Lq=3, chunk_requests=2)),
 ])
 def test_relay_identity(oracle_lib, name, over):
     case = synth.make_case(synth.workload(name, **over), seed=11)
@@ -282,3 +284,53 @@ def test_scale_is_applied(oracle_lib):
     assert not np.allclose(o1, o2)
     o_ref, l_ref = _numpy_brute(case, 0.5)
     np.testing.assert_allclose(o1, o_ref, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- grouped-query heads
+# Query head h reads KV head h / (H / Hkv).  Two pins that do not restate that
+# formula: the multi-head oracle (pinned above) over caches whose KV heads are
+# expanded with torch.repeat_interleave, and torch's fp64 scaled-dot-product
+# attention with its own grouped-query option.  Both fail for a wrong
+# grouping (for example h % Hkv).
+def _expand_kv(case):
+    G = case.H // case.Hkv
+    ex = lambda t: t.repeat_interleave(G, dim=1).contiguous()
+    from dataclasses import replace
+    return synth.Case(replace(case.wl, Hkv=None), case.seed, case.q, ex(case.sys_k), ex(case.sys_v),
+                      ex(case.k_cache), ex(case.v_cache), case.block_tables, case.ctx_lens, case.q_lens)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny_gqa", {}),
+    ("tiny_mqa", {}),
+    ("tiny_gqa", dict(Lq=3, chunk_requests=2)),
+    ("tiny_gqa", dict(H=8, Hkv=4, Ls=0)),
+])
+def test_gqa_equals_multi_head_on_expanded_kv(oracle_lib, name, over):
+    case = synth.make_case(synth.workload(name, **over), seed=13)
+    assert case.Hkv < case.H
+    full = _expand_kv(case)
+    assert full.Hkv == full.H
+    o, l = oracle_lib.attention_full(case)
+    o2, l2 = oracle_lib.attention_full(full)
+    ok = ~np.isnan(l2)
+    np.testing.assert_array_equal(o[ok], o2[ok])
+    np.testing.assert_array_equal(l[ok], l2[ok])
+
+
+@pytest.mark.parametrize("name", ["tiny_gqa", "tiny_mqa"])
+def test_gqa_sdpa_fp64(oracle_lib, name):
+    case = synth.make_case(name, seed=17)
+    o, l = oracle_lib.attention_full(case)
+    q = case.q.double()
+    for b in range(case.B):
+        n = int(case.ctx_lens[b])
+        t = torch.arange(n)
+        blk = case.block_tables[b, (t // 16)].long()
+        kc = case.k_cache[blk, :, t % 16].double()                            # [n, Hkv, D]
+        vc = case.v_cache[blk, :, t % 16].double()
+        K = torch.cat([case.sys_k.double(), kc], 0).transpose(0, 1)         # [Hkv, L, D]
+        V = torch.cat([case.sys_v.double(), vc], 0).transpose(0, 1)
+        Q = q[b, :1].transpose(0, 1)                                         # [H, 1, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, enable_gqa=True)
+        np.testing.assert_allclose(o[b, :1], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)

@@ -246,7 +246,7 @@ def test_deterministic_and_workspace_reuse():
     import shared_prompt_decode_gb300 as relay
     case = synth.make_case("llama2_7b", 14)
     g = T.to_dev(case)
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv)
     ws = relay.make_workspace(dims)
     outs = [T.run_fused(case, ws=ws, g=g) for _ in range(3)]
     for o, l in outs[1:]:
@@ -262,7 +262,7 @@ def test_cuda_graph_replay():
     import shared_prompt_decode_gb300 as relay
     case = synth.make_case("llama2_7b", 15)
     g = T.to_dev(case)
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv)
     ws = relay.make_workspace(dims)
     out = torch.empty_like(g["q"])
     ref, _ = T.run_fused(case, g=g)
@@ -345,3 +345,45 @@ def test_tensor_core_system_step(name, B, Lq, Ls, ql):
     out, lse = T.run_fused(case)
     T.check_full(case, out, lse)
     T.check_full(case, out2, lse2)
+
+
+# ----------------------------------------------------------------------------- grouped-query heads
+# Hkv KV heads serve H query heads (query head h reads KV head h / (H / Hkv)):
+# every path -- one call, the three separate steps, the non-relay baseline,
+# multi-row requests, and the tensor-core system step -- against the oracle.
+GQA_CASES = [
+    ("tiny_gqa", {}),
+    ("tiny_mqa", {}),
+    ("tiny_gqa", dict(Lq=3, chunk_requests=2)),
+    ("llama2_70b_gqa", {}),
+]
+
+
+@pytest.mark.parametrize("name,over", GQA_CASES, ids=["gqa", "mqa", "gqa_chunks", "llama2_70b_gqa"])
+def test_grouped_query_heads(name, over):
+    case = synth.make_case(synth.workload(name, **over), 21)
+    assert case.Hkv < case.H
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+    o_s, l_s, o_c, l_c, out2, lse2 = T.run_split(case)
+    m = T.valid_mask(case)
+    ref_s, refl_s = oracle.attention_full(case, "sys")
+    T.check(o_s, ref_s, "o_sys", m)
+    T.check(l_s, refl_s, "lse_sys", m)
+    T.check_full(case, out2, lse2)
+    outb, lseb = T.run_baseline(case)
+    T.check_full(case, outb, lseb)
+
+
+def test_grouped_query_heads_tensor_core_system_step():
+    w = synth.Workload("tc_gqa", B=150, H=4, D=128, Ls=1000, ctx_dist=("uniform", 0, 48), value_scale=0.5,
+                       Lq=2, Hkv=2)
+    case = synth.make_case(w, 23)
+    assert case.total_q() > 256
+    o_s, l_s, o_c, l_c, out2, lse2 = T.run_split(case)
+    m = T.valid_mask(case)
+    ref_s, refl_s = oracle.attention_full(case, "sys")
+    T.check(o_s, ref_s, "o_sys", m)
+    T.check(l_s, refl_s, "lse_sys", m)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)

@@ -43,7 +43,7 @@ def test_noalloc_matches_workspace_entry_point(relay, name, seed):
     case = synth.make_case(name, seed)
     g = T.to_dev(case)
     ref_out, ref_lse = T.run_fused(case, g=g)
-    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv)
     assert relay.workspace_size(dims) <= (32 << 20)
     for call in range(2):                   # the shared buffer keeps the previous call's contents
         out = torch.full_like(g["q"], float("nan"))
