@@ -41,10 +41,19 @@ std::mutex g_mu;
 template <int D>
 cudaError_t prepare_kernel(int *occ)
 {
-    cudaError_t e = cudaFuncSetAttribute(relay_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // both decode flavours (multi-head, grouped-query) use the same shared memory
+    cudaError_t e = cudaFuncSetAttribute(relay_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sizeof(Smem<D>));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(relay_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(Smem<D>));
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, relay_kernel<D>, kThreads, sizeof(Smem<D>));
+    int o1 = 0, o2 = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, relay_kernel<D, false>, kThreads, sizeof(Smem<D>));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, relay_kernel<D, true>, kThreads, sizeof(Smem<D>));
+    *occ = std::min(o1, o2);
+    return e;
 }
 
 relay_status_t device_info(const DevInfo **out)
@@ -248,6 +257,8 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.H = d->H;
     p.Hkv = kv_heads(d);
     p.G = d->H / p.Hkv;
+    p.NG = (p.G + 7) / 8;
+    p.HQ = p.G > 1 ? p.Hkv * p.NG : d->H;
     p.Ls = d->Ls;
     p.num_blocks = d->num_blocks;
     p.max_blocks = d->max_blocks_per_seq;
@@ -295,9 +306,11 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
     if (d->D == 128) {
-        relay_kernel<128><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
+        if (p.G > 1) relay_kernel<128, true><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
+        else relay_kernel<128, false><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
     } else {
-        relay_kernel<64><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+        if (p.G > 1) relay_kernel<64, true><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+        else relay_kernel<64, false><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
 

@@ -72,6 +72,8 @@ enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DONE = 2, CTRL_DEC_ITEMS = 3 };
 struct Params {
     int B, Lq, H, Ls, num_blocks, max_blocks, max_q_total;
     int Hkv, G;                       // KV heads; query heads per KV head (query head h reads KV head h / G)
+    int NG, HQ;                       // decode items per request and split: HQ = Hkv * NG head groups of up
+                                      // to 8 query heads (NG = ceil(G / 8)) when G > 1, else HQ = H
     float scale_log2;                 // softmax scale * log2(e)
     const __half *q, *sys_k, *sys_v, *k_cache, *v_cache;
     const int *block_tables, *ctx_lens, *q_lens;
@@ -334,7 +336,7 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
                 const ReqInfo r = req_info(p, n, ql, p.tps_max);
                 m = p.H * r.ns * r.mt;
             }
-            if (has_ctx(p.mode) && ql == 1) pg = p.H * (pp + (n + kBlock - 1) / kBlock);
+            if (has_ctx(p.mode) && ql == 1) pg = p.HQ * (pp + (n + kBlock - 1) / kBlock);
         }
         vq[k] = ql;
         vm[k] = m;
@@ -406,7 +408,7 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
     for (int k = 0; k < PER; k++) {
         const int pos = tid * PER + k;
         dv[k] = 0;
-        if (pos < s.n_dec_req) dv[k] = p.H * req_info(p, s.nctx[s.order[pos]], 1, tps).ns;
+        if (pos < s.n_dec_req) dv[k] = p.HQ * req_info(p, s.nctx[s.order[pos]], 1, tps).ns;
     }
     block_scan<D, PER>(dv, s.dec, s.n_dec_req, s);
     if (tid == 0 && s.qo[p.B] > p.max_q_total) s.bad |= FLAG_Q_TOTAL;
@@ -944,12 +946,16 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
 // ============================================================================= phase 2: decode items
 // A decode item, decoded by every lane of the warp.  Lane j also holds the
 // physical block of the item's page j (fetched when the item is decoded, so
-// the page loads never wait on a block-table lookup) and lanes 0..3 hold the
-// query as the B operand of S^T = K q.
+// the page loads never wait on a block-table lookup) and the lanes hold the
+// query rows as the B operand of S^T = K q: multi-head, one query head in
+// column 0 (lanes 0..3); grouped-query (GRP), the item's nh <= 8 query heads
+// h .. h+nh-1, all reading KV head hk, in columns 0..nh-1 (lanes 4c..4c+3),
+// so one pass over the pages serves the whole head group.
 template <int D>
 struct DecItem {
     int id;          // queue index, or -1 when the queue is exhausted
     int b, h, split;
+    int hk, nh;      // KV head; query heads in the item
     int p0, np;      // first page and page count of the item
     int pp;          // prefix pages of the request's key sequence
     int n_ctx;
@@ -957,7 +963,7 @@ struct DecItem {
     unsigned qb[D / 16][2];
 };
 
-template <int D>
+template <int D, bool GRP>
 __device__ __forceinline__ void dec_item(const Params &p, const Smem<D> &s, int id, int n_dec, DecItem<D> &it)
 {
     const int lane = threadIdx.x & 31;
@@ -971,7 +977,16 @@ __device__ __forceinline__ void dec_item(const Params &p, const Smem<D> &s, int 
     const ReqInfo ri = req_info(p, it.n_ctx, 1, s.tps);
     const int j = id - s.dec[pos];
     it.split = j % ri.ns;
-    it.h = j / ri.ns;
+    const int hq = j / ri.ns;
+    if (GRP) {
+        const int sub = hq % p.NG;
+        it.hk = hq / p.NG;
+        it.h = it.hk * p.G + 8 * sub;
+        it.nh = min(8, p.G - 8 * sub);
+    } else {
+        it.h = it.hk = hq;
+        it.nh = 1;
+    }
     it.p0 = it.split * ri.pages / ri.ns;
     it.np = (it.split + 1) * ri.pages / ri.ns - it.p0;
     it.pp = ri.pp;
@@ -980,13 +995,15 @@ __device__ __forceinline__ void dec_item(const Params &p, const Smem<D> &s, int 
         const int pg = it.p0 + lane;
         it.blk = pg < it.pp ? p.prefix_ids[pg] : p.block_tables[(size_t)it.b * p.max_blocks + (pg - it.pp)];
     }
-    const __half *q = p.q + ((size_t)it.b * p.Lq * p.H + it.h) * D;
+    // column n of the B operand (lanes 4n..4n+3): rows k = 2*tig, 2*tig+1 (b0) and +8 (b1)
+    const int n = lane >> 2;
+    const bool has = n < it.nh;
+    const __half *q = p.q + ((size_t)it.b * p.Lq * p.H + it.h + (has ? n : 0)) * D;
 #pragma unroll
     for (int kt = 0; kt < D / 16; kt++) {
-        // column 0 of the B operand: rows k = 2*tig, 2*tig+1 (b0) and +8 (b1), lanes 0..3
         const int c = kt * 16 + 2 * (lane & 3);
-        it.qb[kt][0] = lane < 4 ? ld_u32(q + c) : 0u;
-        it.qb[kt][1] = lane < 4 ? ld_u32(q + c + 8) : 0u;
+        it.qb[kt][0] = has ? ld_u32(q + c) : 0u;
+        it.qb[kt][1] = has ? ld_u32(q + c + 8) : 0u;
     }
 }
 
@@ -1007,7 +1024,7 @@ __device__ __forceinline__ void load_page(const Params &p, __half *K, __half *V,
     const int rows = page_rows(p, it.pp, it.n_ctx, it.p0 + j);
     const bool ok = blk >= 0 && blk < p.num_blocks;
     if (!ok && lane == 0) atomicOr(&p.ctrl[CTRL_FLAGS], FLAG_BAD_BLOCK);
-    const size_t base = (((size_t)(ok ? blk : 0) * p.Hkv + it.h / p.G) * kBlock) * D;
+    const size_t base = (((size_t)(ok ? blk : 0) * p.Hkv + it.hk) * kBlock) * D;
 #pragma unroll
     for (int k = 0; k < PER; k++) {
         int c = lane + k * 32;
@@ -1107,12 +1124,125 @@ __device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem<D>
     if (lane == 0) __stcg(p.part_lse + pr, L > 0.f ? st.m + lg2(L) : kNegInf);
 }
 
+// 8x8 transpose of a b16 matrix held in the accumulator fragment layout
+// (lane 4r + c: row r, columns 2c, 2c+1): the same lane then holds row r of
+// the transpose.
+__device__ __forceinline__ unsigned movmatrix_t(unsigned x)
+{
+    unsigned y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Grouped-query state: lane (g, tig) owns columns 2*tig and 2*tig+1 (query
+// heads h + 2*tig + e) of O^T and their softmax statistics.
+template <int D>
+struct DecStateG {
+    float o[D / 16][4];   // O^T: d = 16*mt + g (c0: col 2tig, c1: col 2tig+1), d + 8 (c2, c3)
+    float m[2];           // running max per owned column (log2 domain)
+    float l[2];           // lane partials of the normalisers
+};
+
+// One warp, one page, up to 8 query heads of one KV head: S^T = K Q (16 keys
+// on M, the heads on N), an online softmax per column, O^T += V^T P.  P moves
+// from the accumulator layout of S^T into the B-operand layout with two 8x8
+// transposes (keys 0-7 and 8-15).
+template <int D>
+__device__ __forceinline__ void dec_page_grp(const __half *K, const __half *V, const unsigned (&qb)[D / 16][2],
+                                             DecStateG<D> &st, int valid_rows, int nh, float scale_log2)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kt = 0; kt < D / 16; kt++) {
+        unsigned a[4];
+        int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+        int ch = 2 * kt + (lane >> 4);
+        ldsm_x4(a[0], a[1], a[2], a[3], K + swz<D>(row, ch));
+        mma16816(acc, a, qb[kt][0], qb[kt][1]);
+    }
+    // lane (g, tig): acc[0..1] = key g, columns 2tig, 2tig+1; acc[2..3] = key g+8
+    const bool c0 = 2 * tig < nh, c1 = 2 * tig + 1 < nh;
+    const bool r0 = g < valid_rows, r1 = g + 8 < valid_rows;
+    const float s00 = (c0 && r0) ? acc[0] * scale_log2 : kNegInf;
+    const float s01 = (c1 && r0) ? acc[1] * scale_log2 : kNegInf;
+    const float s10 = (c0 && r1) ? acc[2] * scale_log2 : kNegInf;
+    const float s11 = (c1 && r1) ? acc[3] * scale_log2 : kNegInf;
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {      // over the 8 key rows g, for each column
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float mu0 = (mn0 == kNegInf) ? 0.f : mn0, mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+    if (__any_sync(0xffffffffu, mn0 != st.m[0] || mn1 != st.m[1])) {
+        const float al0 = ex2(st.m[0] - mu0), al1 = ex2(st.m[1] - mu1);
+        st.l[0] *= al0;
+        st.l[1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            st.o[mt][0] *= al0;
+            st.o[mt][2] *= al0;
+            st.o[mt][1] *= al1;
+            st.o[mt][3] *= al1;
+        }
+        st.m[0] = mn0;
+        st.m[1] = mn1;
+    }
+    const float p00 = ex2(s00 - mu0), p01 = ex2(s01 - mu1), p10 = ex2(s10 - mu0), p11 = ex2(s11 - mu1);
+    st.l[0] += p00 + p10;
+    st.l[1] += p01 + p11;
+    // B operand P[16 keys x 8 heads]: lane (g, tig) needs keys 2tig, 2tig+1 of
+    // head g (b0) and keys 2tig+8, 2tig+9 (b1): the transposes of the lane's
+    // (key g, heads 2tig..2tig+1) and (key g+8, ...) pairs.
+    const unsigned b0 = movmatrix_t(pack_half2(p00, p01));
+    const unsigned b1 = movmatrix_t(pack_half2(p10, p11));
+#pragma unroll
+    for (int mt = 0; mt < D / 16; mt++) {
+        unsigned a[4];
+        int row = (lane & 7) + ((lane >> 4) << 3);
+        int ch = 2 * mt + ((lane >> 3) & 1);
+        ldsm_x4_t(a[0], a[1], a[2], a[3], V + swz<D>(row, ch));
+        mma16816(st.o[mt], a, b0, b1);
+    }
+}
+
+// Finish a grouped decode item: one partial (normalised output, log2-sum-exp)
+// per query head of the group.
+template <int D>
+__device__ void dec_epilogue_grp(const Params &p, const Smem<D> &s, const DecItem<D> &it, DecStateG<D> &st)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    float L[2] = {st.l[0], st.l[1]};
+#pragma unroll
+    for (int e = 0; e < 2; e++)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) L[e] += __shfl_xor_sync(0xffffffffu, L[e], off);
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int c = 2 * tig + e;
+        if (c >= it.nh) continue;
+        const float inv = L[e] > 0.f ? 1.f / L[e] : 0.f;
+        const size_t pr = part_row(p, p.ctx_base + it.split, s.qo[it.b], it.h + c);
+        float *po = p.part_o + pr * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            __stcg(po + 16 * mt + g, st.o[mt][e] * inv);
+            __stcg(po + 16 * mt + g + 8, st.o[mt][2 + e] * inv);
+        }
+        if (g == 0) __stcg(p.part_lse + pr, L[e] > 0.f ? st.m[e] + lg2(L[e]) : kNegInf);
+    }
+}
+
 // Phase 2 for one warp: pull decode items until the queue is empty, streaming
 // pages through the warp's ring and prefetching across item boundaries.  The
 // item after the current one is decoded (block ids and query loads issued)
 // as soon as the current one starts, and the queue ticket after that is
 // requested at the same time, so no item start waits on memory.
-template <int D>
+template <int D, bool GRP>
 __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
@@ -1128,7 +1258,7 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
     };
     auto take = [&](DecItem<D> &it) {
         int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
-        dec_item<D>(p, s, id, n_dec, it);
+        dec_item<D, GRP>(p, s, id, n_dec, it);
         if (++taken == 1) ticket = n_w + blockIdx.x * kWarps + warp;
         else if (it.id >= 0) request();
     };
@@ -1167,24 +1297,40 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 
     fill();
     for (;;) {
-        DecState<D> st;
+        DecState<D> st;        // multi-head
+        DecStateG<D> stg_;     // grouped-query
+        if (GRP) {
 #pragma unroll
-        for (int mt = 0; mt < D / 16; mt++)
+            for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
-            for (int e = 0; e < 4; e++) st.o[mt][e] = 0.f;
-        st.m = kNegInf;
-        st.l = 0.f;
+                for (int e = 0; e < 4; e++) stg_.o[mt][e] = 0.f;
+            stg_.m[0] = stg_.m[1] = kNegInf;
+            stg_.l[0] = stg_.l[1] = 0.f;
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; mt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) st.o[mt][e] = 0.f;
+            st.m = kNegInf;
+            st.l = 0.f;
+        }
         for (int j = 0; j < cur.np; j++) {
             cp_async_wait_dyn(issued - computed - 1);
             __syncwarp();
             const int stg = computed % S;
-            dec_page<D>(s.wk(warp, stg), s.wv(warp, stg), cur.qb, st, page_rows(p, cur.pp, cur.n_ctx, cur.p0 + j),
-                        p.scale_log2);
+            const int rows = page_rows(p, cur.pp, cur.n_ctx, cur.p0 + j);
+            if (GRP)
+                dec_page_grp<D>(s.wk(warp, stg), s.wv(warp, stg), cur.qb, stg_, rows, cur.nh, p.scale_log2);
+            else
+                dec_page<D>(s.wk(warp, stg), s.wv(warp, stg), cur.qb, st, rows, p.scale_log2);
             __syncwarp();
             computed++;
             fill();
         }
-        dec_epilogue<D>(p, s, cur, st);
+        if (GRP)
+            dec_epilogue_grp<D>(p, s, cur, stg_);
+        else
+            dec_epilogue<D>(p, s, cur, st);
         if (nxt.id < 0) break;
         // nxt becomes current (its pages already issued stay in flight), and
         // the item after it is decoded now
@@ -1199,7 +1345,8 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 }
 
 // ============================================================================= persistent kernel
-template <int D>
+// GRP: decode items serve a group of query heads sharing one KV head (G > 1)
+template <int D, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1237,7 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
         }
     }
     // phase 2: decode items, each warp on its own
-    if (n_dec > 0) decode_phase<D>(p, s, n_dec);
+    if (n_dec > 0) decode_phase<D, GRP>(p, s, n_dec);
     __syncthreads();
     // this CTA's partials are written: the merge kernel may be launched
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
