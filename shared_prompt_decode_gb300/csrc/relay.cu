@@ -100,6 +100,7 @@ relay_status_t check_dims(const relay_dims_t *d)
     if (d->B > kMaxB) return RELAY_ERR_UNSUPPORTED;
     // 32-bit item and row counters on the device
     if ((int64_t)d->B * d->Lq > INT_MAX / 2 || (int64_t)d->B * d->H > INT_MAX / 2 ||
+        (int64_t)d->B * d->Lq * d->H > INT_MAX / 2 ||     // virtual rows of the system step
         (int64_t)d->max_blocks_per_seq * kBlock + d->Ls > INT_MAX / 2)
         return RELAY_ERR_UNSUPPORTED;
     return RELAY_OK;
@@ -159,14 +160,16 @@ Plan make_plan(const relay_dims_t *d, int mode)
     const bool sys = mode == MODE_FUSED || mode == MODE_SYS;
     const bool ctx = mode != MODE_SYS;
     pl.n_prefix = mode == MODE_BASELINE ? d->Ls : 0;
-    pl.tc = sys && d->D == 128 && d->Ls > 0 && pl.Mtot > kTcMinRows;
+    const int G = d->H / kv_heads(d);            // query heads per KV head
+    const long long Mv = (long long)pl.Mtot * G;   // rows of the system step per KV head
+    pl.tc = sys && d->D == 128 && d->Ls > 0 && Mv > kTcMinRows;
     if (pl.tc) {
         // (head, tile pair, key range) items, one CTA each.  The number of
         // ranges R minimises the makespan in waves of one CTA per SM times
         // keys per range, ceil(n R / SMs) / R, among ranges of at least
         // 2048 keys (so the partials stay small); the smallest R within 2%
         // of the best wins.
-        const long long n = (long long)tc_pairs(pl.Mtot) * d->H;
+        const long long n = (long long)tc_pairs((int)Mv) * kv_heads(d);
         const int r_cap = std::max(1, d->Ls / 2048);
         double best = 1e30;
         int r_best = 1;
@@ -190,8 +193,11 @@ Plan make_plan(const relay_dims_t *d, int mode)
                 // Enough system items to spread over the GPU, but long enough
                 // ranges that each range's partial results stay small next to
                 // the system keys it streams.
-                int tiles = (pl.Mtot + kTileM - 1) / kTileM;
-                int r_want = (kGridTarget + d->H * tiles - 1) / (d->H * tiles);
+                const int tiles = (int)((Mv + kTileM - 1) / kTileM);
+                const int hkv = kv_heads(d);
+                int r_want = (kGridTarget + hkv * tiles - 1) / (hkv * tiles);
+                // cap on the ranges from the query rows per head (not the
+                // virtual rows of a head group), so the items stay short
                 int r_cap = d->Ls / std::max(256, 16 * pl.Mtot);
                 int r = std::max(1, std::min(r_want, r_cap));
                 range = round_up((d->Ls + r - 1) / r, kTileK);
@@ -287,6 +293,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.Lq = d->Lq;
         t.H = d->H;
         t.G = p.G;
+        t.Hkv = p.Hkv;
         t.Ls = d->Ls;
         t.max_q_total = pl.Mtot;
         t.scale_log2 = p.scale_log2;
@@ -297,11 +304,11 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.part_lse = p.part_lse;
         t.R = pl.R_sys;
         t.range = pl.sys_range;
-        t.pairs = tc_pairs(pl.Mtot);
+        t.pairs = tc_pairs(pl.Mtot * p.G);
         CUtensorMap tmK, tmV;
         if (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls))
             return RELAY_ERR_CUDA;
-        const long long items = (long long)t.pairs * d->H * pl.R_sys;
+        const long long items = (long long)t.pairs * p.Hkv * pl.R_sys;
         tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }

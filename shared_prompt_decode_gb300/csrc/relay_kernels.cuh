@@ -752,8 +752,8 @@ __device__ __forceinline__ void load_q_rows(unsigned (&qf)[D / 16][4], const __h
 
 // Write one warp's partial rows (normalised output, log2-sum-exp).
 template <int D>
-__device__ __forceinline__ void write_row_partials(const Params &p, const RowState<D> &ws, int part, int h, int rA,
-                                                   bool vA, int rB, bool vB)
+__device__ __forceinline__ void write_row_partials(const Params &p, const RowState<D> &ws, int part, int hA, int rA,
+                                                   bool vA, int hB, int rB, bool vB)
 {
     const int tig = threadIdx.x & 3;
     float l0 = ws.l[0], l1 = ws.l[1];
@@ -766,7 +766,7 @@ __device__ __forceinline__ void write_row_partials(const Params &p, const RowSta
         if (!(half ? vB : vA)) continue;
         float l = half ? l1 : l0, m = ws.m[half];
         float inv = l > 0.f ? 1.f / l : 0.f;
-        size_t pr = part_row(p, part, half ? rB : rA, h);
+        size_t pr = part_row(p, part, half ? rB : rA, half ? hB : hA);
         float *po = p.part_o + pr * D;
 #pragma unroll
         for (int n = 0; n < D / 8; n++)
@@ -852,34 +852,41 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
     team_sync();
 }
 
+// System items run over the virtual rows v = r * G + c of one KV head hk:
+// query row r of the batch with query head hk * G + c, so a KV head's
+// system keys are read once per 64 virtual rows whatever the head grouping
+// (multi-head: G = 1, v = r).
 template <int D>
 __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
 {
-    // heads vary fastest: CTAs that run concurrently read whole [H, D] rows of
-    // the system cache together instead of one head's 256-byte slivers
-    const int T = (Mtot + kTileM - 1) / kTileM;
-    const int h = item % p.H;
-    const int tau = (item / p.H) % T;
-    const int rho = item / (p.H * T);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // KV heads vary fastest: CTAs that run concurrently read whole [Hkv, D]
+    // rows of the system cache together instead of one head's slivers
+    const int Mv = Mtot * p.G;
+    const int T = (Mv + kTileM - 1) / kTileM;
+    const int hk = item % p.Hkv;
+    const int tau = (item / p.Hkv) % T;
+    const int rho = item / (p.Hkv * T);
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2;
 
-    KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.Hkv, h / p.G, 0};
+    KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.Hkv, hk, 0};
     const int key0 = rho * p.sys_range;
     const int key_hi = min(key0 + p.sys_range, p.Ls);
     row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
-    const RowRoles rr = row_roles(min(kTileM, Mtot - tau * kTileM));
-    const int rW = tau * kTileM + rr.rg * 16;
-    const int rA = rW + g, rB = rA + 8;
+    const RowRoles rr = row_roles(min(kTileM, Mv - tau * kTileM));
+    const int vW = tau * kTileM + rr.rg * 16;
+    const int vA = vW + g, vB = vA + 8;
+    const int rA = vA / p.G, hA = hk * p.G + vA % p.G;
+    const int rB = vB / p.G, hB = hk * p.G + vB % p.G;
     const __half *qa = nullptr, *qb = nullptr;
-    if (rA < Mtot) {
+    if (vA < Mv) {
         int b = find_owner(s.qo, p.B, rA);
-        qa = p.q + (((size_t)b * p.Lq + (rA - s.qo[b])) * p.H + h) * D;
+        qa = p.q + (((size_t)b * p.Lq + (rA - s.qo[b])) * p.H + hA) * D;
     }
-    if (rB < Mtot) {
+    if (vB < Mv) {
         int b = find_owner(s.qo, p.B, rB);
-        qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + h) * D;
+        qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + hB) * D;
     }
     unsigned qf[D / 16][4];
     load_q_rows<D>(qf, qa, qb);
@@ -891,7 +898,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
-    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, rho, h, rA, rA < Mtot, rB, rB < Mtot);
+    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
 }
 
 // Context item of a request with several query rows (causal within the context).
@@ -940,7 +947,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     ws.l[0] = ws.l[1] = 0.f;
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0)
-        write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, s.qo[b] + iB, iB < ql);
+        write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, h, s.qo[b] + iB, iB < ql);
 }
 
 // ============================================================================= phase 2: decode items
@@ -1364,8 +1371,8 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
         return;    // counters untouched: nothing was scheduled
     }
     const int Mtot = s.qo[p.B];
-    const int T = (Mtot + kTileM - 1) / kTileM;
-    const int n_sys = (has_sys(p.mode) && !p.skip_sys) ? p.H * p.R_sys * T : 0;
+    const int T = (Mtot * p.G + kTileM - 1) / kTileM;     // tiles of virtual rows per KV head
+    const int n_sys = (has_sys(p.mode) && !p.skip_sys) ? p.Hkv * p.R_sys * T : 0;
     const int n_rows = n_sys + s.mq[p.B];
     const int n_dec = s.dec[s.n_dec_req];
 

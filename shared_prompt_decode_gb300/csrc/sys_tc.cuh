@@ -4,8 +4,11 @@
 // "RelayAttention": the per-request matrix-vector products over the shared
 // system prompt grouped into one matrix-matrix product).
 //
-// One CTA per item: head h, a pair of 128-row tiles of the batch's query
-// rows, a range of system keys.  Both tiles share every K/V stage.  Warps
+// One CTA per item: KV head hk, a pair of 128-row tiles of its virtual rows
+// (v = r * G + c: query row r of the batch with query head hk * G + c, so
+// under grouped-query attention the heads of a group share every K/V stage
+// too; multi-head: G = 1, v = r), a range of system keys.  Both tiles share
+// every K/V stage.  Warps
 // have fixed roles:
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile; row t of a tile
 //                   lives in TMEM lane t and is owned by thread t, so the
@@ -282,8 +285,9 @@ struct TcParams {
     unsigned *flags;
     float *part_o, *part_lse;        // partial slots: [part][max_q_total][H][128]
     int R, range;                    // key ranges of the system prompt
-    int pairs;                       // tile pairs in the grid: ceil(ceil(max_q_total / 128) / 2)
+    int pairs;                       // tile pairs in the grid: ceil(ceil(max_q_total * G / 128) / 2)
     int G;                           // query heads per KV head: head h reads KV head h / G
+    int Hkv;                         // KV heads
 };
 
 __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
@@ -298,7 +302,7 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 
 
 
-// blockIdx.x = (range * pairs + pair) * H + h.  tmK / tmV view sys_k / sys_v
+// blockIdx.x = (range * pairs + pair) * Hkv + hk.  tmK / tmV view sys_k / sys_v
 // as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
 __global__ void __launch_bounds__(kThreadsTC, 1)
     sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const TcParams p)
@@ -327,11 +331,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (tid == 0) abort_sh = 0;
     __syncthreads();
     const int Mtot = min(qo[p.B], p.max_q_total);
-    const int T = (Mtot + kRowsTC - 1) / kRowsTC;
-    const int h = blockIdx.x % p.H;
-    const int pair = (blockIdx.x / p.H) % p.pairs;
-    const int rho = blockIdx.x / (p.H * p.pairs);
-    const int hk = h / p.G;                          // KV head
+    const int Mv = Mtot * p.G;                       // virtual rows of a KV head
+    const int T = (Mv + kRowsTC - 1) / kRowsTC;
+    const int hk = blockIdx.x % p.Hkv;
+    const int pair = (blockIdx.x / p.Hkv) % p.pairs;
+    const int rho = blockIdx.x / (p.Hkv * p.pairs);
     if (2 * pair >= T || rho >= p.R) return;        // the whole CTA leaves together
     const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
     const int key0 = rho * p.range;
@@ -375,8 +379,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int row = tid & 127;
         const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
         const int tile = 2 * pair + wg;
-        const int r = tile * kRowsTC + row;
-        const bool row_ok = wg < n_act && r < Mtot;
+        const int v = tile * kRowsTC + row;              // virtual row: query row r, query head h
+        const bool row_ok = wg < n_act && v < Mv;
+        const int r = v / p.G, h = hk * p.G + v % p.G;
         {
             // this row's query into the K-major, 128-byte-swizzled Q tile
             const __half *qrow = p.q;

@@ -375,11 +375,15 @@ def test_grouped_query_heads(name, over):
     T.check_full(case, outb, lseb)
 
 
-def test_grouped_query_heads_tensor_core_system_step():
-    w = synth.Workload("tc_gqa", B=150, H=4, D=128, Ls=1000, ctx_dist=("uniform", 0, 48), value_scale=0.5,
-                       Lq=2, Hkv=2)
+# The system step runs over virtual rows (query row, query head of the group)
+# of each KV head: 300 rows x 2 heads, and 48 decode rows x 8 heads of one KV
+# head, where only the grouping takes it past 256 rows onto the tensor cores.
+@pytest.mark.parametrize("B,Lq,H,Hkv", [(150, 2, 4, 2), (48, 1, 8, 1)], ids=["rows300_g2", "rows48_mqa8"])
+def test_grouped_query_heads_tensor_core_system_step(B, Lq, H, Hkv):
+    w = synth.Workload("tc_gqa", B=B, H=H, D=128, Ls=1000, ctx_dist=("uniform", 0, 48), value_scale=0.5,
+                       Lq=Lq, Hkv=Hkv)
     case = synth.make_case(w, 23)
-    assert case.total_q() > 256
+    assert case.total_q() * (H // Hkv) > 256
     o_s, l_s, o_c, l_c, out2, lse2 = T.run_split(case)
     m = T.valid_mask(case)
     ref_s, refl_s = oracle.attention_full(case, "sys")
