@@ -377,6 +377,21 @@ def run_relay(args):
     h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4 + (0 if hql is None else hql.numel() * 4)
     d2h = hout.numel() * hout.element_size()
 
+    # the cache write that precedes the step: this step's new K/V rows into the pool (timed like the step)
+    gk = torch.Generator().manual_seed(args.seed + 7)
+    kv_shape = (case.B, case.Lq, case.Hkv, case.D)
+    k_new = torch.randn(*kv_shape, generator=gk).half().to(dev)
+    v_new = torch.randn(*kv_shape, generator=gk).half().to(dev)
+    kc_scratch, vc_scratch = g["k_cache"].clone(), g["v_cache"].clone()
+    ws_a = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def append_step():
+        relay.relay_kv_append(k_new, v_new, g["block_tables"], g["ctx_lens"], kc_scratch, vc_scratch,
+                              q_lens=g["q_lens"], workspace=ws_a)
+    ms_a, _ = timed(as_graph(append_step), max(5, args.steps // 4), args.warmup)
+    append_bytes = 2 * 2 * rows * case.Hkv * case.D * 2          # K and V rows, read once and written once
+    del kc_scratch, vc_scratch
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=200)
@@ -405,6 +420,9 @@ def run_relay(args):
         "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(case) * args.steps,
+        "kv_append": {"kernel": "kv_append_kernel (relay_kv_append: the step's new K/V rows into the pool)",
+                      "us": 1e3 * statistics.mean(ms_a), "bytes": append_bytes,
+                      "gbs": append_bytes / (statistics.mean(ms_a) * 1e-3) / 1e9},
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

@@ -166,6 +166,27 @@ relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
                                       const int32_t *q_lens, void *out, float *lse_out,
                                       void *ws, size_t ws_bytes, relay_stream_t stream);
 
+/* KV append: the step's new keys and values into the paged context pool (the
+ * cache write that precedes attention in every decode iteration; the
+ * RelayAttention pages keep the request contexts in the paged cache and move
+ * only the system prompt to a separate one, atyun.com RelayAttention article,
+ * section "RelayAttention").  Row i < q_lens[b] of request b is context
+ * position pos = ctx_lens[b] - q_lens[b] + i (ctx_lens already counts the
+ * new tokens, as attention does); its row of every KV head hk is copied
+ *     k_cache[blk][hk][pos % 16][:] = k_new[b][i][hk][:]   (and v alike),
+ * blk = block_tables[b][pos / 16], bit for bit.  k_new, v_new: [B, Lq, Hkv,
+ * D] fp16, 16-byte aligned; dims->num_blocks, max_blocks_per_seq, Hkv as for
+ * attention (dims->Ls is not used).  A request whose q_len is outside
+ * [0, Lq] or whose ctx_len is below its q_len or above
+ * 16*max_blocks_per_seq is skipped, and so is a row whose block id is
+ * outside [0, num_blocks); each raises its RELAY_FLAG_* in the workspace
+ * (relay_device_status).  ws: at least 256 bytes (only the flag word is
+ * used; a workspace sized by relay_workspace_size serves). */
+relay_status_t relay_kv_append(const relay_dims_t *dims, const void *k_new, const void *v_new,
+                               const int32_t *block_tables, const int32_t *ctx_lens,
+                               const int32_t *q_lens, void *k_cache, void *v_cache,
+                               void *ws, size_t ws_bytes, relay_stream_t stream);
+
 /* The non-relay formulation, as a paged-attention system with prefix sharing
  * runs it (atyun.com RelayAttention article, section "RelayAttention": the
  * system KVs are read from memory once per request).  The system prompt's KV

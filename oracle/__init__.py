@@ -60,6 +60,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB_PATH)
             lib.oracle_attention_rows.restype = ctypes.c_int
+            lib.oracle_kv_append.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -124,6 +125,24 @@ def attention_rows(case, rows, part: str = "full", scale: float | None = None,
     if rc != 0:
         raise ValueError(f"oracle_attention_rows failed with code {rc}")
     return out[:n], lse[:n]
+
+
+def kv_append(case, k_new, v_new):
+    """The case's pools after appending k_new / v_new ([B, Lq, Hkv, D] fp16)
+    at each request's last q_lens[b] context positions; returns new torch
+    tensors (the case is not modified)."""
+    import torch
+    lib = _load()
+    kc = _u16(case.k_cache).copy()
+    vc = _u16(case.v_cache).copy()
+    dims = _Dims(case.B, case.Lq, case.H, case.D, case.Ls, 16, case.k_cache.shape[0], case.block_tables.shape[1],
+                 case.k_cache.shape[1], 0.0)
+    rc = lib.oracle_kv_append(ctypes.byref(dims), _ptr(_u16(k_new)), _ptr(_u16(v_new)), _ptr(_i32(case.block_tables)),
+                              _ptr(_i32(case.ctx_lens)), _ptr(_i32(case.q_lens)), _ptr(kc), _ptr(vc))
+    if rc != 0:
+        raise ValueError(f"oracle_kv_append failed with code {rc}")
+    to_t = lambda a: torch.from_numpy(a.view(np.int16).reshape(case.k_cache.shape)).view(torch.float16)
+    return to_t(kc), to_t(vc)
 
 
 def all_rows(case):

@@ -194,6 +194,47 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
     return ORACLE_OK;
 }
 
+/* KV append, the cache write that precedes attention in a decode step: row
+ * i < q_lens[b] of request b is context position pos = ctx_lens[b] -
+ * q_lens[b] + i (its new token is the last of the context), and its K and V
+ * rows of every KV head hk are copied into the pool at block
+ * block_tables[b][pos / bs], row pos % bs.  k_new, v_new are [B, Lq, Hkv, D]
+ * fp16 bit patterns; the pools are updated in place.  Everything is checked
+ * before anything is written. */
+int oracle_kv_append(const oracle_dims_t *dm, const uint16_t *k_new, const uint16_t *v_new,
+                     const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                     uint16_t *k_cache, uint16_t *v_cache)
+{
+    if (!dm || !k_new || !v_new || !block_tables || !ctx_lens || !k_cache || !v_cache) return ORACLE_BAD_ARG;
+    const int B = dm->B, Lq = dm->Lq, D = dm->D, Hkv = dm->Hkv, bs = dm->block_size, MB = dm->max_blocks;
+    if (B < 0 || Lq < 1 || D < 1 || Hkv < 1 || bs < 1 || MB < 1) return ORACLE_BAD_ARG;
+    for (int b = 0; b < B; b++) {
+        int ql = q_lens ? q_lens[b] : Lq, n = ctx_lens[b];
+        if (ql < 0 || ql > Lq || n < ql || n > MB * bs) return ORACLE_BAD_ARG;
+        for (int i = 0; i < ql; i++) {
+            int pos = n - ql + i;
+            int blk = block_tables[(int64_t)b * MB + pos / bs];
+            if (blk < 0 || blk >= dm->num_blocks) return ORACLE_BAD_BLOCK;
+        }
+    }
+    for (int b = 0; b < B; b++) {
+        int ql = q_lens ? q_lens[b] : Lq, n = ctx_lens[b];
+        for (int i = 0; i < ql; i++) {
+            int pos = n - ql + i;
+            int64_t blk = block_tables[(int64_t)b * MB + pos / bs];
+            for (int hk = 0; hk < Hkv; hk++) {
+                int64_t src = (((int64_t)b * Lq + i) * Hkv + hk) * D;
+                int64_t dst = ((blk * Hkv + hk) * bs + pos % bs) * D;
+                for (int d = 0; d < D; d++) {
+                    k_cache[dst + d] = k_new[src + d];
+                    v_cache[dst + d] = v_new[src + d];
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Relay fusion of two partial results (atyun.com RelayAttention article,
  * section "RelayAttention": the final output is a convex combination of the
  * system-only and context-only outputs).  The weights that make the

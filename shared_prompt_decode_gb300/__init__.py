@@ -11,6 +11,7 @@ Entry points (same names as the C ABI in include/relay.h):
     relay_ctx_attn(...)           step 2: context attention -> fp32 o, lse
     relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
     relay_baseline_decode(...)    non-relay paged attention over [system; context]
+    relay_kv_append(...)          the step's new K/V rows into the paged pool
     workspace_size(dims), make_workspace(dims), device_status(ws)
 """
 from __future__ import annotations
@@ -61,6 +62,7 @@ _SIGS = {
     "relay_attention_decode": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 11 + [ctypes.c_size_t, _VP]),
     "relay_baseline_decode": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 10 + [ctypes.c_size_t, _VP]),
     "relay_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), _VP]),
+    "relay_kv_append": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 8 + [ctypes.c_size_t, _VP]),
     "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -254,6 +256,31 @@ def relay_baseline_decode(q, k_pool, v_pool, sys_block_ids, Ls, block_tables, ct
                                      _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "relay_baseline_decode")
     return out
+
+
+def relay_kv_append(k_new, v_new, block_tables, ctx_lens, k_cache, v_cache, q_lens=None, workspace=None,
+                    stream=None):
+    """Write the step's new K/V rows ([B, Lq, Hkv, D] fp16) into the paged pools in place, at each request's
+    last q_lens[b] context positions.  Device-side problems are flagged in `workspace` (device_status)."""
+    dev = k_new.device
+    _need(k_new, "k_new", torch.float16)
+    for name, t in (("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, torch.float16, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    if q_lens is not None:
+        _need(q_lens, "q_lens", torch.int32, dev)
+    B, Lq, Hkv, D = k_new.shape
+    if v_new.shape != k_new.shape or k_cache.shape != v_cache.shape or k_cache.shape[1] != Hkv or k_cache.shape[3] != D:
+        raise ValueError("k_new/v_new [B, Lq, Hkv, D] and the pools [num_blocks, Hkv, 16, D] disagree")
+    dims = Dims(B, Lq, Hkv, D, 0, 16, k_cache.shape[0], block_tables.shape[1], 0, 0, 0, 0.0, Hkv)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
+    rc = lib().relay_kv_append(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(ctx_lens),
+                               _ptr(q_lens), _ptr(k_cache), _ptr(v_cache), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check(rc, "relay_kv_append")
+    return workspace
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

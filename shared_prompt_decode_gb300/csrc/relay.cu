@@ -504,6 +504,39 @@ relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q, co
     return launch_relay(dims, MODE_BASELINE, p, ws, ws_bytes, stream);
 }
 
+relay_status_t relay_kv_append(const relay_dims_t *dims, const void *k_new, const void *v_new,
+                               const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                               void *k_cache, void *v_cache, void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!ws || ws_bytes < 256) return RELAY_ERR_WORKSPACE;
+    if (dims->B == 0) return RELAY_OK;
+    if (!k_new || !v_new || !block_tables || !ctx_lens || !k_cache || !v_cache || dims->max_blocks_per_seq < 1)
+        return RELAY_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4) || !aligned(ws, 256))
+        return RELAY_ERR_INVALID_ARG;
+    KvAppend a{};
+    a.B = dims->B;
+    a.Lq = dims->Lq;
+    a.Hkv = kv_heads(dims);
+    a.D = dims->D;
+    a.num_blocks = dims->num_blocks;
+    a.max_blocks = dims->max_blocks_per_seq;
+    a.k_new = static_cast<const __half *>(k_new);
+    a.v_new = static_cast<const __half *>(v_new);
+    a.block_tables = block_tables;
+    a.ctx_lens = ctx_lens;
+    a.q_lens = q_lens;
+    a.k_cache = static_cast<__half *>(k_cache);
+    a.v_cache = static_cast<__half *>(v_cache);
+    a.flags = static_cast<unsigned *>(ws) + CTRL_FLAGS;
+    const long long warps = (long long)a.B * a.Lq * a.Hkv;
+    kv_append_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
+}
+
 // ----------------------------------------------------------------------------- allocation-free variant
 // Scratch for relay_attention_decode_noalloc: one fixed buffer per device,
 // part of the module image, never allocated or freed at run time.

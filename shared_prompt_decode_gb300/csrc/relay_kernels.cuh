@@ -1460,6 +1460,52 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     merge_row<D>(p, r, b, r - qo[b], h, n_sys, n_ctx);
 }
 
+// ============================================================================= KV append
+// The step's new keys and values into the paged pool (the cache write that
+// precedes attention): one warp per (row slot b * Lq + i, KV head); lanes
+// 0..D/8-1 copy the K row and lanes 16..16+D/8-1 the V row, 16 bytes each.
+struct KvAppend {
+    int B, Lq, Hkv, D, num_blocks, max_blocks;
+    const __half *k_new, *v_new;      // [B, Lq, Hkv, D]
+    const int *block_tables, *ctx_lens, *q_lens;
+    __half *k_cache, *v_cache;        // [num_blocks, Hkv, 16, D]
+    unsigned *flags;
+};
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const KvAppend a)
+{
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)a.B * a.Lq * a.Hkv) return;
+    const int hk = (int)(w % a.Hkv);
+    const long long bi = w / a.Hkv;
+    const int b = (int)(bi / a.Lq), i = (int)(bi % a.Lq);
+    const int ql = a.q_lens ? a.q_lens[b] : a.Lq;
+    if (ql < 0 || ql > a.Lq) {
+        if (lane == 0 && i == 0 && hk == 0) atomicOr(a.flags, FLAG_BAD_Q_LEN);
+        return;
+    }
+    if (i >= ql) return;
+    const int n = a.ctx_lens[b];
+    if (n < ql || n > a.max_blocks * kBlock) {      // the new tokens are the last ql of the context
+        if (lane == 0 && i == 0 && hk == 0) atomicOr(a.flags, FLAG_BAD_CTX_LEN);
+        return;
+    }
+    const int pos = n - ql + i;
+    const int blk = a.block_tables[(size_t)b * a.max_blocks + pos / kBlock];
+    if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) atomicOr(a.flags, FLAG_BAD_BLOCK);
+        return;
+    }
+    const int half = lane >> 4, c = lane & 15;
+    if (c >= a.D / 8) return;
+    const size_t src = ((size_t)bi * a.Hkv + hk) * a.D + c * 8;
+    const size_t dst = (((size_t)blk * a.Hkv + hk) * kBlock + pos % kBlock) * a.D + c * 8;
+    const __half *from = half ? a.v_new : a.k_new;
+    __half *to = half ? a.v_cache : a.k_cache;
+    *reinterpret_cast<uint4 *>(to + dst) = __ldg(reinterpret_cast<const uint4 *>(from + src));
+}
+
 // ============================================================================= stand-alone relay fusion
 // out = a*o_sys + (1-a)*o_ctx, a = e^lse_sys / (e^lse_sys + e^lse_ctx).
 template <int D>

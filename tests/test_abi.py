@@ -123,6 +123,23 @@ def test_host_validation(relay):
     assert lib.relay_device_status(None, None, None) == relay.ERR_WORKSPACE
 
 
+def test_kv_append_host_validation(relay):
+    lib = relay.lib()
+    d = _dims(relay, Lq=2)
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    call = lambda **o: lib.relay_kv_append(
+        ctypes.byref(d), *[vp(o.get(k, FAKE)) for k in ("kn", "vn", "bt", "cl", "ql", "kc", "vc", "ws")],
+        o.get("ws_bytes", 1 << 20), None)
+    assert call(ws=None) == relay.ERR_WORKSPACE
+    assert call(ws_bytes=128) == relay.ERR_WORKSPACE
+    assert call(kn=None) == relay.ERR_INVALID_ARG
+    assert call(kc=None) == relay.ERR_INVALID_ARG
+    assert call(kn=FAKE + 8) == relay.ERR_INVALID_ARG      # not 16-byte aligned
+    assert call(ws=FAKE + 16) == relay.ERR_INVALID_ARG     # workspace not 256-aligned
+    assert lib.relay_kv_append(ctypes.byref(_dims(relay, Hkv=3)), *([ctypes.c_void_p(FAKE)] * 8), 1 << 20,
+                               None) == relay.ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors(relay):
     import torch
     q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)

@@ -334,3 +334,47 @@ def test_gqa_sdpa_fp64(oracle_lib, name):
         Q = q[b, :1].transpose(0, 1)                                         # [H, 1, D]
         ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, enable_gqa=True)
         np.testing.assert_allclose(o[b, :1], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- KV append
+# Append then attend must equal attention over the explicit concatenation
+# [system; the context before the new tokens, read from the original pool;
+# the new rows] with the causal mask: a row written to the wrong slot, head
+# or request changes the result.
+@pytest.mark.parametrize("name,over", [("tiny", dict(Lq=3, chunk_requests=2)), ("tiny_gqa", dict(Lq=2, chunk_requests=4))])
+def test_kv_append_then_attend_equals_concatenation(oracle_lib, name, over):
+    from dataclasses import replace
+    case = synth.make_case(synth.workload(name, **over), seed=29)
+    g = torch.Generator().manual_seed(5)
+    shape = (case.B, case.Lq, case.Hkv, case.D)
+    k_new = torch.randn(*shape, generator=g).half()
+    v_new = torch.randn(*shape, generator=g).half()
+    kc2, vc2 = oracle_lib.kv_append(case, k_new, v_new)
+    o, l = oracle_lib.attention_full(replace(case, k_cache=kc2, v_cache=vc2))
+    q = case.q.double()
+    for b in range(case.B):
+        n, ql = int(case.ctx_lens[b]), case.q_lens_list()[b]
+        old = n - ql
+        t = torch.arange(old)
+        blk = case.block_tables[b, t // 16].long()
+        K = torch.cat([case.sys_k.double(), case.k_cache[blk, :, t % 16].double(), k_new[b, :ql].double()], 0)
+        V = torch.cat([case.sys_v.double(), case.v_cache[blk, :, t % 16].double(), v_new[b, :ql].double()], 0)
+        kpos = torch.arange(K.shape[0]) - case.Ls                   # context position of each key (< 0: system)
+        mask = (kpos[None, :] < 0) | (kpos[None, :] <= old + torch.arange(ql)[:, None])
+        ref = torch.nn.functional.scaled_dot_product_attention(q[b, :ql].transpose(0, 1), K.transpose(0, 1),
+                                                               V.transpose(0, 1), attn_mask=mask, enable_gqa=True)
+        np.testing.assert_allclose(o[b, :ql], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_kv_append_rejects_bad_input(oracle_lib):
+    case = synth.make_case(synth.workload("tiny", Lq=2, chunk_requests=2), seed=31)
+    k_new = torch.zeros(case.B, case.Lq, case.Hkv, case.D, dtype=torch.float16)
+    bad = case.block_tables.clone()
+    bad[bad >= 0] = case.num_blocks                                 # every used block id out of range
+    from dataclasses import replace
+    with pytest.raises(ValueError):
+        oracle_lib.kv_append(replace(case, block_tables=bad), k_new, k_new)
+    short = case.ctx_lens.clone()
+    short[-1] = 1                                                   # a 2-row request with a 1-token context
+    with pytest.raises(ValueError):
+        oracle_lib.kv_append(replace(case, ctx_lens=short), k_new, k_new)

@@ -391,3 +391,49 @@ def test_grouped_query_heads_tensor_core_system_step(B, Lq, H, Hkv):
     T.check(l_s, refl_s, "lse_sys", m)
     out, lse = T.run_fused(case)
     T.check_full(case, out, lse)
+
+
+# ----------------------------------------------------------------------------- KV append
+# relay_kv_append must leave the pools bit-identical to the oracle's append
+# (every slot: the written rows, and the untouched and NaN slots as they were).
+def _kv_append_case(name, over, seed):
+    case = synth.make_case(synth.workload(name, **over), seed)
+    g = torch.Generator().manual_seed(seed + 100)
+    shape = (case.B, case.Lq, case.Hkv, case.D)
+    return case, torch.randn(*shape, generator=g).half(), torch.randn(*shape, generator=g).half()
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny_gqa", dict(Lq=3, chunk_requests=2)),
+                                        ("llama2_7b", {}), ("llama2_13b_mixed", dict(Ls=64))],
+                         ids=["tiny", "gqa_chunks", "llama2_7b", "13b_mixed_chunks"])
+def test_kv_append_bit_exact(name, over):
+    import shared_prompt_decode_gb300 as relay
+    case, k_new, v_new = _kv_append_case(name, over, 41)
+    ref_k, ref_v = oracle.kv_append(case, k_new, v_new)
+    g = T.to_dev(case)
+    kc, vc = g["k_cache"].clone(), g["v_cache"].clone()
+    ws = relay.relay_kv_append(k_new.to(T.DEV), v_new.to(T.DEV), g["block_tables"], g["ctx_lens"], kc, vc,
+                               q_lens=g["q_lens"])
+    torch.cuda.synchronize()
+    assert relay.device_status(ws) == 0
+    assert torch.equal(kc.cpu().view(torch.int16), ref_k.view(torch.int16))
+    assert torch.equal(vc.cpu().view(torch.int16), ref_v.view(torch.int16))
+
+
+def test_kv_append_device_checks():
+    import shared_prompt_decode_gb300 as relay
+    case, k_new, v_new = _kv_append_case("tiny", dict(Lq=2, chunk_requests=4), 43)
+    g = T.to_dev(case)
+    bt = g["block_tables"].clone()
+    bt[0, :] = case.num_blocks + 5                  # request 0: every block id out of range
+    cl = g["ctx_lens"].clone()
+    cl[1] = 1                                       # request 1: 2 new rows, 1-token context
+    kc, vc = g["k_cache"].clone(), g["v_cache"].clone()
+    ws = relay.relay_kv_append(k_new.to(T.DEV), v_new.to(T.DEV), bt, cl, kc, vc, q_lens=g["q_lens"])
+    flags = relay.device_status(ws)
+    assert flags & relay.FLAG_BAD_BLOCK and flags & relay.FLAG_BAD_CTX_LEN
+    # the valid requests (2, 3) are written exactly as the oracle writes them
+    from dataclasses import replace
+    sub = replace(case, q_lens=torch.tensor([0, 0, 2, 2], dtype=torch.int32))
+    ref_k, _ = oracle.kv_append(sub, k_new, v_new)
+    assert torch.equal(kc.cpu().view(torch.int16), ref_k.view(torch.int16))
