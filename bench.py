@@ -392,6 +392,26 @@ def run_relay(args):
     append_bytes = 2 * 2 * rows * case.Hkv * case.D * 2          # K and V rows, read once and written once
     del kc_scratch, vc_scratch
 
+    # the system prompt's own prefill attention (causal, compute-bound: tcgen05), timed like the step
+    prefill = None
+    if case.D == 128 and case.Ls > 0:
+        gp = torch.Generator().manual_seed(args.seed + 9)
+        q_sys = (torch.randn(case.Ls, case.H, case.D, generator=gp) * 0.5).half().to(dev)
+        out_p = torch.empty_like(q_sys)
+        ws_p = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+        def prefill_step():
+            relay.relay_sys_prefill(q_sys, g["sys_k"], g["sys_v"], out=out_p, workspace=ws_p)
+        ms_p, _ = timed(as_graph(prefill_step), max(5, args.steps // 40), args.warmup)
+        flops = 2 * case.D * case.H * case.Ls * (case.Ls + 1)    # QK^T and PV over the t+1 visible keys of row t
+        tflops = flops / (statistics.mean(ms_p) * 1e-3) / 1e12
+        peaks_p = load_peaks()
+        prefill = {"kernel": "sys_tc_kernel<prefill> (relay_sys_prefill: causal self-attention of the system prompt)",
+                   "us": 1e3 * statistics.mean(ms_p), "flops": flops, "tflops": tflops,
+                   "peak_tflops": peaks_p["bf16_tflops"], "frac": tflops / peaks_p["bf16_tflops"],
+                   "peak_source": f"{peaks_p['source']} dense bf16 (fp16 has the same nominal tensor rate)"}
+        del q_sys, out_p
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=200)
@@ -420,6 +440,7 @@ def run_relay(args):
         "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(case) * args.steps,
+        "sys_prefill": prefill,
         "kv_append": {"kernel": "kv_append_kernel (relay_kv_append: the step's new K/V rows into the pool)",
                       "us": 1e3 * statistics.mean(ms_a), "bytes": append_bytes,
                       "gbs": append_bytes / (statistics.mean(ms_a) * 1e-3) / 1e9},

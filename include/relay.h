@@ -187,6 +187,20 @@ relay_status_t relay_kv_append(const relay_dims_t *dims, const void *k_new, cons
                                const int32_t *q_lens, void *k_cache, void *v_cache,
                                void *ws, size_t ws_bytes, relay_stream_t stream);
 
+/* Prefill attention of the system prompt: causal self-attention of its Ls
+ * tokens, the attention step of filling the separate system cache offline,
+ * once, before serving (atyun.com RelayAttention article, section
+ * "RelayAttention": the system KVs are computed offline into their own
+ * cache).  Row t (query q_sys[t][h]) attends to system keys 0..t of KV head
+ * h / (H / Hkv); out[t][h] = softmax(scale * q K^T) V, lse[t][h] its natural-
+ * log normaliser.  q_sys, out: [Ls, H, 128] fp16; sys_k, sys_v: [Ls, Hkv,
+ * 128] fp16; lse_out: [Ls, H] fp32 or NULL.  Uses dims->H, D, Ls, Hkv,
+ * scale; D must be 128 (it runs on the tcgen05 tensor-core kernel).  ws: at
+ * least 256 bytes (flag word for RELAY_FLAG_WAIT_TIMEOUT). */
+relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, const void *sys_k,
+                                 const void *sys_v, void *out, float *lse_out, void *ws,
+                                 size_t ws_bytes, relay_stream_t stream);
+
 /* The non-relay formulation, as a paged-attention system with prefix sharing
  * runs it (atyun.com RelayAttention article, section "RelayAttention": the
  * system KVs are read from memory once per request).  The system prompt's KV

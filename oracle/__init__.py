@@ -61,6 +61,7 @@ def _load():
             lib = ctypes.CDLL(_LIB_PATH)
             lib.oracle_attention_rows.restype = ctypes.c_int
             lib.oracle_kv_append.restype = ctypes.c_int
+            lib.oracle_sys_prefill.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -124,6 +125,29 @@ def attention_rows(case, rows, part: str = "full", scale: float | None = None,
                                    ctypes.c_int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention_rows failed with code {rc}")
+    return out[:n], lse[:n]
+
+
+def sys_prefill(q_sys, sys_k, sys_v, rows=None, scale=None, threads: int = 0):
+    """Causal self-attention of the system prompt: q_sys [Ls, H, D], sys_k /
+    sys_v [Ls, Hkv, D] (fp16 torch tensors).  rows: (t, h) pairs (default:
+    all).  Returns (out [n, D], lse [n]) in fp64."""
+    lib = _load()
+    Ls, H, D = q_sys.shape
+    Hkv = sys_k.shape[1]
+    if rows is None:
+        rows = [(t, h) for t in range(Ls) for h in range(H)]
+    rows = list(rows)
+    n = len(rows)
+    dims = _Dims(1, Ls, H, D, Ls, 16, 0, 0, Hkv, float(1.0 / math.sqrt(D)) if scale is None else float(scale))
+    rt = np.ascontiguousarray(np.array([r[0] for r in rows], dtype=np.int32))
+    rh = np.ascontiguousarray(np.array([r[1] for r in rows], dtype=np.int32))
+    out = np.zeros((max(n, 1), D), dtype=np.float64)
+    lse = np.zeros(max(n, 1), dtype=np.float64)
+    rc = lib.oracle_sys_prefill(ctypes.byref(dims), _ptr(_u16(q_sys)), _ptr(_u16(sys_k)), _ptr(_u16(sys_v)),
+                                ctypes.c_int64(n), _ptr(rt), _ptr(rh), _ptr(out), _ptr(lse), ctypes.c_int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_sys_prefill failed with code {rc}")
     return out[:n], lse[:n]
 
 

@@ -194,6 +194,49 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
     return ORACLE_OK;
 }
 
+/* Prefill attention of the system prompt (atyun.com RelayAttention article,
+ * section "RelayAttention": the system KVs are computed offline into their
+ * own cache): causal self-attention of its Ls tokens.  Row (t, h) attends to
+ * system keys 0..t of KV head h / (H / Hkv):
+ *     out = sum_{j<=t} softmax(scale * <q_sys[t,h], k_j>) v_j,  lse = log sum exp.
+ * q_sys [Ls, H, D], sys_k / sys_v [Ls, Hkv, D] (fp16 bit patterns); only the
+ * (t, h) rows listed are computed. */
+int oracle_sys_prefill(const oracle_dims_t *dm, const uint16_t *q_sys, const uint16_t *sys_k,
+                       const uint16_t *sys_v, int64_t n_rows, const int32_t *row_t, const int32_t *row_h,
+                       double *out, double *lse, int n_threads)
+{
+    if (!dm || !q_sys || !sys_k || !sys_v || !out || !lse || n_rows < 0) return ORACLE_BAD_ARG;
+    const int H = dm->H, D = dm->D, Ls = dm->Ls, Hkv = dm->Hkv;
+    if (D <= 0 || H <= 0 || Ls <= 0 || Hkv <= 0 || H % Hkv != 0) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < n_rows; r++)
+        if (row_t[r] < 0 || row_t[r] >= Ls || row_h[r] < 0 || row_h[r] >= H) return ORACLE_BAD_ARG;
+    const int group = H / Hkv;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)Ls);
+        const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)Ls);
+        double *scores = (double *)malloc(sizeof(double) * (size_t)Ls);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; r++) {
+            int t = row_t[r], h = row_h[r], hk = h / group;
+            for (int j = 0; j <= t; j++) {
+                krows[j] = sys_k + ((int64_t)j * Hkv + hk) * D;
+                vrows[j] = sys_v + ((int64_t)j * Hkv + hk) * D;
+            }
+            attend(q_sys + ((int64_t)t * H + h) * D, D, dm->scale, t + 1, krows, vrows, scores, out + r * D, lse + r);
+        }
+        free(krows);
+        free(vrows);
+        free(scores);
+    }
+    return ORACLE_OK;
+}
+
 /* KV append, the cache write that precedes attention in a decode step: row
  * i < q_lens[b] of request b is context position pos = ctx_lens[b] -
  * q_lens[b] + i (its new token is the last of the context), and its K and V

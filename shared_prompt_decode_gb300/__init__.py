@@ -12,6 +12,7 @@ Entry points (same names as the C ABI in include/relay.h):
     relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
     relay_baseline_decode(...)    non-relay paged attention over [system; context]
     relay_kv_append(...)          the step's new K/V rows into the paged pool
+    relay_sys_prefill(...)        causal self-attention of the system prompt (filling its cache)
     workspace_size(dims), make_workspace(dims), device_status(ws)
 """
 from __future__ import annotations
@@ -63,6 +64,7 @@ _SIGS = {
     "relay_baseline_decode": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 10 + [ctypes.c_size_t, _VP]),
     "relay_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), _VP]),
     "relay_kv_append": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 8 + [ctypes.c_size_t, _VP]),
+    "relay_sys_prefill": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 6 + [ctypes.c_size_t, _VP]),
     "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -281,6 +283,30 @@ def relay_kv_append(k_new, v_new, block_tables, ctx_lens, k_cache, v_cache, q_le
                                _stream(stream))
     _check(rc, "relay_kv_append")
     return workspace
+
+
+def relay_sys_prefill(q_sys, sys_k, sys_v, out=None, lse_out=None, workspace=None, scale=None, stream=None):
+    """Causal self-attention of the system prompt (the attention step of filling its cache offline):
+    q_sys [Ls, H, 128] fp16, sys_k / sys_v [Ls, Hkv, 128] fp16 -> out [Ls, H, 128] fp16 (and lse_out [Ls, H])."""
+    dev = q_sys.device
+    _need(q_sys, "q_sys", torch.float16)
+    _need(sys_k, "sys_k", torch.float16, dev)
+    _need(sys_v, "sys_v", torch.float16, dev)
+    Ls, H, D = q_sys.shape
+    if sys_k.shape != sys_v.shape or sys_k.shape[0] != Ls or sys_k.shape[2] != D:
+        raise ValueError("q_sys [Ls, H, D] and sys_k / sys_v [Ls, Hkv, D] disagree")
+    dims = Dims(1, 1, H, D, Ls, 16, 0, 0, 0, 0, 0, 0.0 if scale is None else float(scale), sys_k.shape[1])
+    if out is None:
+        out = torch.empty_like(q_sys)
+    _need(out, "out", torch.float16, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, dev)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
+    rc = lib().relay_sys_prefill(ctypes.byref(dims), _ptr(q_sys), _ptr(sys_k), _ptr(sys_v), _ptr(out), _ptr(lse_out),
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "relay_sys_prefill")
+    return out
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

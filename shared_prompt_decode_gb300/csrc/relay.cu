@@ -72,8 +72,10 @@ relay_status_t device_info(const DevInfo **out)
             return RELAY_ERR_CUDA;
         }
         if (d.occ64 < 1 || d.occ128 < 1) return RELAY_ERR_CUDA;
-        if (cudaFuncSetAttribute(tc::sys_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemTC) !=
-            cudaSuccess) {
+        if (cudaFuncSetAttribute(tc::sys_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc::kSmemTC) != cudaSuccess ||
+            cudaFuncSetAttribute(tc::sys_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc::kSmemTC) != cudaSuccess) {
             cudaGetLastError();
             return RELAY_ERR_CUDA;
         }
@@ -309,7 +311,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         if (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls))
             return RELAY_ERR_CUDA;
         const long long items = (long long)t.pairs * p.Hkv * pl.R_sys;
-        tc::sys_tc_kernel<<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);
+        tc::sys_tc_kernel<false><<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
     if (d->D == 128) {
@@ -534,6 +536,47 @@ relay_status_t relay_kv_append(const relay_dims_t *dims, const void *k_new, cons
     a.flags = static_cast<unsigned *>(ws) + CTRL_FLAGS;
     const long long warps = (long long)a.B * a.Lq * a.Hkv;
     kv_append_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
+}
+
+relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, const void *sys_k, const void *sys_v,
+                                 void *out, float *lse_out, void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!ws || ws_bytes < 256) return RELAY_ERR_WORKSPACE;
+    if (dims->Ls == 0) return RELAY_OK;
+    if (dims->D != 128) return RELAY_ERR_UNSUPPORTED;
+    if ((int64_t)dims->Ls * dims->H > INT_MAX / 2) return RELAY_ERR_UNSUPPORTED;
+    if (!q_sys || !sys_k || !sys_v || !out) return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q_sys, 16) || !aligned(sys_k, 16) || !aligned(sys_v, 16) || !aligned(out, 16) ||
+        !aligned(lse_out, 4) || !aligned(ws, 256))
+        return RELAY_ERR_INVALID_ARG;
+    const DevInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != RELAY_OK) return st;
+    tc::TcParams t{};
+    t.B = 1;
+    t.Lq = dims->Ls;
+    t.H = dims->H;
+    t.Ls = dims->Ls;
+    t.max_q_total = dims->Ls;
+    t.scale_log2 = scale_log2_of(dims);
+    t.q = static_cast<const __half *>(q_sys);
+    t.flags = static_cast<unsigned *>(ws);
+    t.R = 1;
+    t.range = dims->Ls;
+    t.Hkv = kv_heads(dims);
+    t.G = dims->H / t.Hkv;
+    t.pairs = tc_pairs(dims->Ls * t.G);
+    t.out = static_cast<__half *>(out);
+    t.lse_out = lse_out;
+    CUtensorMap tmK, tmV;
+    if (!encode_sys_map(&tmK, sys_k, t.Hkv, dims->Ls) || !encode_sys_map(&tmV, sys_v, t.Hkv, dims->Ls))
+        return RELAY_ERR_CUDA;
+    const long long items = (long long)t.pairs * t.Hkv;
+    tc::sys_tc_kernel<true><<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, reinterpret_cast<cudaStream_t>(stream)>>>(
+        tmK, tmV, t);
     return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
 }
 

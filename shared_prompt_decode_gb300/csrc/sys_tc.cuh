@@ -288,6 +288,8 @@ struct TcParams {
     int pairs;                       // tile pairs in the grid: ceil(ceil(max_q_total * G / 128) / 2)
     int G;                           // query heads per KV head: head h reads KV head h / G
     int Hkv;                         // KV heads
+    __half *out;                     // prefill: [Ls][H][128] fp16 output
+    float *lse_out;                  // prefill: [Ls][H] natural-log LSE (nullable)
 };
 
 __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
@@ -304,6 +306,13 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 
 // blockIdx.x = (range * pairs + pair) * Hkv + hk.  tmK / tmV view sys_k / sys_v
 // as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
+//
+// PREFILL: causal self-attention of the system prompt itself (its Ls query
+// rows, in q = [Ls][H][128]; row t sees system keys 0..t), one key range:
+// a CTA streams keys up to its last row's position, masks per row on the
+// diagonal stages, takes tile pairs latest first (the longest first), and
+// writes the final fp16 output and natural-log LSE instead of partials.
+template <bool PREFILL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
@@ -319,7 +328,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     volatile int *abort_p = &abort_sh;
 
     // rows of the batch: prefix of q_lens (B <= 512)
-    if (p.q_lens) {
+    if (PREFILL) {
+    } else if (p.q_lens) {
         if (tid == 0) {
             int acc = 0;
             for (int b = 0; b < p.B; b++) { qo[b] = acc; acc += p.q_lens[b]; }
@@ -330,16 +340,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
     if (tid == 0) abort_sh = 0;
     __syncthreads();
-    const int Mtot = min(qo[p.B], p.max_q_total);
+    const int Mtot = PREFILL ? p.Ls : min(qo[p.B], p.max_q_total);
     const int Mv = Mtot * p.G;                       // virtual rows of a KV head
     const int T = (Mv + kRowsTC - 1) / kRowsTC;
     const int hk = blockIdx.x % p.Hkv;
-    const int pair = (blockIdx.x / p.Hkv) % p.pairs;
+    const int pair = PREFILL ? p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs : (blockIdx.x / p.Hkv) % p.pairs;
     const int rho = blockIdx.x / (p.Hkv * p.pairs);
     if (2 * pair >= T || rho >= p.R) return;        // the whole CTA leaves together
     const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
-    const int key0 = rho * p.range;
-    const int key_hi = min(key0 + p.range, p.Ls);
+    const int key0 = PREFILL ? 0 : rho * p.range;
+    // prefill: every key up to the position of the CTA's last row
+    const int key_hi = PREFILL ? (min(Mv, (2 * pair + n_act) * kRowsTC) - 1) / p.G + 1 : min(key0 + p.range, p.Ls);
     const int n_tiles = key_hi > key0 ? (key_hi - key0 + kKeysTC - 1) / kKeysTC : 0;
 
     if (warp == kWarpMmaS) {
@@ -385,7 +396,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         {
             // this row's query into the K-major, 128-byte-swizzled Q tile
             const __half *qrow = p.q;
-            if (row_ok) {
+            if (row_ok && PREFILL) {
+                qrow = p.q + ((size_t)r * p.H + h) * 128;
+            } else if (row_ok) {
                 const int b = owner_of(qo, p.B, r);
                 qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
             }
@@ -422,10 +435,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                 }
                 const int kbase = key0 + j * kKeysTC;
-                if (kbase + kKeysTC > key_hi) {
+                const int lim = PREFILL ? r + 1 : key_hi;     // keys visible to this row: below lim
+                if (kbase + kKeysTC > lim) {
 #pragma unroll
                     for (int i = 0; i < 64; i++)
-                        if (kbase + i >= key_hi) s[i] = kNegInf;
+                        if (kbase + i >= lim) s[i] = kNegInf;
                 }
                 float mx[8];
 #pragma unroll
@@ -510,8 +524,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             fin = __all_sync(0xffffffffu, fin);
             tc_fence_after();
             if (!fin && lane == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
-            const size_t prow = ((size_t)rho * p.max_q_total + r) * p.H + h;
-            float *po = p.part_o + prow * 128;
+            const size_t prow = PREFILL ? (size_t)r * p.H + h : ((size_t)rho * p.max_q_total + r) * p.H + h;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int q4 = 0; q4 < 4; q4++) {
@@ -523,7 +536,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
                     for (int i = 0; i < 32; i++) o[i] = 0u;
                 }
-                if (row_ok) {
+                if (row_ok && PREFILL) {
+                    __half *po = p.out + prow * 128 + q4 * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8)
+                        *reinterpret_cast<uint4 *>(po + i) = make_uint4(
+                            pack_half2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
+                            pack_half2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
+                            pack_half2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
+                            pack_half2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+                } else if (row_ok) {
+                    float *po = p.part_o + prow * 128;
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
                         __stcg(reinterpret_cast<float4 *>(po + q4 * 32 + i),
@@ -531,7 +554,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv));
                 }
             }
-            if (row_ok) __stcg(p.part_lse + prow, (l_run > 0.f && fin) ? m_run + lg2(l_run) : kNegInf);
+            if (row_ok && PREFILL) {
+                if (p.lse_out) p.lse_out[prow] = (l_run > 0.f && fin) ? (m_run + lg2(l_run)) * 0.69314718055994531f : kNegInf;
+            } else if (row_ok) {
+                __stcg(p.part_lse + prow, (l_run > 0.f && fin) ? m_run + lg2(l_run) : kNegInf);
+            }
         }
     } else if (warp == kWarpLoad) {
         // ------------------------------------------------------------ TMA producer

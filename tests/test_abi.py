@@ -140,6 +140,21 @@ def test_kv_append_host_validation(relay):
                                None) == relay.ERR_INVALID_ARG
 
 
+def test_sys_prefill_host_validation(relay):
+    lib = relay.lib()
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    def call(d=None, **o):
+        return lib.relay_sys_prefill(ctypes.byref(d or _dims(relay)),
+                                     *[vp(o.get(k, FAKE)) for k in ("q", "k", "v", "out", "lse", "ws")],
+                                     o.get("ws_bytes", 1 << 20), None)
+    assert call(ws=None) == relay.ERR_WORKSPACE
+    assert call(d=_dims(relay, D=64)) == relay.ERR_UNSUPPORTED       # tensor-core kernel: D = 128
+    assert call(q=None) == relay.ERR_INVALID_ARG
+    assert call(out=FAKE + 8) == relay.ERR_INVALID_ARG
+    assert call(lse=FAKE + 2) == relay.ERR_INVALID_ARG
+    assert call(d=_dims(relay, Ls=0)) == relay.OK                    # nothing to do, nothing queued
+
+
 def test_binding_refuses_cpu_tensors(relay):
     import torch
     q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)

@@ -378,3 +378,42 @@ def test_kv_append_rejects_bad_input(oracle_lib):
     short[-1] = 1                                                   # a 2-row request with a 1-token context
     with pytest.raises(ValueError):
         oracle_lib.kv_append(replace(case, ctx_lens=short), k_new, k_new)
+
+
+# ----------------------------------------------------------------------------- system-prompt prefill
+# Causal self-attention of the system prompt: torch's fp64 scaled-dot-product
+# attention with its own causal and grouped-query options, and row t against
+# the (pinned) decode oracle attending one query over the first t+1 system
+# tokens with no context.
+def _prefill_inputs(Ls, H, Hkv, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(Ls, H, D, generator=g).half()
+    k = torch.randn(Ls, Hkv, D, generator=g).half()
+    v = torch.randn(Ls, Hkv, D, generator=g).half()
+    return q, k, v
+
+
+@pytest.mark.parametrize("Ls,H,Hkv", [(40, 4, 4), (37, 4, 2), (20, 3, 1)])
+def test_sys_prefill_sdpa_causal(oracle_lib, Ls, H, Hkv):
+    D = 16
+    q, k, v = _prefill_inputs(Ls, H, Hkv, D, 3)
+    o, l = oracle_lib.sys_prefill(q, k, v)
+    ref = torch.nn.functional.scaled_dot_product_attention(q.double().transpose(0, 1), k.double().transpose(0, 1),
+                                                           v.double().transpose(0, 1), is_causal=True,
+                                                           enable_gqa=True)
+    np.testing.assert_allclose(o.reshape(Ls, H, D), ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_sys_prefill_row_is_decode_over_prefix(oracle_lib):
+    Ls, H, Hkv, D = 24, 4, 2, 8
+    q, k, v = _prefill_inputs(Ls, H, Hkv, D, 4)
+    rows = [(t, h) for t in (0, 1, 7, 23) for h in range(H)]
+    o, l = oracle_lib.sys_prefill(q, k, v, rows)
+    for n, (t, h) in enumerate(rows):
+        wl = synth.Workload("prefix", B=1, H=H, D=D, Ls=t + 1, ctx_dist=("fixed", 0), value_scale=1.0, Hkv=Hkv)
+        case = synth.Case(wl, 0, q[t][None, None].contiguous(), k[:t + 1].contiguous(), v[:t + 1].contiguous(),
+                          torch.zeros(1, Hkv, 16, D, dtype=torch.float16), torch.zeros(1, Hkv, 16, D, dtype=torch.float16),
+                          torch.zeros(1, 1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32), None)
+        od, ld = oracle_lib.attention_rows(case, [(0, 0, h)], "sys")
+        np.testing.assert_allclose(o[n], od[0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l[n], ld[0], rtol=0, atol=1e-13)

@@ -437,3 +437,39 @@ def test_kv_append_device_checks():
     sub = replace(case, q_lens=torch.tensor([0, 0, 2, 2], dtype=torch.int32))
     ref_k, _ = oracle.kv_append(sub, k_new, v_new)
     assert torch.equal(kc.cpu().view(torch.int16), ref_k.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- system-prompt prefill
+# relay_sys_prefill (tcgen05 kernel, causal) against the oracle: every row for
+# short prompts; first, last, diagonal-tile and random rows for a 32768-token
+# prompt at the Llama-2-13B shape.
+PREFILL_CASES = [
+    (300, 4, 2, None), (2048, 32, 32, None), (1000, 8, 1, None), (129, 2, 2, None),
+    (32768, 40, 40, 192),
+]
+
+
+@pytest.mark.parametrize("Ls,H,Hkv,sample", PREFILL_CASES,
+                         ids=["Ls300_gqa", "Ls2048_llama2_7b", "Ls1000_mqa", "Ls129_ragged", "Ls32768_13b_sampled"])
+def test_sys_prefill(Ls, H, Hkv, sample):
+    import shared_prompt_decode_gb300 as relay
+    g = torch.Generator().manual_seed(Ls + H)
+    q = (torch.randn(Ls, H, 128, generator=g) * 0.5).half()
+    k = (torch.randn(Ls, Hkv, 128, generator=g) * 0.5).half()
+    v = (torch.randn(Ls, Hkv, 128, generator=g) * 0.5).half()
+    lse = torch.full((Ls, H), float("nan"), dtype=torch.float32, device=T.DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=T.DEV)
+    out = relay.relay_sys_prefill(q.to(T.DEV), k.to(T.DEV), v.to(T.DEV), lse_out=lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert relay.device_status(ws) == 0
+    if sample is None:
+        rows = [(t, h) for t in range(Ls) for h in range(H)]
+    else:
+        gen = torch.Generator().manual_seed(7)
+        ts = [0, 1, 63, 64, 127, 128, 255, Ls - 1, Ls - 64, Ls - 129] + torch.randint(0, Ls, (sample,), generator=gen).tolist()
+        rows = [(t, int(h)) for t, h in zip(ts, torch.randint(0, H, (len(ts),), generator=gen))]
+    ref_o, ref_l = oracle.sys_prefill(q, k, v, rows)
+    got_o = out.cpu().double().numpy()[[r[0] for r in rows], [r[1] for r in rows]]
+    got_l = lse.cpu().double().numpy()[[r[0] for r in rows], [r[1] for r in rows]]
+    T.check(got_o, ref_o, "prefill out")
+    T.check(got_l, ref_l, "lse prefill")
