@@ -389,6 +389,14 @@ def run_relay(args):
         relay.relay_kv_append(k_new, v_new, g["block_tables"], g["ctx_lens"], kc_scratch, vc_scratch,
                               q_lens=g["q_lens"], workspace=ws_a)
     ms_a, _ = timed(as_graph(append_step), max(5, args.steps // 4), args.warmup)
+    # rotary positions of the step's q and new k, offset by the system prompt (in place on scratch copies)
+    q_rot, k_rot = g["q"].clone(), k_new.clone()
+
+    def rope_step():
+        relay.relay_rope(q_rot, g["ctx_lens"], case.Ls, k_new=k_rot, q_lens=g["q_lens"], workspace=ws_a)
+    ms_r, _ = timed(as_graph(rope_step), max(5, args.steps // 4), args.warmup)
+    rope_bytes = 2 * rows * (case.H + case.Hkv) * case.D * 2    # q and k rows, read and written
+    del q_rot, k_rot
     append_bytes = 2 * 2 * rows * case.Hkv * case.D * 2          # K and V rows, read once and written once
     del kc_scratch, vc_scratch
 
@@ -441,6 +449,9 @@ def run_relay(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(case) * args.steps,
         "sys_prefill": prefill,
+        "rope": {"kernel": "rope_kernel (relay_rope: rotary positions offset by the system prompt)",
+                 "us": 1e3 * statistics.mean(ms_r), "bytes": rope_bytes,
+                 "gbs": rope_bytes / (statistics.mean(ms_r) * 1e-3) / 1e9},
         "kv_append": {"kernel": "kv_append_kernel (relay_kv_append: the step's new K/V rows into the pool)",
                       "us": 1e3 * statistics.mean(ms_a), "bytes": append_bytes,
                       "gbs": append_bytes / (statistics.mean(ms_a) * 1e-3) / 1e9},

@@ -201,6 +201,23 @@ relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, co
                                  const void *sys_v, void *out, float *lse_out, void *ws,
                                  size_t ws_bytes, relay_stream_t stream);
 
+/* Rotary position embedding of the step's new rows with the system-prompt
+ * offset: the system KVs are computed offline, so the request tokens'
+ * positions are shifted by the system prompt's length (atyun.com
+ * RelayAttention article, section "RelayAttention").  Row i < q_lens[b] of
+ * request b is at position p = Ls + ctx_lens[b] - q_lens[b] + i; q[b][i][h]
+ * (every query head) and k_new[b][i][hk] (every KV head; k_new may be NULL)
+ * are rotated in place, rotate-half form: for j < D/2 the pair
+ * (x[j], x[j + D/2]) turns by the angle p * base^(-2j/D),
+ *     x[j] <- x[j] cos - x[j+D/2] sin,   x[j+D/2] <- x[j+D/2] cos + x[j] sin.
+ * Angles are computed in fp64, the rotation in fp32, results rounded to
+ * fp16.  q: [B, Lq, H, D], k_new: [B, Lq, Hkv, D] fp16; base > 1 (10000 for
+ * Llama).  A request with q_len outside [0, Lq] or ctx_len < q_len is skipped
+ * and flagged.  ws: at least 256 bytes (flag word). */
+relay_status_t relay_rope(const relay_dims_t *dims, void *q, void *k_new, const int32_t *ctx_lens,
+                          const int32_t *q_lens, float base, void *ws, size_t ws_bytes,
+                          relay_stream_t stream);
+
 /* The non-relay formulation, as a paged-attention system with prefix sharing
  * runs it (atyun.com RelayAttention article, section "RelayAttention": the
  * system KVs are read from memory once per request).  The system prompt's KV

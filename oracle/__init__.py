@@ -62,6 +62,7 @@ def _load():
             lib.oracle_attention_rows.restype = ctypes.c_int
             lib.oracle_kv_append.restype = ctypes.c_int
             lib.oracle_sys_prefill.restype = ctypes.c_int
+            lib.oracle_rope.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -149,6 +150,20 @@ def sys_prefill(q_sys, sys_k, sys_v, rows=None, scale=None, threads: int = 0):
     if rc != 0:
         raise ValueError(f"oracle_sys_prefill failed with code {rc}")
     return out[:n], lse[:n]
+
+
+def rope(x, Ls, ctx_lens, q_lens=None, base=10000.0):
+    """x [B, Lq, heads, D] fp16 rotated at positions Ls + ctx_lens[b] - q_lens[b] + i
+    (rotate-half pairs j, j + D/2; angle p * base^(-2j/D)); fp64 result, padding rows NaN."""
+    lib = _load()
+    B, Lq, heads, D = x.shape
+    out = np.zeros((B, Lq, heads, D), dtype=np.float64)
+    dims = _Dims(B, Lq, heads, D, int(Ls), 16, 0, 0, 1, 0.0)
+    rc = lib.oracle_rope(ctypes.byref(dims), ctypes.c_double(base), ctypes.c_int(heads), _ptr(_i32(ctx_lens)),
+                         _ptr(_i32(q_lens)), _ptr(_u16(x)), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_rope failed with code {rc}")
+    return out
 
 
 def kv_append(case, k_new, v_new):

@@ -237,6 +237,46 @@ int oracle_sys_prefill(const oracle_dims_t *dm, const uint16_t *q_sys, const uin
     return ORACLE_OK;
 }
 
+/* Rotary position embedding with the system-prompt offset (atyun.com
+ * RelayAttention article, section "RelayAttention": the request tokens'
+ * positions are shifted by the system prompt's length).  Row i < q_lens[b]
+ * of request b is at position p = Ls + ctx_lens[b] - q_lens[b] + i; for
+ * j < D/2 the pair (x[j], x[j + D/2]) is rotated by the angle
+ * p * base^(-2j/D).  x: [B, Lq, heads, D] fp16 bit patterns; out (fp64, same
+ * shape) receives the rotated rows; rows i >= q_lens[b] are NaN. */
+int oracle_rope(const oracle_dims_t *dm, double base, int heads, const int32_t *ctx_lens,
+                const int32_t *q_lens, const uint16_t *x, double *out)
+{
+    if (!dm || !x || !out || !ctx_lens || heads < 1 || dm->D < 2 || dm->D % 2 || !(base > 1.0)) return ORACLE_BAD_ARG;
+    const int B = dm->B, Lq = dm->Lq, D = dm->D, half = dm->D / 2;
+    for (int b = 0; b < B; b++) {
+        int ql = q_lens ? q_lens[b] : Lq;
+        if (ql < 0 || ql > Lq || ctx_lens[b] < ql) return ORACLE_BAD_ARG;
+    }
+    for (int b = 0; b < B; b++) {
+        int ql = q_lens ? q_lens[b] : Lq;
+        for (int i = 0; i < Lq; i++) {
+            double p = (double)dm->Ls + (double)(ctx_lens[b] - ql + i);
+            for (int h = 0; h < heads; h++) {
+                const uint16_t *xr = x + (((int64_t)b * Lq + i) * heads + h) * D;
+                double *o = out + (((int64_t)b * Lq + i) * heads + h) * D;
+                for (int j = 0; j < half; j++) {
+                    if (i >= ql) {
+                        o[j] = o[j + half] = NAN;
+                        continue;
+                    }
+                    double ang = p * pow(base, -2.0 * j / D);
+                    double c = cos(ang), s = sin(ang);
+                    double x0 = half_to_double(xr[j]), x1 = half_to_double(xr[j + half]);
+                    o[j] = x0 * c - x1 * s;
+                    o[j + half] = x1 * c + x0 * s;
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* KV append, the cache write that precedes attention in a decode step: row
  * i < q_lens[b] of request b is context position pos = ctx_lens[b] -
  * q_lens[b] + i (its new token is the last of the context), and its K and V

@@ -13,6 +13,7 @@ Entry points (same names as the C ABI in include/relay.h):
     relay_baseline_decode(...)    non-relay paged attention over [system; context]
     relay_kv_append(...)          the step's new K/V rows into the paged pool
     relay_sys_prefill(...)        causal self-attention of the system prompt (filling its cache)
+    relay_rope(...)               rotary positions of the new rows, offset by the system prompt
     workspace_size(dims), make_workspace(dims), device_status(ws)
 """
 from __future__ import annotations
@@ -65,6 +66,7 @@ _SIGS = {
     "relay_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), _VP]),
     "relay_kv_append": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 8 + [ctypes.c_size_t, _VP]),
     "relay_sys_prefill": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 6 + [ctypes.c_size_t, _VP]),
+    "relay_rope": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 4 + [ctypes.c_float, _VP, ctypes.c_size_t, _VP]),
     "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -307,6 +309,27 @@ def relay_sys_prefill(q_sys, sys_k, sys_v, out=None, lse_out=None, workspace=Non
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "relay_sys_prefill")
     return out
+
+
+def relay_rope(q, ctx_lens, Ls, k_new=None, q_lens=None, base=10000.0, workspace=None, stream=None):
+    """Rotary embedding in place of q [B, Lq, H, D] (and k_new [B, Lq, Hkv, D]) at positions
+    Ls + ctx_lens[b] - q_lens[b] + i: the request tokens follow the Ls system tokens."""
+    dev = q.device
+    _need(q, "q", torch.float16)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    if k_new is not None:
+        _need(k_new, "k_new", torch.float16, dev)
+    if q_lens is not None:
+        _need(q_lens, "q_lens", torch.int32, dev)
+    B, Lq, H, D = q.shape
+    Hkv = k_new.shape[2] if k_new is not None else H
+    dims = Dims(B, Lq, H, D, int(Ls), 16, 0, 0, 0, 0, 0, 0.0, Hkv)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
+    rc = lib().relay_rope(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(ctx_lens), _ptr(q_lens), float(base),
+                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "relay_rope")
+    return workspace
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -580,6 +580,35 @@ relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, co
     return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
 }
 
+relay_status_t relay_rope(const relay_dims_t *dims, void *q, void *k_new, const int32_t *ctx_lens,
+                          const int32_t *q_lens, float base, void *ws, size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (!ws || ws_bytes < 256) return RELAY_ERR_WORKSPACE;
+    if (!(base > 1.f) || !(base < 1e30f)) return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    if (!q || !ctx_lens) return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4) || !aligned(ws, 256))
+        return RELAY_ERR_INVALID_ARG;
+    Rope a{};
+    a.B = dims->B;
+    a.Lq = dims->Lq;
+    a.H = dims->H;
+    a.Hkv = kv_heads(dims);
+    a.D = dims->D;
+    a.Ls = dims->Ls;
+    a.log2_base = std::log2((double)base);
+    a.q = static_cast<__half *>(q);
+    a.k = static_cast<__half *>(k_new);
+    a.ctx_lens = ctx_lens;
+    a.q_lens = q_lens;
+    a.flags = static_cast<unsigned *>(ws) + CTRL_FLAGS;
+    const long long warps = (long long)a.B * a.Lq * (a.H + (k_new ? a.Hkv : 0));
+    rope_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
+}
+
 // ----------------------------------------------------------------------------- allocation-free variant
 // Scratch for relay_attention_decode_noalloc: one fixed buffer per device,
 // part of the module image, never allocated or freed at run time.

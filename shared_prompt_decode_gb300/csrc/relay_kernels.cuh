@@ -1506,6 +1506,51 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const KvAppend a)
     *reinterpret_cast<uint4 *>(to + dst) = __ldg(reinterpret_cast<const uint4 *>(from + src));
 }
 
+// ============================================================================= rotary positions
+// Rotary position embedding of the step's new rows with the system-prompt
+// offset: row i of request b sits at position Ls + ctx_lens[b] - q_lens[b] + i
+// (the request tokens follow the Ls system tokens).  Rotate-half pairs
+// (j, j + D/2) turn by the angle pos * base^(-2j/D), computed in fp64 (the
+// angle reaches tens of thousands of radians); the rotation itself is fp32.
+// One warp per (row slot, head); q heads first, then the KV heads of k_new.
+struct Rope {
+    int B, Lq, H, Hkv, D, Ls;
+    double log2_base;
+    __half *q, *k;                    // [B, Lq, H, D], [B, Lq, Hkv, D] (k nullable)
+    const int *ctx_lens, *q_lens;
+    unsigned *flags;
+};
+
+__global__ void __launch_bounds__(256) rope_kernel(const Rope a)
+{
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nh = a.H + (a.k ? a.Hkv : 0);
+    if (w >= (long long)a.B * a.Lq * nh) return;
+    const int head = (int)(w % nh);
+    const long long bi = w / nh;
+    const int b = (int)(bi / a.Lq), i = (int)(bi % a.Lq);
+    const int ql = a.q_lens ? a.q_lens[b] : a.Lq;
+    const int n = a.ctx_lens[b];
+    if (ql < 0 || ql > a.Lq || n < ql) {
+        if (lane == 0 && i == 0 && head == 0) atomicOr(a.flags, (ql < 0 || ql > a.Lq) ? FLAG_BAD_Q_LEN : FLAG_BAD_CTX_LEN);
+        return;
+    }
+    if (i >= ql) return;
+    const double pos = (double)a.Ls + (double)(n - ql + i);
+    __half *x = head < a.H ? a.q + ((size_t)bi * a.H + head) * a.D : a.k + ((size_t)bi * a.Hkv + (head - a.H)) * a.D;
+    const int half = a.D / 2;
+    for (int j = lane; j < half; j += 32) {
+        const double ang = pos * exp2(-2.0 * j / a.D * a.log2_base);
+        double sd, cd;
+        sincos(ang, &sd, &cd);
+        const float s = (float)sd, c = (float)cd;
+        const float x0 = __half2float(x[j]), x1 = __half2float(x[j + half]);
+        x[j] = __float2half_rn(x0 * c - x1 * s);
+        x[j + half] = __float2half_rn(x1 * c + x0 * s);
+    }
+}
+
 // ============================================================================= stand-alone relay fusion
 // out = a*o_sys + (1-a)*o_ctx, a = e^lse_sys / (e^lse_sys + e^lse_ctx).
 template <int D>

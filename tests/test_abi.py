@@ -155,6 +155,19 @@ def test_sys_prefill_host_validation(relay):
     assert call(d=_dims(relay, Ls=0)) == relay.OK                    # nothing to do, nothing queued
 
 
+def test_rope_host_validation(relay):
+    lib = relay.lib()
+    vp = lambda x: ctypes.c_void_p(x) if x is not None else None
+    call = lambda base=10000.0, **o: lib.relay_rope(ctypes.byref(_dims(relay)),
+                                                    *[vp(o.get(k, FAKE)) for k in ("q", "k", "cl", "ql")], base,
+                                                    vp(o.get("ws", FAKE)), o.get("ws_bytes", 1 << 20), None)
+    assert call(ws=None) == relay.ERR_WORKSPACE
+    assert call(base=1.0) == relay.ERR_INVALID_ARG
+    assert call(base=float("nan")) == relay.ERR_INVALID_ARG
+    assert call(q=None) == relay.ERR_INVALID_ARG
+    assert call(k=FAKE + 4) == relay.ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors(relay):
     import torch
     q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)

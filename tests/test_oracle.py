@@ -417,3 +417,39 @@ def test_sys_prefill_row_is_decode_over_prefix(oracle_lib):
         od, ld = oracle_lib.attention_rows(case, [(0, 0, h)], "sys")
         np.testing.assert_allclose(o[n], od[0], rtol=0, atol=1e-13)
         np.testing.assert_allclose(l[n], ld[0], rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- rotary positions
+# Rows sit at position Ls + ctx_len - q_len + i.  Pins from the mathematics
+# of the rotation: a D = 2 head turns by exactly the position; in a D = 4 head
+# pair 1 turns by p / sqrt(base); position 0 is the identity; rotations keep
+# pair norms; and scores depend only on relative positions.
+def _rope1(oracle_lib, vec, Ls, n, base=10000.0):
+    x = torch.tensor(vec, dtype=torch.float16).reshape(1, 1, 1, -1)
+    return oracle_lib.rope(x, Ls, torch.tensor([n], dtype=torch.int32), None, base)[0, 0, 0]
+
+
+def test_rope_closed_forms(oracle_lib):
+    for Ls, n in [(0, 1), (5, 3), (1000, 1), (32768, 4096)]:
+        p = Ls + n - 1
+        o = _rope1(oracle_lib, [1.0, 0.0], Ls, n)
+        np.testing.assert_allclose(o, [math.cos(p), math.sin(p)], rtol=0, atol=1e-12)
+        o = _rope1(oracle_lib, [0.0, 1.0, 0.0, 0.0], Ls, n, base=400.0)
+        ang = p / 20.0                                            # p * 400^(-2/4)
+        np.testing.assert_allclose(o, [0.0, math.cos(ang), 0.0, math.sin(ang)], rtol=0, atol=1e-12)
+
+
+def test_rope_identity_norms_and_relative_positions(oracle_lib):
+    g = torch.Generator().manual_seed(8)
+    x = torch.randn(2, 1, 3, 16, generator=g).half()
+    y = torch.randn(2, 1, 3, 16, generator=g).half()
+    one = torch.ones(2, dtype=torch.int32)
+    np.testing.assert_array_equal(oracle_lib.rope(x, 0, one), x.double().numpy())     # position 0
+    ctx = torch.tensor([7, 300], dtype=torch.int32)
+    rx = oracle_lib.rope(x, 11, ctx)
+    pairs = lambda a: np.hypot(a[..., :8], a[..., 8:])
+    np.testing.assert_allclose(pairs(rx), pairs(x.double().numpy()), rtol=1e-13)
+    for shift in (1, 1000):
+        a = (oracle_lib.rope(x, 11, ctx) * oracle_lib.rope(y, 4, ctx)).sum(-1)
+        b = (oracle_lib.rope(x, 11 + shift, ctx) * oracle_lib.rope(y, 4 + shift, ctx)).sum(-1)
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-9)

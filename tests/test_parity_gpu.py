@@ -473,3 +473,65 @@ def test_sys_prefill(Ls, H, Hkv, sample):
     got_l = lse.cpu().double().numpy()[[r[0] for r in rows], [r[1] for r in rows]]
     T.check(got_o, ref_o, "prefill out")
     T.check(got_l, ref_l, "lse prefill")
+
+
+# ----------------------------------------------------------------------------- rotary positions, decode loop
+def _fp16_close(got, ref, what):
+    """within fp16 rounding of the fp64 rotation (half an ulp, doubled for the fp32 arithmetic)"""
+    g = got.cpu().double().numpy()
+    ok = ~np.isnan(ref)
+    err = np.abs(g[ok] - ref[ok])
+    assert np.all(err <= 2.0 ** -10 * np.abs(ref[ok]) + 2.0 ** -24), f"{what}: max err {err.max():.3e}"
+
+
+@pytest.mark.parametrize("name,over", [("tiny_gqa", dict(Lq=3, chunk_requests=2)), ("llama2_7b", {}),
+                                        ("llama2_13b_mixed", dict(Ls=32768))], ids=["gqa_chunks", "llama2_7b", "13b"])
+def test_rope_positions(name, over):
+    import shared_prompt_decode_gb300 as relay
+    case = synth.make_case(synth.workload(name, **over), 51)
+    g = T.to_dev(case)
+    gk = torch.Generator().manual_seed(52)
+    k_new = torch.randn(case.B, case.Lq, case.Hkv, case.D, generator=gk).half()
+    q = g["q"].clone()
+    kd = k_new.to(T.DEV)
+    ws = relay.relay_rope(q, g["ctx_lens"], case.Ls, k_new=kd, q_lens=g["q_lens"])
+    torch.cuda.synchronize()
+    assert relay.device_status(ws) == 0
+    _fp16_close(q, oracle.rope(case.q, case.Ls, case.ctx_lens, case.q_lens), "q")
+    _fp16_close(kd, oracle.rope(k_new, case.Ls, case.ctx_lens, case.q_lens), "k_new")
+
+
+# The attention layer's decode loop, several steps: rotate the step's new q
+# and k at positions offset by the system prompt, append k and v to the pool,
+# attend; the oracle runs the same loop on its own (its own rotation rounded
+# to fp16, its own append) and every step's output is compared.
+@pytest.mark.parametrize("name", ["llama2_7b", "tiny_gqa"])
+def test_decode_loop(name):
+    import shared_prompt_decode_gb300 as relay
+    from dataclasses import replace
+    steps = 4
+    base_case = synth.make_case(name, 61)
+    n0 = base_case.ctx_lens.clone()
+    case = synth.make_case(name, 61, ctx_lens=[int(n) + steps for n in n0])   # tables with room for the new tokens
+    g = T.to_dev(case)
+    kc, vc = g["k_cache"].clone(), g["v_cache"].clone()
+    ref_k, ref_v = case.k_cache.clone(), case.v_cache.clone()
+    gen = torch.Generator().manual_seed(62)
+    for step in range(steps):
+        ctx = (n0 + step + 1).to(torch.int32)
+        q = torch.randn(case.B, 1, case.H, case.D, generator=gen).half()
+        k = torch.randn(case.B, 1, case.Hkv, case.D, generator=gen).half()
+        v = torch.randn(case.B, 1, case.Hkv, case.D, generator=gen).half()
+        # GPU: rotate, append, attend
+        qd, kd, cd = q.to(T.DEV), k.to(T.DEV), ctx.to(T.DEV)
+        relay.relay_rope(qd, cd, case.Ls, k_new=kd)
+        relay.relay_kv_append(kd, v.to(T.DEV), g["block_tables"], cd, kc, vc)
+        out = relay.relay_attention_decode(qd, g["sys_k"], g["sys_v"], kc, vc, g["block_tables"], cd)
+        torch.cuda.synchronize()
+        # oracle: the same loop on its own
+        qr = torch.from_numpy(oracle.rope(q, case.Ls, ctx).astype(np.float16))
+        kr = torch.from_numpy(oracle.rope(k, case.Ls, ctx).astype(np.float16))
+        cur = replace(case, q=qr, ctx_lens=ctx, k_cache=ref_k, v_cache=ref_v)
+        ref_k, ref_v = oracle.kv_append(cur, kr, v)
+        ref_o, ref_l = oracle.attention_full(replace(cur, k_cache=ref_k, v_cache=ref_v))
+        T.check(out, ref_o, f"out (step {step})")
