@@ -420,6 +420,58 @@ def run_relay(args):
                    "peak_source": f"{peaks_p['source']} dense bf16 (fp16 has the same nominal tensor rate)"}
         del q_sys, out_p
 
+    # a two-level prefix tree on this batch: the workload's system prompt shared by every request plus one
+    # 512-token prompt per group of requests (4 groups), served as a tree (global and group prompts each read
+    # once, K = 6 parts merged by relay_fuse_n) and flattened (one relay call per group with its prompts
+    # concatenated, the global prompt re-read per group)
+    tree = None
+    if case.q_lens is None and case.Ls > 0 and case.B % 4 == 0:
+        groups, Lp = 4, 512
+        gt = torch.Generator().manual_seed(args.seed + 11)
+        grp = [((torch.randn(Lp, case.Hkv, case.D, generator=gt) * 0.5).half().to(dev),
+                (torch.randn(Lp, case.Hkv, case.D, generator=gt) * 0.5).half().to(dev)) for _ in range(groups)]
+        masks = [torch.tensor([1 if b % groups == p else 0 for b in range(case.B)], dtype=torch.int32, device=dev)
+                 for p in range(groups)]
+        shp = (case.B, case.Lq, case.H)
+        o_parts = [torch.zeros(*shp, case.D, dtype=torch.float32, device=dev) for _ in range(groups + 2)]
+        l_parts = [torch.full(shp, float("-inf"), dtype=torch.float32, device=dev) for _ in range(groups + 2)]
+        ws_t = [relay.make_workspace(relay.make_dims(g["q"], Ls_, case.num_blocks, case.max_blocks, Hkv=case.Hkv), dev)
+                for Ls_ in [case.Ls] + [Lp] * groups + [0]]
+        out_t = torch.empty_like(out)
+
+        def tree_step():
+            relay.relay_sys_attn(g["q"], g["sys_k"], g["sys_v"], o_sys=o_parts[0], lse_sys=l_parts[0], workspace=ws_t[0])
+            for p, (k, v) in enumerate(grp):
+                relay.relay_sys_attn(g["q"], k, v, q_lens=masks[p], o_sys=o_parts[1 + p], lse_sys=l_parts[1 + p],
+                                     workspace=ws_t[1 + p])
+            relay.relay_ctx_attn(g["q"], g["k_cache"], g["v_cache"], g["block_tables"], g["ctx_lens"],
+                                 o_ctx=o_parts[-1], lse_ctx=l_parts[-1], workspace=ws_t[-1])
+            relay.relay_fuse_n(o_parts, l_parts, out=out_t)
+        ms_t, _ = timed(as_graph(tree_step), max(5, args.steps // 8), args.warmup)
+        # flattened: each group alone, its system prompt = [global; group prompt]
+        flat = []
+        for p, (k, v) in enumerate(grp):
+            idx = torch.tensor([b for b in range(case.B) if b % groups == p], device=dev)
+            fk, fv = torch.cat([g["sys_k"], k]), torch.cat([g["sys_v"], v])
+            qg = g["q"][idx].contiguous()
+            fd = relay.make_dims(qg, fk.shape[0], case.num_blocks, case.max_blocks, Hkv=case.Hkv)
+            flat.append((qg, fk, fv, g["block_tables"][idx].contiguous(), g["ctx_lens"][idx].contiguous(),
+                         torch.empty_like(qg), relay.make_workspace(fd, dev), fd))
+
+        def flat_step():
+            for qg, fk, fv, btg, clg, og, wsg, fd in flat:
+                relay.relay_attention_decode(qg, fk, fv, g["k_cache"], g["v_cache"], btg, clg, out=og, workspace=wsg,
+                                             dims=fd)
+        ms_f, _ = timed(as_graph(flat_step), max(5, args.steps // 8), args.warmup)
+        kv_tok = 2 * case.Hkv * case.D * 2
+        tree = {"groups": groups, "group_prompt_tokens": Lp,
+                "tree_us": 1e3 * statistics.mean(ms_t), "flattened_us": 1e3 * statistics.mean(ms_f),
+                "tree_kv_bytes": (case.Ls + groups * Lp + int(case.ctx_lens.sum())) * kv_tok,
+                "flattened_kv_bytes": (groups * (case.Ls + Lp) + int(case.ctx_lens.sum())) * kv_tok,
+                "launches": {"tree": "5 x relay_sys_attn + relay_ctx_attn (two kernels each) + fuse_n_kernel",
+                             "flattened": "4 x relay_attention_decode (two kernels each)"}}
+        del o_parts, l_parts, ws_t, flat
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=200)
@@ -449,6 +501,7 @@ def run_relay(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(case) * args.steps,
         "sys_prefill": prefill,
+        "tree_prefixes": tree,
         "rope": {"kernel": "rope_kernel (relay_rope: rotary positions offset by the system prompt)",
                  "us": 1e3 * statistics.mean(ms_r), "bytes": rope_bytes,
                  "gbs": rope_bytes / (statistics.mean(ms_r) * 1e-3) / 1e9},

@@ -166,6 +166,22 @@ relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
                                       const int32_t *q_lens, void *out, float *lse_out,
                                       void *ws, size_t ws_bytes, relay_stream_t stream);
 
+/* Relay fusion of K partial results of the same query rows, 1 <= K <= 16:
+ * the convex combination of relay fusion (atyun.com RelayAttention article,
+ * section "RelayAttention") generalised from two parts to K, for a tree of
+ * shared prefixes (one part per shared level, e.g. a global system prompt
+ * and a group prompt, plus the context, each from relay_sys_attn /
+ * relay_ctx_attn):  out = sum_k w_k o_k, w_k = exp(lse_k) / sum_j exp(lse_j),
+ * lse_out = log sum_k exp(lse_k).  A part whose lse is -inf for a row (an
+ * empty segment, or rows relay_sys_attn left untouched after the caller
+ * filled lse with -inf) contributes nothing; all K empty gives out = 0,
+ * lse = -inf.  o_parts / lse_parts are HOST arrays of K device pointers to
+ * [B, Lq, H, D] fp32 and [B, Lq, H] fp32; out [B, Lq, H, D] fp16, lse_out
+ * nullable. */
+relay_status_t relay_fuse_n(const relay_dims_t *dims, int K, const float *const *o_parts,
+                            const float *const *lse_parts, const int32_t *q_lens, void *out,
+                            float *lse_out, relay_stream_t stream);
+
 /* KV append: the step's new keys and values into the paged context pool (the
  * cache write that precedes attention in every decode iteration; the
  * RelayAttention pages keep the request contexts in the paged cache and move

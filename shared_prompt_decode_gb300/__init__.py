@@ -10,6 +10,7 @@ Entry points (same names as the C ABI in include/relay.h):
     relay_sys_attn(...)           step 1: system attention -> fp32 o, lse
     relay_ctx_attn(...)           step 2: context attention -> fp32 o, lse
     relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
+    relay_fuse_n(...)             relay fusion of K parts (a tree of shared prefixes)
     relay_baseline_decode(...)    non-relay paged attention over [system; context]
     relay_kv_append(...)          the step's new K/V rows into the paged pool
     relay_sys_prefill(...)        causal self-attention of the system prompt (filling its cache)
@@ -66,6 +67,7 @@ _SIGS = {
     "relay_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), _VP]),
     "relay_kv_append": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 8 + [ctypes.c_size_t, _VP]),
     "relay_sys_prefill": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 6 + [ctypes.c_size_t, _VP]),
+    "relay_fuse_n": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP, _VP, _VP]),
     "relay_rope": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 4 + [ctypes.c_float, _VP, ctypes.c_size_t, _VP]),
     "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -235,6 +237,27 @@ def relay_fuse(o_sys, lse_sys, o_ctx, lse_ctx, q_lens=None, out=None, lse_out=No
     rc = lib().relay_fuse(ctypes.byref(dims), _ptr(o_sys), _ptr(lse_sys), _ptr(o_ctx), _ptr(lse_ctx), _ptr(q_lens),
                           _ptr(out), _ptr(lse_out), _stream(stream))
     _check(rc, "relay_fuse")
+    return out
+
+
+def relay_fuse_n(o_parts, lse_parts, q_lens=None, out=None, lse_out=None, stream=None):
+    """Relay fusion of K partial results (lists of [B, Lq, H, D] / [B, Lq, H] fp32 tensors)."""
+    K = len(o_parts)
+    if K != len(lse_parts) or K < 1:
+        raise ValueError("o_parts and lse_parts must be non-empty and of the same length")
+    dev = o_parts[0].device
+    for k in range(K):
+        _need(o_parts[k], f"o_parts[{k}]", torch.float32, dev)
+        _need(lse_parts[k], f"lse_parts[{k}]", torch.float32, dev)
+    B, Lq, H, D = o_parts[0].shape
+    dims = Dims(B, Lq, H, D, 0, 16, 0, 0, 0, 0, 0, 0.0)
+    if out is None:
+        out = torch.empty(B, Lq, H, D, dtype=torch.float16, device=dev)
+    op = (ctypes.c_void_p * K)(*[t.data_ptr() for t in o_parts])
+    lp = (ctypes.c_void_p * K)(*[t.data_ptr() for t in lse_parts])
+    rc = lib().relay_fuse_n(ctypes.byref(dims), K, ctypes.cast(op, ctypes.c_void_p), ctypes.cast(lp, ctypes.c_void_p),
+                            _ptr(q_lens), _ptr(out), _ptr(lse_out), _stream(stream))
+    _check(rc, "relay_fuse_n")
     return out
 
 

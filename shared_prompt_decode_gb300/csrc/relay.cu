@@ -449,6 +449,42 @@ relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const fl
     return RELAY_OK;
 }
 
+relay_status_t relay_fuse_n(const relay_dims_t *dims, int K, const float *const *o_parts,
+                            const float *const *lse_parts, const int32_t *q_lens, void *out, float *lse_out,
+                            relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    if (K < 1 || K > kMaxFuseParts || !o_parts || !lse_parts || !out) return RELAY_ERR_INVALID_ARG;
+    FuseN f{};
+    for (int k = 0; k < K; k++) {
+        if (!o_parts[k] || !lse_parts[k] || !aligned(o_parts[k], 16) || !aligned(lse_parts[k], 4))
+            return RELAY_ERR_INVALID_ARG;
+        f.o[k] = o_parts[k];
+        f.lse[k] = lse_parts[k];
+    }
+    if (!aligned(out, 16) || !aligned(lse_out, 4) || !aligned(q_lens, 4)) return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    const DevInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != RELAY_OK) return st;
+    f.B = dims->B;
+    f.Lq = dims->Lq;
+    f.H = dims->H;
+    f.K = K;
+    f.q_lens = q_lens;
+    f.out = static_cast<__half *>(out);
+    f.lse_out = lse_out;
+    const size_t n = (size_t)dims->B * dims->Lq * dims->H * (dims->D / 4);
+    const int grid = (int)std::max<size_t>(1, std::min((n + 255) / 256, (size_t)dev->sms * 8));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dims->D == 128)
+        fuse_n_kernel<128><<<grid, 256, 0, s>>>(f);
+    else
+        fuse_n_kernel<64><<<grid, 256, 0, s>>>(f);
+    return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
+}
+
 relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q, const void *sys_k, const void *sys_v,
                                       const void *k_cache, const void *v_cache, const int32_t *block_tables,
                                       const int32_t *ctx_lens, const int32_t *q_lens, void *out, float *lse_out,
@@ -598,7 +634,8 @@ relay_status_t relay_rope(const relay_dims_t *dims, void *q, void *k_new, const 
     a.Hkv = kv_heads(dims);
     a.D = dims->D;
     a.Ls = dims->Ls;
-    a.log2_base = std::log2((double)base);
+    if (dims->D / 2 > kMaxRopePairs) return RELAY_ERR_UNSUPPORTED;
+    for (int j = 0; j < dims->D / 2; j++) a.inv_freq[j] = std::pow((double)base, -2.0 * j / dims->D);
     a.q = static_cast<__half *>(q);
     a.k = static_cast<__half *>(k_new);
     a.ctx_lens = ctx_lens;

@@ -1510,12 +1510,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const KvAppend a)
 // Rotary position embedding of the step's new rows with the system-prompt
 // offset: row i of request b sits at position Ls + ctx_lens[b] - q_lens[b] + i
 // (the request tokens follow the Ls system tokens).  Rotate-half pairs
-// (j, j + D/2) turn by the angle pos * base^(-2j/D), computed in fp64 (the
-// angle reaches tens of thousands of radians); the rotation itself is fp32.
-// One warp per (row slot, head); q heads first, then the KV heads of k_new.
+// (j, j + D/2) turn by the angle pos * base^(-2j/D).  The angle reaches tens
+// of thousands of radians, so it is formed and reduced modulo 2 pi in fp64
+// (inv_freq[j] = base^(-2j/D) comes from the host in fp64); sine and cosine
+// of the reduced angle, and the rotation, are fp32.  One warp per (row slot,
+// head); q heads first, then the KV heads of k_new.
+constexpr int kMaxRopePairs = 64;
 struct Rope {
     int B, Lq, H, Hkv, D, Ls;
-    double log2_base;
+    double inv_freq[kMaxRopePairs];
     __half *q, *k;                    // [B, Lq, H, D], [B, Lq, Hkv, D] (k nullable)
     const int *ctx_lens, *q_lens;
     unsigned *flags;
@@ -1540,11 +1543,12 @@ __global__ void __launch_bounds__(256) rope_kernel(const Rope a)
     const double pos = (double)a.Ls + (double)(n - ql + i);
     __half *x = head < a.H ? a.q + ((size_t)bi * a.H + head) * a.D : a.k + ((size_t)bi * a.Hkv + (head - a.H)) * a.D;
     const int half = a.D / 2;
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
     for (int j = lane; j < half; j += 32) {
-        const double ang = pos * exp2(-2.0 * j / a.D * a.log2_base);
-        double sd, cd;
-        sincos(ang, &sd, &cd);
-        const float s = (float)sd, c = (float)cd;
+        const double ang = pos * a.inv_freq[j];
+        const float red = (float)(ang - kTwoPi * rint(ang * (1.0 / kTwoPi)));   // in [-pi, pi]
+        float s, c;
+        sincosf(red, &s, &c);
         const float x0 = __half2float(x[j]), x1 = __half2float(x[j + half]);
         x[j] = __float2half_rn(x0 * c - x1 * s);
         x[j + half] = __float2half_rn(x1 * c + x0 * s);
@@ -1588,6 +1592,60 @@ __global__ void __launch_bounds__(256) fuse_kernel(int B, int Lq, int H, const f
         uint2 pk = make_uint2(pack_half2(r.x, r.y), pack_half2(r.z, r.w));
         *reinterpret_cast<uint2 *>(out + row * D + d) = pk;
         if (lse_out && d == 0) lse_out[row] = lse2 * kLn2;
+    }
+}
+
+// ============================================================================= relay fusion of K parts
+// The relay fusion generalised from two parts to K (a tree of shared
+// prefixes: one part per shared level plus the context): out = sum_k w_k o_k,
+// w_k = e^lse_k / sum_j e^lse_j, lse = log sum_k e^lse_k.  A part with
+// lse = -inf for a row contributes nothing to it.
+constexpr int kMaxFuseParts = 16;
+struct FuseN {
+    int B, Lq, H, K;
+    const float *o[kMaxFuseParts];      // [B, Lq, H, D] fp32
+    const float *lse[kMaxFuseParts];    // [B, Lq, H] natural log
+    const int *q_lens;
+    __half *out;
+    float *lse_out;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) fuse_n_kernel(const FuseN f)
+{
+    constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.69314718055994531f;
+    constexpr int V = 4;   // elements per thread
+    const size_t rows = (size_t)f.B * f.Lq * f.H;
+    const size_t n = rows * (D / V);
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = idx / (D / V);
+        const int d = (int)(idx % (D / V)) * V;
+        const int b = (int)(row / ((size_t)f.Lq * f.H));
+        const int i = (int)((row / f.H) % f.Lq);
+        const int ql = f.q_lens ? f.q_lens[b] : f.Lq;
+        if (i >= ql) continue;
+        float M = kNegInf;
+        for (int k = 0; k < f.K; k++) M = fmaxf(M, f.lse[k][row] * kLog2e);
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse2 = kNegInf;
+        if (M != kNegInf) {
+            float W = 0.f;
+            for (int k = 0; k < f.K; k++) {
+                const float w = ex2(f.lse[k][row] * kLog2e - M);
+                if (w == 0.f) continue;                  // an empty part: its o is never read
+                const float4 x = *reinterpret_cast<const float4 *>(f.o[k] + row * D + d);
+                r.x += w * x.x;
+                r.y += w * x.y;
+                r.z += w * x.z;
+                r.w += w * x.w;
+                W += w;
+            }
+            const float inv = 1.f / W;
+            r = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
+            lse2 = M + lg2(W);
+        }
+        *reinterpret_cast<uint2 *>(f.out + row * D + d) = make_uint2(pack_half2(r.x, r.y), pack_half2(r.z, r.w));
+        if (f.lse_out && d == 0) f.lse_out[row] = lse2 * kLn2;
     }
 }
 

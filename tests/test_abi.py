@@ -168,6 +168,23 @@ def test_rope_host_validation(relay):
     assert call(k=FAKE + 4) == relay.ERR_INVALID_ARG
 
 
+def test_fuse_n_host_validation(relay):
+    lib = relay.lib()
+    arr = lambda *xs: ctypes.cast((ctypes.c_void_p * len(xs))(*xs), ctypes.c_void_p)
+    d = _dims(relay)
+    ok_parts = arr(FAKE, FAKE)
+    assert lib.relay_fuse_n(ctypes.byref(d), 0, ok_parts, ok_parts, None, ctypes.c_void_p(FAKE), None, None) \
+        == relay.ERR_INVALID_ARG                                             # K < 1
+    assert lib.relay_fuse_n(ctypes.byref(d), 17, ok_parts, ok_parts, None, ctypes.c_void_p(FAKE), None, None) \
+        == relay.ERR_INVALID_ARG                                             # K > 16
+    assert lib.relay_fuse_n(ctypes.byref(d), 2, arr(FAKE, None), ok_parts, None, ctypes.c_void_p(FAKE), None,
+                            None) == relay.ERR_INVALID_ARG                   # a null part
+    assert lib.relay_fuse_n(ctypes.byref(d), 2, arr(FAKE, FAKE + 4), ok_parts, None, ctypes.c_void_p(FAKE), None,
+                            None) == relay.ERR_INVALID_ARG                   # a misaligned part
+    assert lib.relay_fuse_n(ctypes.byref(_dims(relay, B=0)), 2, ok_parts, ok_parts, None, ctypes.c_void_p(FAKE), None,
+                            None) == relay.OK                                # nothing to do
+
+
 def test_binding_refuses_cpu_tensors(relay):
     import torch
     q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)

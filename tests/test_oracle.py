@@ -453,3 +453,28 @@ def test_rope_identity_norms_and_relative_positions(oracle_lib):
         a = (oracle_lib.rope(x, 11, ctx) * oracle_lib.rope(y, 4, ctx)).sum(-1)
         b = (oracle_lib.rope(x, 11 + shift, ctx) * oracle_lib.rope(y, 4 + shift, ctx)).sum(-1)
         np.testing.assert_allclose(a, b, rtol=0, atol=1e-9)
+
+
+# ----------------------------------------------------------------------------- tree-shaped prefixes
+# A two-level tree: a global prompt shared by every request, a group prompt
+# shared by some, then each request's context.  Attention over the explicit
+# concatenation [global; group; context] equals the cascaded relay fusion
+# fuse(fuse(global, group), context), built from the oracle's (pinned)
+# two-part fusion: the LSE merge is associative.
+def test_cascaded_fusion_equals_concatenation(oracle_lib):
+    from dataclasses import replace
+    base = synth.make_case(synth.workload("tiny_gqa", Ls=48), seed=71)
+    g = torch.Generator().manual_seed(72)
+    grp_k = torch.randn(20, base.Hkv, base.D, generator=g).half()
+    grp_v = torch.randn(20, base.Hkv, base.D, generator=g).half()
+    flat = replace(base, sys_k=torch.cat([base.sys_k, grp_k]), sys_v=torch.cat([base.sys_v, grp_v]))
+    od, ld = oracle_lib.attention_full(flat)
+    rows = oracle_lib.all_rows(base)
+    og, lg = oracle_lib.attention_rows(base, rows, "sys")
+    op, lp = oracle_lib.attention_rows(replace(base, sys_k=grp_k, sys_v=grp_v), rows, "sys")
+    oc, lc = oracle_lib.attention_rows(base, rows, "ctx")
+    o1, l1, _ = oracle_lib.relay_fuse(og, lg, op, lp)
+    o2, l2, _ = oracle_lib.relay_fuse(o1, l1, oc, lc)
+    for n, (b, i, h) in enumerate(rows):
+        np.testing.assert_allclose(o2[n], od[b, i, h], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l2[n], ld[b, i, h], rtol=0, atol=1e-12)

@@ -477,11 +477,12 @@ def test_sys_prefill(Ls, H, Hkv, sample):
 
 # ----------------------------------------------------------------------------- rotary positions, decode loop
 def _fp16_close(got, ref, what):
-    """within fp16 rounding of the fp64 rotation (half an ulp, doubled for the fp32 arithmetic)"""
+    """within fp16 rounding of the rotation (half an ulp, doubled) plus fp32 rounding of its unit-scale
+    products (the rotation is computed in fp32)"""
     g = got.cpu().double().numpy()
     ok = ~np.isnan(ref)
     err = np.abs(g[ok] - ref[ok])
-    assert np.all(err <= 2.0 ** -10 * np.abs(ref[ok]) + 2.0 ** -24), f"{what}: max err {err.max():.3e}"
+    assert np.all(err <= 2.0 ** -10 * np.abs(ref[ok]) + 2.0 ** -20), f"{what}: max err {err.max():.3e}"
 
 
 @pytest.mark.parametrize("name,over", [("tiny_gqa", dict(Lq=3, chunk_requests=2)), ("llama2_7b", {}),
@@ -535,3 +536,56 @@ def test_decode_loop(name):
         ref_k, ref_v = oracle.kv_append(cur, kr, v)
         ref_o, ref_l = oracle.attention_full(replace(cur, k_cache=ref_k, v_cache=ref_v))
         T.check(out, ref_o, f"out (step {step})")
+
+
+# ----------------------------------------------------------------------------- tree-shaped prefixes
+# A global system prompt shared by every request and one group prompt per
+# group of requests (a two-level prefix tree), then each request's context:
+# relay_sys_attn over the global prompt (all rows) and over each group prompt
+# (its group's rows, the others masked by q_lens = 0 and left at lse = -inf),
+# relay_ctx_attn, and relay_fuse_n over the K = groups + 2 parts, against the
+# oracle over each request's explicit concatenation [global; group; context].
+def _tree_inputs(name, groups, Lp, seed):
+    base = synth.make_case(name, seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    grp = [((torch.randn(Lp, base.Hkv, base.D, generator=g) * base.wl.value_scale).half(),
+            (torch.randn(Lp, base.Hkv, base.D, generator=g) * base.wl.value_scale).half()) for _ in range(groups)]
+    return base, grp, [b % groups for b in range(base.B)]
+
+
+def run_tree(base, grp, group_of, g=None):
+    import shared_prompt_decode_gb300 as relay
+    g = g or T.to_dev(base)
+    o_parts, l_parts = [], []
+    o, l = relay.relay_sys_attn(g["q"], g["sys_k"], g["sys_v"])
+    o_parts.append(o)
+    l_parts.append(l)
+    for p, (k, v) in enumerate(grp):
+        mask = torch.tensor([1 if group_of[b] == p else 0 for b in range(base.B)], dtype=torch.int32, device=T.DEV)
+        o = torch.zeros(base.B, base.Lq, base.H, base.D, dtype=torch.float32, device=T.DEV)
+        l = torch.full((base.B, base.Lq, base.H), float("-inf"), dtype=torch.float32, device=T.DEV)
+        relay.relay_sys_attn(g["q"], k.to(T.DEV), v.to(T.DEV), q_lens=mask, o_sys=o, lse_sys=l)
+        o_parts.append(o)
+        l_parts.append(l)
+    o, l = relay.relay_ctx_attn(g["q"], g["k_cache"], g["v_cache"], g["block_tables"], g["ctx_lens"])
+    o_parts.append(o)
+    l_parts.append(l)
+    lse = torch.full((base.B, base.Lq, base.H), float("nan"), dtype=torch.float32, device=T.DEV)
+    out = relay.relay_fuse_n(o_parts, l_parts, lse_out=lse)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("name,groups,Lp", [("llama2_7b", 4, 512), ("tiny_gqa", 2, 40), ("tiny", 3, 0)],
+                         ids=["llama2_7b_4groups", "gqa_2groups", "no_group_prompt"])
+def test_tree_prefixes(name, groups, Lp):
+    from dataclasses import replace
+    base, grp, group_of = _tree_inputs(name, groups, Lp, 81)
+    out, lse = run_tree(base, grp, group_of)
+    got_o, got_l = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    for p, (k, v) in enumerate(grp):
+        flat = replace(base, sys_k=torch.cat([base.sys_k, k]), sys_v=torch.cat([base.sys_v, v]))
+        ref_o, ref_l = oracle.attention_full(flat)
+        idx = [b for b in range(base.B) if group_of[b] == p]
+        T.check(got_o[idx], ref_o[idx], f"out (group {p})")
+        T.check(got_l[idx], ref_l[idx], f"lse (group {p})")
