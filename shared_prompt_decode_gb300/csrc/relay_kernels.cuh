@@ -913,7 +913,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     j /= ri.mt;
     const int split = j % ri.ns;
     const int h = j / ri.ns;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2;
     const int n_ctx = ri.n_ctx;
 
