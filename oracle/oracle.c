@@ -151,12 +151,13 @@ int oracle_attention_rows(const oracle_dims_t *dm, int part,
     if (max_keys < 1) max_keys = 1;
 
 #ifdef _OPENMP
-    if (n_threads > 0) omp_set_num_threads(n_threads);
+    /* n_threads > 0 applies to this call only */
+    const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
 #else
     (void)n_threads;
 #endif
 
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
     {
         const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)max_keys);
         const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)max_keys);
@@ -212,11 +213,12 @@ int oracle_sys_prefill(const oracle_dims_t *dm, const uint16_t *q_sys, const uin
         if (row_t[r] < 0 || row_t[r] >= Ls || row_h[r] < 0 || row_h[r] >= H) return ORACLE_BAD_ARG;
     const int group = H / Hkv;
 #ifdef _OPENMP
-    if (n_threads > 0) omp_set_num_threads(n_threads);
+    /* n_threads > 0 applies to this call only */
+    const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
 #else
     (void)n_threads;
 #endif
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
     {
         const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)Ls);
         const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)Ls);
