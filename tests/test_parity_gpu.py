@@ -445,12 +445,13 @@ def test_kv_append_device_checks():
 # prompt at the Llama-2-13B shape.
 PREFILL_CASES = [
     (300, 4, 2, None), (2048, 32, 32, None), (1000, 8, 1, None), (129, 2, 2, None),
-    (32768, 40, 40, 192),
+    (32768, 40, 40, 192), (1, 2, 2, None), (64, 3, 1, None), (200, 8, 2, None),
 ]
 
 
 @pytest.mark.parametrize("Ls,H,Hkv,sample", PREFILL_CASES,
-                         ids=["Ls300_gqa", "Ls2048_llama2_7b", "Ls1000_mqa", "Ls129_ragged", "Ls32768_13b_sampled"])
+                         ids=["Ls300_gqa", "Ls2048_llama2_7b", "Ls1000_mqa", "Ls129_ragged", "Ls32768_13b_sampled",
+                              "Ls1_single_key", "Ls64_one_partial_tile", "Ls200_group4"])
 def test_sys_prefill(Ls, H, Hkv, sample):
     import shared_prompt_decode_gb300 as relay
     g = torch.Generator().manual_seed(Ls + H)
