@@ -16,6 +16,14 @@
  * The result equals causal attention over the concatenation
  * [system prompt; request context] exactly, up to rounding.
  *
+ * Entry points: relay_attention_decode (all three steps; also an
+ * allocation-free variant), relay_sys_attn / relay_ctx_attn / relay_fuse
+ * (the steps one at a time), relay_fuse_n (fusion of K parts: a tree of
+ * shared prefixes), relay_baseline_decode (the non-relay formulation), and
+ * the steps on either side of the path: relay_kv_append (cache write),
+ * relay_rope (rotary positions offset by the system prompt) and
+ * relay_sys_prefill (causal attention of the system prompt itself).
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - fp16 arrays are IEEE binary16 (`const void*` here); accumulation is fp32.
