@@ -431,7 +431,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
                           bool have_lk0 = false, float lk0 = 0.f)
 {
     constexpr int V = D / 32;
-    constexpr int CH = 8;
+    constexpr int CH = 16;     // partial rows in flight per lane (one round for up to 16 partials)
     constexpr float kLn2 = 0.69314718055994531f;
     const int lane = threadIdx.x & 31;
     const int n = n_sys + n_ctx;
