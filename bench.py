@@ -47,13 +47,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 KERNEL_SOURCES = ["shared_prompt_decode_gb300/csrc/relay.cu", "shared_prompt_decode_gb300/csrc/relay_kernels.cuh",
                   "shared_prompt_decode_gb300/csrc/sys_tc.cuh"]
 # The library runs the system step on the tcgen05 kernel, a third launch per
-# step, when D = 128, Ls > 0 and the batch holds more than this many query
-# rows per head (the dispatch rule of relay.cu).
+# step, when D = 128, Ls > 0 and the batch holds more than this many virtual
+# rows per KV head (query rows x query heads per KV head; the dispatch rule of
+# relay.cu).
 TC_MIN_ROWS = 256
 
 
 def launches_per_step(case):
-    return 3 if (case.D == 128 and case.Ls > 0 and case.total_q() > TC_MIN_ROWS) else 2
+    rows = case.total_q() * (case.H // case.Hkv)
+    return 3 if (case.D == 128 and case.Ls > 0 and rows > TC_MIN_ROWS) else 2
 
 
 # ----------------------------------------------------------------------------- helpers
