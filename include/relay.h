@@ -107,7 +107,9 @@ typedef struct {
     int32_t block_size;         /* paged block size: must be 16 */
     int32_t num_blocks;         /* blocks in the paged pool */
     int32_t max_blocks_per_seq; /* row stride of block_tables */
-    int32_t max_q_total;        /* bound on sum(q_lens); 0 means B*Lq */
+    int32_t max_q_total;        /* bound on sum(q_lens); 0 means B*Lq.  A call
+                                   without q_lens needs 0 or >= B*Lq, else it
+                                   returns RELAY_ERR_INVALID_ARG */
     int32_t ctx_split;          /* context keys per work item for 1-row requests;
                                    0 = automatic; else a multiple of 64 */
     int32_t sys_range;          /* system keys per work item; 0 = automatic;

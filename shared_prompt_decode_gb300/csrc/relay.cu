@@ -255,6 +255,10 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     if (!aligned(ws, 256)) return RELAY_ERR_INVALID_ARG;
     Plan pl = make_plan(d, mode);
     if (ws_bytes < pl.total) return RELAY_ERR_WORKSPACE;
+    // without q_lens every request has Lq rows: the partial slots are laid out
+    // for max_q_total rows, so a smaller bound is an argument error (with
+    // q_lens the kernel checks their sum on the device)
+    if (!p.q_lens && (long long)d->B * d->Lq > pl.Mtot) return RELAY_ERR_INVALID_ARG;
     const DevInfo *dev = nullptr;
     relay_status_t st = device_info(&dev);
     if (st != RELAY_OK) return st;

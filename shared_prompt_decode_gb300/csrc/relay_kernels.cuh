@@ -1422,8 +1422,12 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     if (p.q_lens == nullptr) {
         // every request has Lq rows: row r is row r % Lq of request r / Lq, so
         // no schedule table is needed; the request's context length, the
-        // split size and the log-sum-exps of every slot the row may use are
-        // loaded together (one round trip)
+        // split size and the log-sum-exps of the first 32 slots the row may
+        // use are loaded together (one round trip).  Lane k's slot is part k
+        // of the row whatever its context turns out to be (system ranges
+        // first, then context splits from ctx_base), which is what merge_row
+        // reads for its first 32 parts; slots past the row's own parts are
+        // inside the workspace and masked there.
         const int lane = threadIdx.x & 31;
         const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
         const int r = w / p.H, h = w % p.H;
@@ -1431,19 +1435,17 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
         const int b = r / p.Lq;
         const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
         const int ncand = n_sys + (has_ctx(p.mode) ? p.c_max : 0);
-        if (ncand <= 32) {
-            float lk = kNegInf;
-            if (lane < ncand) {
-                const int part = lane < n_sys ? lane : p.ctx_base + (lane - n_sys);
-                lk = __ldcg(p.part_lse + part_row(p, part, r, h));
-            }
-            const int tps = __ldcg(p.sched);
-            const int nc = has_ctx(p.mode) ? __ldg(p.ctx_lens + b) : 0;
-            if (tps < 0) return;
-            const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
-            merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, true, lk);
-            return;
+        float lk = kNegInf;
+        if (lane < ncand) {
+            const int part = lane < n_sys ? lane : p.ctx_base + (lane - n_sys);
+            lk = __ldcg(p.part_lse + part_row(p, part, r, h));
         }
+        const int tps = __ldcg(p.sched);
+        const int nc = has_ctx(p.mode) ? __ldg(p.ctx_lens + b) : 0;
+        if (tps < 0) return;
+        const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
+        merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, true, lk);
+        return;
     }
     const int tps = p.sched[0];
     if (tps < 0) return;                 // the producer rejected its inputs

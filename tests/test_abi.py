@@ -114,6 +114,8 @@ def test_host_validation(relay):
     assert _call_decode(relay, d, ws=None) == relay.ERR_WORKSPACE
     assert _call_decode(relay, d, ws_bytes=1024) == relay.ERR_WORKSPACE
     assert _call_decode(relay, d, ws=FAKE + 16) == relay.ERR_INVALID_ARG    # workspace not 256-aligned
+    # no q_lens: B * Lq rows, above a smaller max_q_total (with q_lens the device checks the sum)
+    assert _call_decode(relay, _dims(relay, Lq=2, max_q_total=3)) == relay.ERR_INVALID_ARG
     # Ls == 0: the system cache may be absent; B == 0: nothing to do, nothing queued
     assert _call_decode(relay, _dims(relay, B=0)) == relay.OK
     lib = relay.lib()
