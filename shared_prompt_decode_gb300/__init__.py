@@ -6,7 +6,8 @@ memory and the current stream.  There is no CPU or PyTorch fallback: if the
 library is missing, importing the binding's functions raises.
 
 Entry points (same names as the C ABI in include/relay.h):
-    relay_attention_decode(...)   all three steps in one launch
+    relay_attention_decode(...)   all three steps, queued as one unit (two kernels; three with
+                                  the tensor-core system step)
     relay_sys_attn(...)           step 1: system attention -> fp32 o, lse
     relay_ctx_attn(...)           step 2: context attention -> fp32 o, lse
     relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
@@ -121,6 +122,50 @@ def _need(t, name, dtype, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _shape(t, name, shape):
+    """Shape check of a tensor the kernels index by the dims (an optional one may be None); done before the
+    device checks, so that a wrong size never reaches the library as a plain pointer."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _same(a, b, names):
+    if tuple(a.shape) != tuple(b.shape):
+        raise ValueError(f"{names[0]} {tuple(a.shape)} and {names[1]} {tuple(b.shape)} must have the same shape")
+
+
+def _opt(t, name, dtype, device):
+    if t is not None:
+        _need(t, name, dtype, device)
+
+
+def _check_dims(dims: Dims, q, Ls=None, pool=None, block_tables=None):
+    """Explicit dims must describe the tensors: the kernels take every size and stride from them."""
+    B, Lq, H, D = q.shape
+    if (dims.B, dims.Lq, dims.H, dims.D) != (B, Lq, H, D):
+        raise ValueError(f"dims {dims} do not match q {tuple(q.shape)}")
+    if Ls is not None and dims.Ls != Ls:
+        raise ValueError(f"dims.Ls = {dims.Ls}, but the system cache holds {Ls} tokens")
+    if pool is not None and dims.num_blocks > pool.shape[0]:
+        raise ValueError(f"dims.num_blocks = {dims.num_blocks} exceeds the pool's {pool.shape[0]} blocks")
+    if block_tables is not None and dims.max_blocks_per_seq != block_tables.shape[1]:
+        raise ValueError(f"dims.max_blocks_per_seq = {dims.max_blocks_per_seq}, but block_tables rows hold "
+                         f"{block_tables.shape[1]} entries")
+
+
+def _pool_shapes(k, v, D, names):
+    _same(k, v, names)
+    if k.dim() != 4 or k.shape[2] != 16 or k.shape[3] != D:
+        raise ValueError(f"{names[0]} {tuple(k.shape)} must be [num_blocks, Hkv, 16, {D}]")
+
+
+def _table_shapes(B, block_tables, ctx_lens, q_lens):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError(f"block_tables {tuple(block_tables.shape)} must be [{B}, max_blocks]")
+    _shape(ctx_lens, "ctx_lens", (B,))
+    _shape(q_lens, "q_lens", (B,))
+
+
 def make_dims(q: torch.Tensor, Ls: int, num_blocks: int, max_blocks: int, scale: Optional[float] = None,
               max_q_total: int = 0, ctx_split: int = 0, sys_range: int = 0, Hkv: int = 0) -> Dims:
     """Hkv: KV heads of the caches (0: as many as query heads)."""
@@ -157,25 +202,32 @@ def _ws(dims, workspace, device):
 def relay_attention_decode(q, sys_k, sys_v, k_cache, v_cache, block_tables, ctx_lens, q_lens=None,
                            out=None, lse_out=None, workspace=None, scale=None, max_q_total=0,
                            ctx_split=0, sys_range=0, stream=None, dims=None):
-    """All three steps in one launch.  Returns out [B, Lq, H, D] fp16."""
+    """All three steps, queued as one unit on the stream.  Returns out [B, Lq, H, D] fp16."""
     dev = q.device
+    B, Lq, H, D = q.shape
+    _same(sys_k, sys_v, ("sys_k", "sys_v"))
+    if sys_k.dim() != 3 or sys_k.shape[2] != D:
+        raise ValueError(f"sys_k {tuple(sys_k.shape)} must be [Ls, Hkv, {D}]")
+    _pool_shapes(k_cache, v_cache, D, ("k_cache", "v_cache"))
+    _table_shapes(B, block_tables, ctx_lens, q_lens)
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", (B, Lq, H))
     _need(q, "q", torch.float16)
     for name, t in (("sys_k", sys_k), ("sys_v", sys_v), ("k_cache", k_cache), ("v_cache", v_cache)):
         _need(t, name, torch.float16, dev)
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
-    if q_lens is not None:
-        _need(q_lens, "q_lens", torch.int32, dev)
+    _opt(q_lens, "q_lens", torch.int32, dev)
     if dims is None:
         dims = make_dims(q, sys_k.shape[0], k_cache.shape[0], block_tables.shape[1], scale,
                          max_q_total, ctx_split, sys_range, k_cache.shape[1])
+    _check_dims(dims, q, sys_k.shape[0], k_cache, block_tables)
     _check_kv(dims, sys_k, "sys_k")
     _check_kv(dims, k_cache, "k_cache")
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.float16, dev)
-    if lse_out is not None:
-        _need(lse_out, "lse_out", torch.float32, dev)
+    _opt(lse_out, "lse_out", torch.float32, dev)
     ws = _ws(dims, workspace, dev)
     rc = lib().relay_attention_decode(ctypes.byref(dims), _ptr(q), _ptr(sys_k), _ptr(sys_v), _ptr(k_cache),
                                       _ptr(v_cache), _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
@@ -187,10 +239,19 @@ def relay_attention_decode(q, sys_k, sys_v, k_cache, v_cache, block_tables, ctx_
 def relay_sys_attn(q, sys_k, sys_v, q_lens=None, o_sys=None, lse_sys=None, workspace=None, scale=None,
                    max_q_total=0, sys_range=0, stream=None, max_blocks=0):
     dev = q.device
+    B, Lq, H, D = q.shape
+    _same(sys_k, sys_v, ("sys_k", "sys_v"))
+    if sys_k.dim() != 3 or sys_k.shape[2] != D:
+        raise ValueError(f"sys_k {tuple(sys_k.shape)} must be [Ls, Hkv, {D}]")
+    _shape(q_lens, "q_lens", (B,))
+    _shape(o_sys, "o_sys", q.shape)
+    _shape(lse_sys, "lse_sys", (B, Lq, H))
     _need(q, "q", torch.float16)
     _need(sys_k, "sys_k", torch.float16, dev)
     _need(sys_v, "sys_v", torch.float16, dev)
-    B, Lq, H, D = q.shape
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(o_sys, "o_sys", torch.float32, dev)
+    _opt(lse_sys, "lse_sys", torch.float32, dev)
     dims = make_dims(q, sys_k.shape[0], 0, max_blocks, scale, max_q_total, 0, sys_range, sys_k.shape[1])
     if o_sys is None:
         o_sys = torch.empty(B, Lq, H, D, dtype=torch.float32, device=dev)
@@ -206,12 +267,19 @@ def relay_sys_attn(q, sys_k, sys_v, q_lens=None, o_sys=None, lse_sys=None, works
 def relay_ctx_attn(q, k_cache, v_cache, block_tables, ctx_lens, q_lens=None, o_ctx=None, lse_ctx=None,
                    workspace=None, scale=None, max_q_total=0, ctx_split=0, stream=None):
     dev = q.device
+    B, Lq, H, D = q.shape
+    _pool_shapes(k_cache, v_cache, D, ("k_cache", "v_cache"))
+    _table_shapes(B, block_tables, ctx_lens, q_lens)
+    _shape(o_ctx, "o_ctx", q.shape)
+    _shape(lse_ctx, "lse_ctx", (B, Lq, H))
     _need(q, "q", torch.float16)
     _need(k_cache, "k_cache", torch.float16, dev)
     _need(v_cache, "v_cache", torch.float16, dev)
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
-    B, Lq, H, D = q.shape
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(o_ctx, "o_ctx", torch.float32, dev)
+    _opt(lse_ctx, "lse_ctx", torch.float32, dev)
     dims = make_dims(q, 0, k_cache.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0,
                      k_cache.shape[1])
     if o_ctx is None:
@@ -228,9 +296,18 @@ def relay_ctx_attn(q, k_cache, v_cache, block_tables, ctx_lens, q_lens=None, o_c
 
 def relay_fuse(o_sys, lse_sys, o_ctx, lse_ctx, q_lens=None, out=None, lse_out=None, stream=None):
     dev = o_sys.device
+    B, Lq, H, D = o_sys.shape
+    _shape(o_ctx, "o_ctx", o_sys.shape)
+    _shape(lse_sys, "lse_sys", (B, Lq, H))
+    _shape(lse_ctx, "lse_ctx", (B, Lq, H))
+    _shape(q_lens, "q_lens", (B,))
+    _shape(out, "out", o_sys.shape)
+    _shape(lse_out, "lse_out", (B, Lq, H))
     for name, t in (("o_sys", o_sys), ("lse_sys", lse_sys), ("o_ctx", o_ctx), ("lse_ctx", lse_ctx)):
         _need(t, name, torch.float32, dev)
-    B, Lq, H, D = o_sys.shape
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(out, "out", torch.float16, dev)
+    _opt(lse_out, "lse_out", torch.float32, dev)
     dims = Dims(B, Lq, H, D, 0, 16, 0, 0, 0, 0, 0, 0.0)
     if out is None:
         out = torch.empty(B, Lq, H, D, dtype=torch.float16, device=dev)
@@ -246,10 +323,19 @@ def relay_fuse_n(o_parts, lse_parts, q_lens=None, out=None, lse_out=None, stream
     if K != len(lse_parts) or K < 1:
         raise ValueError("o_parts and lse_parts must be non-empty and of the same length")
     dev = o_parts[0].device
+    B, Lq, H, D = o_parts[0].shape
+    for k in range(K):
+        _shape(o_parts[k], f"o_parts[{k}]", (B, Lq, H, D))
+        _shape(lse_parts[k], f"lse_parts[{k}]", (B, Lq, H))
+    _shape(q_lens, "q_lens", (B,))
+    _shape(out, "out", (B, Lq, H, D))
+    _shape(lse_out, "lse_out", (B, Lq, H))
     for k in range(K):
         _need(o_parts[k], f"o_parts[{k}]", torch.float32, dev)
         _need(lse_parts[k], f"lse_parts[{k}]", torch.float32, dev)
-    B, Lq, H, D = o_parts[0].shape
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(out, "out", torch.float16, dev)
+    _opt(lse_out, "lse_out", torch.float32, dev)
     dims = Dims(B, Lq, H, D, 0, 16, 0, 0, 0, 0, 0, 0.0)
     if out is None:
         out = torch.empty(B, Lq, H, D, dtype=torch.float16, device=dev)
@@ -265,15 +351,27 @@ def relay_baseline_decode(q, k_pool, v_pool, sys_block_ids, Ls, block_tables, ct
                           out=None, lse_out=None, workspace=None, scale=None, max_q_total=0, ctx_split=0,
                           stream=None, dims=None):
     dev = q.device
+    B, Lq, H, D = q.shape
+    _pool_shapes(k_pool, v_pool, D, ("k_pool", "v_pool"))
+    _table_shapes(B, block_tables, ctx_lens, q_lens)
+    if sys_block_ids.dim() != 1 or sys_block_ids.shape[0] < (int(Ls) + 15) // 16:
+        raise ValueError(f"sys_block_ids {tuple(sys_block_ids.shape)} must list the {(int(Ls) + 15) // 16} "
+                         f"blocks of the {int(Ls)} system tokens")
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", (B, Lq, H))
     _need(q, "q", torch.float16)
     _need(k_pool, "k_pool", torch.float16, dev)
     _need(v_pool, "v_pool", torch.float16, dev)
     _need(sys_block_ids, "sys_block_ids", torch.int32, dev)
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(out, "out", torch.float16, dev)
+    _opt(lse_out, "lse_out", torch.float32, dev)
     if dims is None:
         dims = make_dims(q, Ls, k_pool.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, 0,
                          k_pool.shape[1])
+    _check_dims(dims, q, int(Ls), k_pool, block_tables)
     _check_kv(dims, k_pool, "k_pool")
     if out is None:
         out = torch.empty_like(q)
@@ -290,16 +388,17 @@ def relay_kv_append(k_new, v_new, block_tables, ctx_lens, k_cache, v_cache, q_le
     """Write the step's new K/V rows ([B, Lq, Hkv, D] fp16) into the paged pools in place, at each request's
     last q_lens[b] context positions.  Device-side problems are flagged in `workspace` (device_status)."""
     dev = k_new.device
+    B, Lq, Hkv, D = k_new.shape
+    if v_new.shape != k_new.shape or k_cache.shape != v_cache.shape or k_cache.dim() != 4 or \
+            k_cache.shape[1] != Hkv or k_cache.shape[2] != 16 or k_cache.shape[3] != D:
+        raise ValueError("k_new/v_new [B, Lq, Hkv, D] and the pools [num_blocks, Hkv, 16, D] disagree")
+    _table_shapes(B, block_tables, ctx_lens, q_lens)
     _need(k_new, "k_new", torch.float16)
     for name, t in (("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
         _need(t, name, torch.float16, dev)
     _need(block_tables, "block_tables", torch.int32, dev)
     _need(ctx_lens, "ctx_lens", torch.int32, dev)
-    if q_lens is not None:
-        _need(q_lens, "q_lens", torch.int32, dev)
-    B, Lq, Hkv, D = k_new.shape
-    if v_new.shape != k_new.shape or k_cache.shape != v_cache.shape or k_cache.shape[1] != Hkv or k_cache.shape[3] != D:
-        raise ValueError("k_new/v_new [B, Lq, Hkv, D] and the pools [num_blocks, Hkv, 16, D] disagree")
+    _opt(q_lens, "q_lens", torch.int32, dev)
     dims = Dims(B, Lq, Hkv, D, 0, 16, k_cache.shape[0], block_tables.shape[1], 0, 0, 0, 0.0, Hkv)
     if workspace is None:
         workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
@@ -314,12 +413,14 @@ def relay_sys_prefill(q_sys, sys_k, sys_v, out=None, lse_out=None, workspace=Non
     """Causal self-attention of the system prompt (the attention step of filling its cache offline):
     q_sys [Ls, H, 128] fp16, sys_k / sys_v [Ls, Hkv, 128] fp16 -> out [Ls, H, 128] fp16 (and lse_out [Ls, H])."""
     dev = q_sys.device
+    Ls, H, D = q_sys.shape
+    if sys_k.shape != sys_v.shape or sys_k.dim() != 3 or sys_k.shape[0] != Ls or sys_k.shape[2] != D:
+        raise ValueError("q_sys [Ls, H, D] and sys_k / sys_v [Ls, Hkv, D] disagree")
+    _shape(out, "out", q_sys.shape)
+    _shape(lse_out, "lse_out", (Ls, H))
     _need(q_sys, "q_sys", torch.float16)
     _need(sys_k, "sys_k", torch.float16, dev)
     _need(sys_v, "sys_v", torch.float16, dev)
-    Ls, H, D = q_sys.shape
-    if sys_k.shape != sys_v.shape or sys_k.shape[0] != Ls or sys_k.shape[2] != D:
-        raise ValueError("q_sys [Ls, H, D] and sys_k / sys_v [Ls, Hkv, D] disagree")
     dims = Dims(1, 1, H, D, Ls, 16, 0, 0, 0, 0, 0, 0.0 if scale is None else float(scale), sys_k.shape[1])
     if out is None:
         out = torch.empty_like(q_sys)
@@ -338,14 +439,16 @@ def relay_rope(q, ctx_lens, Ls, k_new=None, q_lens=None, base=10000.0, workspace
     """Rotary embedding in place of q [B, Lq, H, D] (and k_new [B, Lq, Hkv, D]) at positions
     Ls + ctx_lens[b] - q_lens[b] + i: the request tokens follow the Ls system tokens."""
     dev = q.device
-    _need(q, "q", torch.float16)
-    _need(ctx_lens, "ctx_lens", torch.int32, dev)
-    if k_new is not None:
-        _need(k_new, "k_new", torch.float16, dev)
-    if q_lens is not None:
-        _need(q_lens, "q_lens", torch.int32, dev)
     B, Lq, H, D = q.shape
     Hkv = k_new.shape[2] if k_new is not None else H
+    if k_new is not None and (k_new.dim() != 4 or tuple(k_new.shape) != (B, Lq, Hkv, D)):
+        raise ValueError(f"k_new {tuple(k_new.shape)} must be [{B}, {Lq}, Hkv, {D}]")
+    _shape(ctx_lens, "ctx_lens", (B,))
+    _shape(q_lens, "q_lens", (B,))
+    _need(q, "q", torch.float16)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    _opt(k_new, "k_new", torch.float16, dev)
+    _opt(q_lens, "q_lens", torch.int32, dev)
     dims = Dims(B, Lq, H, D, int(Ls), 16, 0, 0, 0, 0, 0, 0.0, Hkv)
     if workspace is None:
         workspace = torch.zeros(256, dtype=torch.uint8, device=dev)

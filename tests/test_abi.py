@@ -187,9 +187,71 @@ def test_fuse_n_host_validation(relay):
                             None) == relay.OK                                # nothing to do
 
 
-def test_binding_refuses_cpu_tensors(relay):
+def _decode_args(B=2, Lq=1, H=4, Hkv=4, D=64, Ls=32, nb=8, mb=4):
     import torch
-    q = torch.zeros(1, 1, 1, 64, dtype=torch.float16)
-    with pytest.raises(ValueError):
-        relay.relay_attention_decode(q, q, q, q, q, torch.zeros(1, 1, dtype=torch.int32),
-                                     torch.zeros(1, dtype=torch.int32))
+    f16, i32 = torch.float16, torch.int32
+    return dict(q=torch.zeros(B, Lq, H, D, dtype=f16), sys_k=torch.zeros(Ls, Hkv, D, dtype=f16),
+                sys_v=torch.zeros(Ls, Hkv, D, dtype=f16), k_cache=torch.zeros(nb, Hkv, 16, D, dtype=f16),
+                v_cache=torch.zeros(nb, Hkv, 16, D, dtype=f16), block_tables=torch.zeros(B, mb, dtype=i32),
+                ctx_lens=torch.zeros(B, dtype=i32))
+
+
+def test_binding_refuses_cpu_tensors(relay):
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        relay.relay_attention_decode(**_decode_args())
+
+
+def test_binding_checks_shapes(relay):
+    """Every tensor the kernels index through the dims is shape-checked before any pointer reaches the
+    library (these raise before the CUDA-tensor check, so no device is needed)."""
+    import torch
+    f16, f32, i32 = torch.float16, torch.float32, torch.int32
+    a = _decode_args()
+    bad = [
+        dict(out=torch.zeros(2, 1, 4, 32, dtype=f16)),                      # out smaller than q
+        dict(lse_out=torch.zeros(2, 1, 3, dtype=f32)),
+        dict(q_lens=torch.zeros(3, dtype=i32)),
+        dict(ctx_lens=torch.zeros(1, dtype=i32)),
+        dict(block_tables=torch.zeros(3, 4, dtype=i32)),
+        dict(sys_v=torch.zeros(31, 4, 64, dtype=f16)),                      # sys_k / sys_v disagree
+        dict(sys_k=torch.zeros(32, 4, 128, dtype=f16), sys_v=torch.zeros(32, 4, 128, dtype=f16)),
+        dict(v_cache=torch.zeros(7, 4, 16, 64, dtype=f16)),
+        dict(k_cache=torch.zeros(8, 4, 8, 64, dtype=f16), v_cache=torch.zeros(8, 4, 8, 64, dtype=f16)),
+    ]
+    for over in bad:
+        with pytest.raises(ValueError) as e:
+            relay.relay_attention_decode(**{**a, **over})
+        assert "CUDA" not in str(e.value), (over.keys(), e.value)
+    # explicit dims must describe the tensors (sizes and the block-table stride come from them)
+    q = a["q"]
+    for over in (dict(B=3), dict(Ls=16), dict(num_blocks=9), dict(max_blocks_per_seq=5)):
+        d = relay.make_dims(q, 32, 8, 4)
+        for k, v in over.items():
+            setattr(d, k, v)
+        with pytest.raises(ValueError) as e:
+            relay._check_dims(d, q, 32, a["k_cache"], a["block_tables"])
+        assert "dims" in str(e.value)
+    relay._check_dims(relay.make_dims(q, 32, 8, 4), q, 32, a["k_cache"], a["block_tables"])
+    # the other entry points
+    o = torch.zeros(2, 1, 4, 64, dtype=f32)
+    l = torch.zeros(2, 1, 4, dtype=f32)
+    with pytest.raises(ValueError, match="o_sys"):
+        relay.relay_sys_attn(q, a["sys_k"], a["sys_v"], o_sys=torch.zeros(2, 1, 4, 32, dtype=f32))
+    with pytest.raises(ValueError, match="lse_ctx"):
+        relay.relay_ctx_attn(q, a["k_cache"], a["v_cache"], a["block_tables"], a["ctx_lens"],
+                             lse_ctx=torch.zeros(2, 4, dtype=f32))
+    with pytest.raises(ValueError, match="lse_ctx"):
+        relay.relay_fuse(o, l, o, torch.zeros(2, 1, 5, dtype=f32))
+    with pytest.raises(ValueError, match="o_parts"):
+        relay.relay_fuse_n([o, torch.zeros(2, 1, 4, 32, dtype=f32)], [l, l])
+    with pytest.raises(ValueError, match="sys_block_ids"):
+        relay.relay_baseline_decode(q, a["k_cache"], a["v_cache"], torch.zeros(1, dtype=i32), 32,
+                                    a["block_tables"], a["ctx_lens"])
+    with pytest.raises(ValueError, match="ctx_lens"):
+        relay.relay_kv_append(torch.zeros(2, 1, 4, 64, dtype=f16), torch.zeros(2, 1, 4, 64, dtype=f16),
+                              a["block_tables"], torch.zeros(5, dtype=i32), a["k_cache"], a["v_cache"])
+    with pytest.raises(ValueError, match="lse_out"):
+        relay.relay_sys_prefill(torch.zeros(32, 4, 128, dtype=f16), torch.zeros(32, 4, 128, dtype=f16),
+                                torch.zeros(32, 4, 128, dtype=f16), lse_out=torch.zeros(32, 2, dtype=f32))
+    with pytest.raises(ValueError, match="k_new"):
+        relay.relay_rope(q, a["ctx_lens"], 32, k_new=torch.zeros(2, 2, 4, 64, dtype=f16))
