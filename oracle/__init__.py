@@ -57,8 +57,14 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB_PATH)
+            # RELAY_ORACLE_LIB: a copy of the oracle with a mistake planted in
+            # it, built by tests/test_oracle_mutations.py to show that the pins
+            # catch it; unset, the oracle is built from oracle.c as it stands
+            path = os.environ.get("RELAY_ORACLE_LIB")
+            if not path:
+                build()
+                path = _LIB_PATH
+            lib = ctypes.CDLL(path)
             lib.oracle_attention_rows.restype = ctypes.c_int
             lib.oracle_kv_append.restype = ctypes.c_int
             lib.oracle_sys_prefill.restype = ctypes.c_int
