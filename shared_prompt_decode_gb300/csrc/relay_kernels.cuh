@@ -9,17 +9,23 @@
 //
 // One CTA of 8 warps per SM works through two queues.
 //
-// Phase 1, row items (the whole CTA per item):
-//   system item  (h, key range, 128-row tile): 128 query rows of the whole
-//                batch against one range of system keys -- the matrix-matrix
+// Phase 1, row items.  The CTA's warps form two independent row teams of 4
+// warps (each with half of the staging ring and its own named barrier); a
+// team takes one item at a time:
+//   system item  (KV head, key range, 64-row tile): 64 virtual rows of the
+//                whole batch (query row x query head of the KV head's group)
+//                against one range of system keys -- the matrix-matrix
 //                product of the system-attention step (atyun.com RelayAttention
-//                article, section "RelayAttention").  Each warp owns 16 rows.
-//   multi-row context item (b, h, split, 128-row tile): the rows of one
+//                article, section "RelayAttention").  Each warp owns 16 rows;
+//                when the rows fill fewer warps, the warps split each tile's
+//                keys and combine their softmax states at the end.
+//   multi-row context item (b, h, split, 64-row tile): the rows of one
 //                request that carries several query tokens against a range of
 //                its paged context, with the causal mask.
-//   K/V tiles of 64 keys flow through a deep cp.async ring in XOR-swizzled
-//   shared memory; S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in,
-//   fp32 accumulate) with an online softmax in the log2 domain.
+//   K/V tiles of 64 keys flow through a cp.async ring in XOR-swizzled shared
+//   memory; S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in, fp32
+//   accumulate) with an online softmax in the log2 domain.  A team with no
+//   row item left moves on to phase 2 at once.
 //
 // Phase 2, decode items (one warp per item, each warp independent):
 //   (b, h, split): the one query row of a decode request against a range of

@@ -104,6 +104,11 @@ def test_host_validation(relay):
     assert _call_decode(relay, _dims(relay, D=96)) == relay.ERR_UNSUPPORTED
     assert _call_decode(relay, _dims(relay, block_size=8)) == relay.ERR_UNSUPPORTED
     assert _call_decode(relay, _dims(relay, Hkv=5)) == relay.ERR_INVALID_ARG   # 32 query heads, 5 KV heads
+    # grouped-query and multi-query heads pass the shape checks: the calls get as far as the pointer checks
+    # (q missing) or, with nothing to do, return OK without queueing anything
+    for hkv in (1, 2, 8, 16):
+        assert _call_decode(relay, _dims(relay, Hkv=hkv), q=None) == relay.ERR_INVALID_ARG, hkv
+        assert _call_decode(relay, _dims(relay, Hkv=hkv, B=0)) == relay.OK, hkv
     assert _call_decode(relay, _dims(relay, B=1024)) == relay.ERR_UNSUPPORTED
     assert _call_decode(relay, d, q=None) == relay.ERR_INVALID_ARG
     assert _call_decode(relay, d, out=None) == relay.ERR_INVALID_ARG
