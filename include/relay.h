@@ -56,8 +56,11 @@
  *    t < max(0, ctx_lens[b] - q_lens[b] + 1 + i).  Rows i >= q_lens[b] of
  *    the outputs are left untouched.
  *  - A row with no visible key at all gets out = 0 and lse = -inf.
- *  - Supported: D in {64, 128}; block size 16; B <= 512; MHA (H query
- *    heads = H KV heads).  Others return RELAY_ERR_UNSUPPORTED.
+ *  - Supported: D in {64, 128}; block size 16; B <= 512; any Hkv that
+ *    divides H (Hkv = 0 means Hkv = H); B*Lq, B*H, B*Lq*H and
+ *    16*max_blocks_per_seq + Ls each below 2^30 (32-bit counters on the
+ *    device).  Other shapes return RELAY_ERR_UNSUPPORTED; an Hkv that does
+ *    not divide H returns RELAY_ERR_INVALID_ARG.
  *  - Errors: argument problems are found on the host before anything is
  *    queued and returned synchronously.  Launch failures return
  *    RELAY_ERR_CUDA.  Values that can only be checked on the device (a
@@ -159,16 +162,22 @@ relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const fl
                           const float *o_ctx, const float *lse_ctx, const int32_t *q_lens,
                           void *out, float *lse_out, relay_stream_t stream);
 
-/* All three steps, queued as two kernels on `stream` (the second launched
- * as a programmatic dependent of the first, so both fit in one CUDA graph):
+/* All three steps, queued on `stream` as two kernels, or three when the
+ * system step runs on the tensor cores (all of them fit in one CUDA graph):
+ *  0. (D = 128 and more than 256 query rows per KV head, counting the query
+ *     heads of a group: the system step is compute-bound) a tcgen05 kernel
+ *     computes the system partials: one CTA per KV head, pair of 128-row
+ *     tiles and range of system keys;
  *  1. a persistent grid (one CTA per SM) works through system items (one
- *     head, a range of system keys, up to 128 query rows of the batch: the
- *     system KV is streamed once per batch) and context items (one request,
- *     one head, a range of its paged context); each item writes an fp32
- *     partial result and its log-sum-exp to the workspace;
- *  2. a merge kernel combines each (row, head)'s partials -- the system
- *     ranges and the context splits -- into `out` (fp16) and `lse_out` (fp32
- *     natural log, nullable): the relay fusion, over any number of parts. */
+ *     KV head, a range of system keys, up to 64 query rows of the batch: the
+ *     system KV is streamed once per batch) -- unless step 0 ran -- and
+ *     context items (one request, one head or head group, a range of its
+ *     paged context); each item writes an fp32 partial result and its
+ *     log-sum-exp to the workspace;
+ *  2. a merge kernel, launched as a programmatic dependent of step 1,
+ *     combines each (row, head)'s partials -- the system ranges and the
+ *     context splits -- into `out` (fp16) and `lse_out` (fp32 natural log,
+ *     nullable): the relay fusion, over any number of parts. */
 relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
                                       const void *sys_k, const void *sys_v,
                                       const void *k_cache, const void *v_cache,
@@ -282,14 +291,22 @@ relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q,
  *    call's contents: calls that may overlap on the GPU (other streams, other
  *    host threads) race and must be serialised by the caller.
  *  - Device-side check flags land in the shared buffer and are cleared by the
- *    next call; callers that need relay_device_status use
- *    relay_attention_decode with their own workspace. */
+ *    next call: read them with relay_noalloc_device_status before that. */
 relay_status_t relay_attention_decode_noalloc(const relay_dims_t *dims, const void *q,
                                               const void *sys_k, const void *sys_v,
                                               const void *k_cache, const void *v_cache,
                                               const int32_t *block_tables, const int32_t *ctx_lens,
                                               const int32_t *q_lens, void *out, float *lse_out,
                                               relay_stream_t stream);
+
+/* Read and clear the device-side check flags that the last
+ * relay_attention_decode_noalloc call on the current device raised (a block
+ * id outside the pool, a q_lens or ctx_lens entry out of range, ...: the
+ * kernels skip those accesses, and without this call the caller could not
+ * tell).  SYNCHRONOUS: waits for `stream`, which must be ordered after that
+ * call.  *flags_out (host pointer, nullable) receives the RELAY_FLAG_* mask.
+ * Returns RELAY_ERR_DEVICE_CHECK if any flag was set.  Allocates nothing. */
+relay_status_t relay_noalloc_device_status(uint32_t *flags_out, relay_stream_t stream);
 
 /* Read and clear the device-side check flags of a workspace.  SYNCHRONOUS:
  * waits for `stream`.  *flags_out (host pointer, nullable) receives the

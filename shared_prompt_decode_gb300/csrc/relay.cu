@@ -655,38 +655,52 @@ relay_status_t relay_rope(const relay_dims_t *dims, void *q, void *k_new, const 
 // part of the module image, never allocated or freed at run time.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RELAY_NOALLOC_SCRATCH_BYTES];
 
+}  // extern "C"
+
+namespace {
+
+// Device address of the scratch buffer on the current device.  The symbol's
+// name is only a host-side stand-in: its device address is looked up once
+// per device, with that device current, and cached.
+relay_status_t noalloc_scratch(void **ws)
+{
+    static void *scratch[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return RELAY_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!scratch[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return RELAY_ERR_CUDA;
+        }
+        scratch[dev] = ptr;
+    }
+    *ws = scratch[dev];
+    return RELAY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 relay_status_t relay_attention_decode_noalloc(const relay_dims_t *dims, const void *q, const void *sys_k,
                                               const void *sys_v, const void *k_cache, const void *v_cache,
                                               const int32_t *block_tables, const int32_t *ctx_lens,
                                               const int32_t *q_lens, void *out, float *lse_out,
                                               relay_stream_t stream)
 {
-    static void *scratch[kMaxDevices] = {};
     relay_status_t st = check_dims(dims);
     if (st != RELAY_OK) return st;
     const size_t need = relay_workspace_size(dims);
     if (need == 0 || need > RELAY_NOALLOC_SCRATCH_BYTES) return RELAY_ERR_WORKSPACE;
     if (dims->B == 0) return RELAY_OK;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return RELAY_ERR_CUDA;
-    }
     void *ws = nullptr;
-    {
-        // The symbol's name is only a host-side stand-in: its device address
-        // is looked up once per device, with that device current.
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!scratch[dev]) {
-            void *ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-                cudaGetLastError();
-                return RELAY_ERR_CUDA;
-            }
-            scratch[dev] = ptr;
-        }
-        ws = scratch[dev];
-    }
+    st = noalloc_scratch(&ws);
+    if (st != RELAY_OK) return st;
     // the queue counters must start at zero; the rest is overwritten
     if (cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
@@ -708,6 +722,14 @@ relay_status_t relay_device_status(void *ws, uint32_t *flags_out, relay_stream_t
     }
     if (flags_out) *flags_out = flags;
     return flags ? RELAY_ERR_DEVICE_CHECK : RELAY_OK;
+}
+
+relay_status_t relay_noalloc_device_status(uint32_t *flags_out, relay_stream_t stream)
+{
+    void *ws = nullptr;
+    relay_status_t st = noalloc_scratch(&ws);
+    if (st != RELAY_OK) return st;
+    return relay_device_status(ws, flags_out, stream);
 }
 
 const char *relay_status_string(relay_status_t status)
