@@ -32,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librelay.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
-FLAG_BAD_Q_LEN, FLAG_BAD_CTX_LEN, FLAG_BAD_BLOCK, FLAG_Q_TOTAL = 1, 2, 4, 8
+FLAG_BAD_Q_LEN, FLAG_BAD_CTX_LEN, FLAG_BAD_BLOCK, FLAG_Q_TOTAL, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class RelayError(RuntimeError):

@@ -24,15 +24,18 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build librelay")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, variant: str = "", defines=()) -> str:
+    """Build librelay.so.  A named variant (tests only) is the same sources
+    with extra -D definitions, built to librelay_<variant>.so."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
+    lib = LIB if not variant else os.path.join(OUT_DIR, f"librelay_{variant}.so")
+    if not force and os.path.exists(lib):
+        t = os.path.getmtime(lib)
         if all(os.path.getmtime(f) <= t for f in DEPS):
-            return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+            return lib
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", INCLUDE, "-o", tmp] + SOURCES
+           "-I", INCLUDE, "-o", tmp] + [f"-D{d}" for d in defines] + SOURCES
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -40,8 +43,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
     if verbose:
         print(r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -55,7 +55,15 @@ constexpr int kKeysTC = 64;           // keys per K/V stage
 constexpr int kStagesK = 3, kStagesV = 2;   // V stage j % 2 is freed by the O-done barrier of PV(j)
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
-constexpr unsigned long long kWaitNs = 1000000000ull;   // give up on a wait after 1 s
+// A protocol wait gives up after RELAY_WAIT_LIMIT_NS (1 s).  A test build
+// sets it to 0, so that the first wait not met at once gives up and the
+// abort path below runs; draining copies and MMAs in flight before TMEM is
+// freed is always bounded by 1 s, whatever the protocol limit.
+#ifndef RELAY_WAIT_LIMIT_NS
+#define RELAY_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr unsigned long long kWaitNs = RELAY_WAIT_LIMIT_NS;
+constexpr unsigned long long kDrainNs = 1000000000ull;
 
 // shared-memory map (byte offsets from a 1024-aligned base), D = 128
 constexpr int kHalfQ = kRowsTC * 128;             // one d-half of a Q tile: [128 rows][64 d] fp16 = 16 KB
@@ -133,7 +141,7 @@ __device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity, volatil
 __device__ __forceinline__ void mbar_drain(unsigned bar, unsigned parity)
 {
     const unsigned long long t0 = global_ns();
-    while (!mbar_try(bar, parity) && global_ns() - t0 < kWaitNs) {
+    while (!mbar_try(bar, parity) && global_ns() - t0 < kDrainNs) {
     }
 }
 
