@@ -73,7 +73,7 @@ enum : unsigned {
 };
 
 // ctrl words in the workspace
-enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DONE = 2, CTRL_DEC_ITEMS = 3 };
+enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DEC_ITEMS = 3 };
 
 struct Params {
     int B, Lq, H, Ls, num_blocks, max_blocks, max_q_total;
@@ -120,7 +120,6 @@ struct Smem {
     int cls_cnt[33];
     int n_dec_req;
     int tps;                  // pages per decode item chosen for this launch
-    int warp_tot[kWarps];
     int item[kTeams];
     int bad;
 
@@ -278,37 +277,21 @@ __device__ __forceinline__ ReqInfo req_info(const Params &p, int n_ctx, int ql, 
     return r;
 }
 
-// Exclusive prefix sum over the batch of per-request values v[k] (request
-// tid*PER + k), written to out[0..n] (out[n] = total).
-template <int D, int PER>
-__device__ __forceinline__ void block_scan(const int (&v)[PER], int *out, int n, Smem<D> &s)
+// Inclusive prefix sum over the 32 lanes of a warp.
+__device__ __forceinline__ int warp_incl_scan(int v)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int loc = 0;
-#pragma unroll
-    for (int k = 0; k < PER; k++) loc += v[k];
-    int inc = loc;
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        int t = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += t;
+        const int t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
     }
-    if (lane == 31) s.warp_tot[warp] = inc;
-    __syncthreads();
-    int base = inc - loc;
-    for (int j = 0; j < warp; j++) base += s.warp_tot[j];
-#pragma unroll
-    for (int k = 0; k < PER; k++) {
-        int b = tid * PER + k;
-        if (b < n) out[b] = base;
-        base += v[k];
-    }
-    if (tid == kThreads - 1) out[n] = base;
-    __syncthreads();
+    return v;
 }
 
-// Per-CTA schedule over the batch (B <= kMaxB, PER requests per thread):
-// row prefix qo, multi-row item prefix mq, and the decode queue.
+// Per-CTA schedule over the batch (B <= kMaxB): row prefix qo, multi-row
+// item prefix mq, and the decode queue.  Built by warp 0 alone, 32 requests
+// per round, with warp shuffles (no block-wide barrier until the end):
 //   * Pages per decode item: between tps_min and tps_max, chosen so that the
 //     decode queue holds about kItemsPerWarp items per warp of the grid (fine
 //     enough for the dynamic queue to balance, coarse enough to keep the
@@ -320,82 +303,79 @@ __device__ __forceinline__ void block_scan(const int (&v)[PER], int *out, int n,
 template <int D>
 __device__ void build_schedule(const Params &p, Smem<D> &s)
 {
-    constexpr int PER = (kMaxB + kThreads - 1) / kThreads;
     constexpr int kClasses = 33;                  // item sizes 0..32 pages
     constexpr int kItemsPerWarp = 4;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int vq[PER], vm[PER], vp[PER], nn[PER];
-    unsigned flags = 0;
-    if (tid < kClasses) s.cls_cnt[tid] = 0;
-    if (tid == 0) s.bad = 0;
-    const int pp = (p.n_prefix + kBlock - 1) / kBlock;
-#pragma unroll
-    for (int k = 0; k < PER; k++) {
-        const int b = tid * PER + k;
-        int ql = 0, n = 0, m = 0, pg = 0;
-        if (b < p.B) {
-            ql = p.q_lens ? p.q_lens[b] : p.Lq;
-            n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
-            if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
-            if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
-            if (has_ctx(p.mode) && ql > 1) {
-                const ReqInfo r = req_info(p, n, ql, p.tps_max);
-                m = p.H * r.ns * r.mt;
+    const int lane = threadIdx.x & 31;
+    if ((threadIdx.x >> 5) == 0) {
+        const int pp = (p.n_prefix + kBlock - 1) / kBlock;
+        unsigned flags = 0;
+        int run_q = 0, run_m = 0, pages = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            int ql = 0, n = 0, m = 0, pg = 0;
+            if (b < p.B) {
+                ql = p.q_lens ? p.q_lens[b] : p.Lq;
+                n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
+                if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
+                if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
+                if (has_ctx(p.mode) && ql > 1) {
+                    const ReqInfo r = req_info(p, n, ql, p.tps_max);
+                    m = p.H * r.ns * r.mt;
+                }
+                if (has_ctx(p.mode) && ql == 1) pg = p.HQ * (pp + (n + kBlock - 1) / kBlock);
+                s.nctx[b] = n;
+                s.dcls[b] = (signed char)(has_ctx(p.mode) && ql == 1 ? 0 : -1);   // decode request (class below)
             }
-            if (has_ctx(p.mode) && ql == 1) pg = p.HQ * (pp + (n + kBlock - 1) / kBlock);
+            const int iq = warp_incl_scan(ql), im = warp_incl_scan(m);
+            if (b < p.B) {
+                s.qo[b] = run_q + iq - ql;
+                s.mq[b] = run_m + im - m;
+            }
+            run_q += __shfl_sync(0xffffffffu, iq, 31);
+            run_m += __shfl_sync(0xffffffffu, im, 31);
+            pages += __reduce_add_sync(0xffffffffu, pg);
         }
-        vq[k] = ql;
-        vm[k] = m;
-        vp[k] = pg;
-        nn[k] = n;
-    }
-    __syncthreads();
-    if (flags) atomicOr(&s.bad, (int)flags);
-    block_scan<D, PER>(vq, s.qo, p.B, s);
-    block_scan<D, PER>(vm, s.mq, p.B, s);
-    block_scan<D, PER>(vp, s.dec, p.B, s);        // s.dec[B]: decode pages over all heads
-    if (tid == 0) {
+        flags = __reduce_or_sync(0xffffffffu, flags);
+        if (run_q > p.max_q_total) flags |= FLAG_Q_TOTAL;
         const long long want = (long long)gridDim.x * kWarps * kItemsPerWarp;
-        int t = (int)((s.dec[p.B] + want - 1) / want);
-        s.tps = max(p.tps_min, min(p.tps_max, t));
-    }
-    __syncthreads();
-    const int tps = s.tps;
-    // decode class of every request: its largest item in pages (-1: not decode)
-#pragma unroll
-    for (int k = 0; k < PER; k++) {
-        const int b = tid * PER + k;
-        if (b < p.B) {
-            s.nctx[b] = nn[k];
+        const int tps = max(p.tps_min, min(p.tps_max, (int)((pages + want - 1) / want)));
+        if (lane == 0) {
+            s.qo[p.B] = run_q;
+            s.mq[p.B] = run_m;
+            s.tps = tps;
+            s.bad = (int)flags;
+        }
+        // decode class of every request (its largest item in pages), counted per class
+        s.cls_cnt[lane] = 0;
+        if (lane == 0) s.cls_cnt[32] = 0;
+        __syncwarp();
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
             int c = -1;
-            if (has_ctx(p.mode) && vq[k] == 1) {
-                const ReqInfo r = req_info(p, nn[k], 1, tps);
+            if (b < p.B && s.dcls[b] == 0) {
+                const ReqInfo r = req_info(p, s.nctx[b], 1, tps);
                 c = (r.pages + r.ns - 1) / r.ns;
-                atomicAdd(&s.cls_cnt[c], 1);
+                s.dcls[b] = (signed char)c;
             }
-            s.dcls[b] = (signed char)c;
+            const unsigned same = __match_any_sync(0xffffffffu, c);
+            if (c >= 0 && lane == __ffs(same) - 1) s.cls_cnt[c] += __popc(same);
+            __syncwarp();
         }
-    }
-    __syncthreads();
-    // counting sort of decode requests: class descending, request index ascending
-    if (warp == 0) {
-        // start position of classes 32..1 (lanes 0..31), then class 0
-        const int v = kClasses - 1 - lane;
-        const int cnt = s.cls_cnt[v];
-        int inc = cnt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int t = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off) inc += t;
+        // counting sort of decode requests: class descending, request index ascending.
+        // Start position of classes 32..1 (lanes 0..31), then class 0.
+        {
+            const int v = kClasses - 1 - lane;
+            const int cnt = s.cls_cnt[v];
+            const int inc = warp_incl_scan(cnt);
+            const int c0 = s.cls_cnt[0];
+            __syncwarp();
+            s.cls_cnt[v] = inc - cnt;
+            if (lane == 31) {
+                s.cls_cnt[0] = inc;
+                s.n_dec_req = inc + c0;
+            }
+            __syncwarp();
         }
-        const int c0 = s.cls_cnt[0];
-        __syncwarp();
-        s.cls_cnt[v] = inc - cnt;
-        if (lane == 31) {
-            s.cls_cnt[0] = inc;
-            s.n_dec_req = inc + c0;
-        }
-        __syncwarp();
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int b = b0 + lane;
             const int c = b < p.B ? s.dcls[b] : -1;
@@ -406,18 +386,18 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
             if (c >= 0 && lane == __ffs(same) - 1) s.cls_cnt[c] = base + __popc(same);
             __syncwarp();
         }
+        // decode items per sorted position: exclusive prefix into s.dec
+        const int n_dec_req = s.n_dec_req;
+        int run_d = 0;
+        for (int q0 = 0; q0 < n_dec_req; q0 += 32) {
+            const int pos = q0 + lane;
+            const int dv = pos < n_dec_req ? p.HQ * req_info(p, s.nctx[s.order[pos]], 1, tps).ns : 0;
+            const int id = warp_incl_scan(dv);
+            if (pos < n_dec_req) s.dec[pos] = run_d + id - dv;
+            run_d += __shfl_sync(0xffffffffu, id, 31);
+        }
+        if (lane == 0) s.dec[n_dec_req] = run_d;
     }
-    __syncthreads();
-    // decode items per sorted position
-    int dv[PER];
-#pragma unroll
-    for (int k = 0; k < PER; k++) {
-        const int pos = tid * PER + k;
-        dv[k] = 0;
-        if (pos < s.n_dec_req) dv[k] = p.HQ * req_info(p, s.nctx[s.order[pos]], 1, tps).ns;
-    }
-    block_scan<D, PER>(dv, s.dec, s.n_dec_req, s);
-    if (tid == 0 && s.qo[p.B] > p.max_q_total) s.bad |= FLAG_Q_TOTAL;
     __syncthreads();
 }
 
@@ -878,7 +858,6 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.Hkv, hk, 0};
     const int key0 = rho * p.sys_range;
     const int key_hi = min(key0 + p.sys_range, p.Ls);
-    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
     const RowRoles rr = row_roles(min(kTileM, Mv - tau * kTileM));
     const int vW = tau * kTileM + rr.rg * 16;
@@ -895,7 +874,8 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
         qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + hB) * D;
     }
     unsigned qf[D / 16][4];
-    load_q_rows<D>(qf, qa, qb);
+    load_q_rows<D>(qf, qa, qb);     // the query rows are requested before the item's tiles
+    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
     RowState<D> ws;
 #pragma unroll
     for (int d = 0; d < D / 8; d++)
@@ -933,7 +913,6 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     const int key0 = split * ri.split;
     const int last_row = min(ql, (mtile + 1) * kTileM) - 1;
     const int key_hi = min(key0 + ri.split, vis(last_row));
-    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
 
     const RowRoles rr = row_roles(min(kTileM, ql - mtile * kTileM));
     const int iW = mtile * kTileM + rr.rg * 16;
@@ -941,7 +920,8 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     const __half *qa = iA < ql ? p.q + (((size_t)b * p.Lq + iA) * p.H + h) * D : nullptr;
     const __half *qb = iB < ql ? p.q + (((size_t)b * p.Lq + iB) * p.H + h) * D : nullptr;
     unsigned qf[D / 16][4];
-    load_q_rows<D>(qf, qa, qb);
+    load_q_rows<D>(qf, qa, qb);     // the query rows are requested before the item's tiles
+    row_prologue<D>(s, src, key0, key_hi, p.ctrl);
     const int endA = iA < ql ? min(key0 + ri.split, vis(iA)) : 0;
     const int endB = iB < ql ? min(key0 + ri.split, vis(iB)) : 0;
     RowState<D> ws;
@@ -1260,26 +1240,33 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // The first two tickets of every warp are static (no warp starts by
-    // queueing on the counter with all the others); later ones come from the
-    // queue, requested one item ahead.
+    // The first three tickets of every warp are static; later ones come from
+    // the queue, requested one item ahead.  So no warp touches the queue
+    // counter before its first item is done (1216 warps incrementing one
+    // address at the same instant hold up the requests behind them).
     const unsigned n_w = gridDim.x * kWarps;
-    unsigned ticket = blockIdx.x * kWarps + warp;
+    const unsigned wid = blockIdx.x * kWarps + warp;
+    unsigned ticket = wid;
     int taken = 0;
+    constexpr int kStatic = 3;
     auto request = [&]() {      // ask for a ticket; its value is read later
-        if (lane == 0) ticket = 2 * n_w + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
+        if (lane == 0) ticket = kStatic * n_w + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
     };
     auto take = [&](DecItem<D> &it) {
         int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
         dec_item<D, GRP>(p, s, id, n_dec, it);
-        if (++taken == 1) ticket = n_w + blockIdx.x * kWarps + warp;
+        ++taken;
+        if (taken < kStatic) ticket = taken * n_w + wid;
         else if (it.id >= 0) request();
     };
 
+    // the first item's first pages are requested before the second item is
+    // decoded
     DecItem<D> cur, nxt;
+    nxt.id = -1;
+    nxt.np = 0;
     take(cur);
     if (cur.id < 0) return;
-    take(nxt);
     bool load_on_nxt = false;     // the loader has moved on to `nxt`
     int load_pg = 0;              // next page (relative) of the item being loaded
     int issued = 0, computed = 0;
@@ -1308,6 +1295,8 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
         }
     };
 
+    fill();
+    take(nxt);
     fill();
     for (;;) {
         DecState<D> st;        // multi-head
@@ -1401,18 +1390,6 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     __syncthreads();
     // this CTA's partials are written: the merge kernel may be launched
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-
-    // the last CTA out resets the queues for the next launch
-    if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned done = atomicAdd(&p.ctrl[CTRL_DONE], 1u);
-        if (done == gridDim.x - 1) {
-            p.ctrl[CTRL_ROW_ITEMS] = 0u;
-            p.ctrl[CTRL_DEC_ITEMS] = 0u;
-            p.ctrl[CTRL_DONE] = 0u;
-            __threadfence();
-        }
-    }
 }
 
 // ============================================================================= merge kernel
@@ -1425,6 +1402,12 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     __shared__ int qo[kMaxB + 1];
     __shared__ int nctx[kMaxB];
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // the streaming grid has finished: its queue counters go back to zero
+    // for the next call (stream order puts that call's kernels after this one)
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        p.ctrl[CTRL_ROW_ITEMS] = 0u;
+        p.ctrl[CTRL_DEC_ITEMS] = 0u;
+    }
     if (p.q_lens == nullptr) {
         // every request has Lq rows: row r is row r % Lq of request r / Lq, so
         // no schedule table is needed; the request's context length, the
