@@ -23,7 +23,7 @@ using namespace relay;
 
 constexpr int kMaxDevices = 64;
 constexpr int kAutoCtxSplit = 512;
-constexpr int kGridTarget = 152;       // resident CTAs on a GB300 (one per SM)
+constexpr int kMaxMqParts = 8;         // context splits of a multi-row request, at most
 
 struct DevInfo {
     bool ready = false;
@@ -145,17 +145,19 @@ bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
 
 struct Plan {
     int Mtot = 0;
-    int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit, C_max = 0;
-    int n_parts = 0, ctx_base = 0, n_prefix = 0;
+    int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit;
+    int c_dec = 0, c_mq = 0, mq_split_min = 0, n_prefix = 0;
     int tps_min = 32, tps_max = 32;
     bool tc = false;          // system step on the tensor-core kernel
+    size_t dec_base = 0, mq_base = 0, rows = 0;   // partial rows: [system | decode | multi-row] sections
     size_t off_sched = 0, off_part_o = 0, off_part_lse = 0, total = 0;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// Work-item sizes and workspace layout for one mode.
-Plan make_plan(const relay_dims_t *d, int mode)
+// Work-item sizes and workspace layout for one mode, for a GPU of `sms` SMs
+// (one streaming CTA per SM; the number of system key ranges depends on it).
+Plan make_plan(const relay_dims_t *d, int mode, int sms)
 {
     Plan pl;
     pl.Mtot = d->max_q_total > 0 ? d->max_q_total : d->B * d->Lq;
@@ -176,11 +178,11 @@ Plan make_plan(const relay_dims_t *d, int mode)
         double best = 1e30;
         int r_best = 1;
         for (int r = 1; r <= r_cap; r++) {
-            const double cost = (double)((n * r + kGridTarget - 1) / kGridTarget) / r;
+            const double cost = (double)((n * r + sms - 1) / sms) / r;
             if (cost < best) best = cost;
         }
         for (int r = 1; r <= r_cap; r++) {
-            if ((double)((n * r + kGridTarget - 1) / kGridTarget) / r <= best * 1.02) {
+            if ((double)((n * r + sms - 1) / sms) / r <= best * 1.02) {
                 r_best = r;
                 break;
             }
@@ -197,7 +199,7 @@ Plan make_plan(const relay_dims_t *d, int mode)
                 // the system keys it streams.
                 const int tiles = (int)((Mv + kTileM - 1) / kTileM);
                 const int hkv = kv_heads(d);
-                int r_want = (kGridTarget + hkv * tiles - 1) / (hkv * tiles);
+                int r_want = (sms + hkv * tiles - 1) / (hkv * tiles);
                 // cap on the ranges from the query rows per head (not the
                 // virtual rows of a head group), so the items stay short
                 int r_cap = d->Ls / std::max(256, 16 * pl.Mtot);
@@ -215,28 +217,34 @@ Plan make_plan(const relay_dims_t *d, int mode)
     if (ctx) {
         // Context splits per request.  A decode request's pages (prefix
         // pages + context pages) go to items of tps pages, tps chosen on the
-        // device in [tps_min, tps_max] (fixed when ctx_split is given); a
-        // multi-row request uses splits of at least ctx_split keys.  tps_min
-        // keeps every request at <= kMaxCtxParts partials, which bounds the
-        // workspace.
+        // device in [tps_min, tps_max] (fixed when ctx_split is given);
+        // tps_min keeps a request at <= kMaxCtxParts partials.  A multi-row
+        // request uses splits of at least ctx_split keys, and at least
+        // mq_split_min, so that it has at most kMaxMqParts of them.
         constexpr int kMaxCtxParts = 32;
         pl.ctx_split = d->ctx_split > 0 ? d->ctx_split : kAutoCtxSplit;
         const int max_pages = (pl.n_prefix + kBlock - 1) / kBlock + d->max_blocks_per_seq;
         pl.tps_max = std::min(pl.ctx_split / kBlock, 32);    // a decode item holds <= 32 pages
         pl.tps_min = d->ctx_split > 0 ? pl.tps_max
                                       : std::min(pl.tps_max, std::max(2, (max_pages + kMaxCtxParts - 1) / kMaxCtxParts));
-        const int c_dec = (max_pages + pl.tps_min - 1) / pl.tps_min;
-        const int c_mq = (pl.n_prefix + d->max_blocks_per_seq * kBlock + pl.ctx_split - 1) / pl.ctx_split;
-        pl.C_max = std::max(1, std::max(c_dec, c_mq));
+        pl.c_dec = std::max(1, (max_pages + pl.tps_min - 1) / pl.tps_min);
+        const long long max_keys = (long long)pl.n_prefix + (long long)d->max_blocks_per_seq * kBlock;
+        pl.mq_split_min = (int)((max_keys + kMaxMqParts - 1) / kMaxMqParts);
+        pl.mq_split_min = round_up(std::max(pl.mq_split_min, 1), pl.ctx_split);
+        // multi-row requests exist only when a request may carry several rows
+        pl.c_mq = d->Lq > 1 ? std::max(1, (int)((max_keys + pl.mq_split_min - 1) / pl.mq_split_min)) : 0;
     }
-    pl.ctx_base = sys ? pl.R_sys : 0;
-    pl.n_parts = (sys ? pl.R_sys : 0) + (ctx ? pl.C_max : 0);
+    const size_t sys_rows = (size_t)(sys ? pl.R_sys : 0) * pl.Mtot * d->H;
+    const size_t dec_rows = (size_t)(ctx ? pl.c_dec : 0) * d->B * d->H;
+    const size_t mq_rows = (size_t)(ctx ? pl.c_mq : 0) * pl.Mtot * d->H;
+    pl.dec_base = sys_rows;
+    pl.mq_base = sys_rows + dec_rows;
+    pl.rows = sys_rows + dec_rows + mq_rows;
     pl.off_sched = 256;
     size_t sched_bytes = ((size_t)(2 * d->B + 2) * sizeof(int) + 255) / 256 * 256;
     pl.off_part_o = pl.off_sched + sched_bytes;
-    size_t rows = (size_t)pl.n_parts * pl.Mtot * d->H;
-    pl.off_part_lse = pl.off_part_o + (rows * d->D * sizeof(float) + 255) / 256 * 256;
-    pl.total = pl.off_part_lse + (rows * sizeof(float) + 255) / 256 * 256;
+    pl.off_part_lse = pl.off_part_o + (pl.rows * d->D * sizeof(float) + 255) / 256 * 256;
+    pl.total = pl.off_part_lse + (pl.rows * sizeof(float) + 255) / 256 * 256;
     return pl;
 }
 
@@ -253,15 +261,17 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
 {
     if (!ws) return RELAY_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return RELAY_ERR_INVALID_ARG;
-    Plan pl = make_plan(d, mode);
-    if (ws_bytes < pl.total) return RELAY_ERR_WORKSPACE;
-    // without q_lens every request has Lq rows: the partial slots are laid out
-    // for max_q_total rows, so a smaller bound is an argument error (with
-    // q_lens the kernel checks their sum on the device)
-    if (!p.q_lens && (long long)d->B * d->Lq > pl.Mtot) return RELAY_ERR_INVALID_ARG;
+    // host checks first: a workspace too small for any device, and (without
+    // q_lens every request has Lq rows, and the partial slots are laid out
+    // for max_q_total rows) a bound below B * Lq; with q_lens the kernel
+    // checks their sum on the device
+    if (ws_bytes < make_plan(d, mode, 1).total) return RELAY_ERR_WORKSPACE;
+    if (!p.q_lens && (long long)d->B * d->Lq > make_plan(d, mode, 1).Mtot) return RELAY_ERR_INVALID_ARG;
     const DevInfo *dev = nullptr;
     relay_status_t st = device_info(&dev);
     if (st != RELAY_OK) return st;
+    Plan pl = make_plan(d, mode, dev->sms);
+    if (ws_bytes < pl.total) return RELAY_ERR_WORKSPACE;
 
     unsigned char *base = static_cast<unsigned char *>(ws);
     p.B = d->B;
@@ -284,10 +294,13 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.R_sys = pl.R_sys;
     p.sys_range = pl.sys_range;
     p.ctx_split = pl.ctx_split;
-    p.ctx_base = pl.ctx_base;
     p.tps_min = pl.tps_min;
     p.tps_max = pl.tps_max;
-    p.c_max = pl.C_max;
+    p.c_dec = pl.c_dec;
+    p.c_mq = pl.c_mq;
+    p.mq_split_min = pl.mq_split_min;
+    p.dec_base = (long long)pl.dec_base;
+    p.mq_base = (long long)pl.mq_base;
     p.skip_sys = pl.tc ? 1 : 0;
     p.mode = mode;
 
@@ -362,8 +375,13 @@ extern "C" {
 size_t relay_workspace_size(const relay_dims_t *dims)
 {
     if (check_dims(dims) != RELAY_OK) return 0;
+    // for the current device (its SM count sets the number of system key
+    // ranges); without a usable device, for as many ranges as any device
+    // would use (an unbounded SM count)
+    const DevInfo *dev = nullptr;
+    const int sms = device_info(&dev) == RELAY_OK ? dev->sms : INT_MAX / 4;
     size_t m = 0;
-    for (int mode : {MODE_FUSED, MODE_SYS, MODE_CTX, MODE_BASELINE}) m = std::max(m, make_plan(dims, mode).total);
+    for (int mode : {MODE_FUSED, MODE_SYS, MODE_CTX, MODE_BASELINE}) m = std::max(m, make_plan(dims, mode, sms).total);
     return m;
 }
 

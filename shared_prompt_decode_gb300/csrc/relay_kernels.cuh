@@ -90,11 +90,13 @@ struct Params {
     float *o_f32, *lse_f32;           // sys-only / ctx-only outputs
     unsigned *ctrl;                   // see CTRL_*
     int *sched;                       // schedule handed to the merge kernel: [tps, qo[0..B], nctx[0..B-1]]
-    float *part_o;                    // [n_parts][max_q_total][H][D]
-    float *part_lse;                  // [n_parts][max_q_total][H]  (log2 domain)
-    int R_sys, sys_range, ctx_split, ctx_base;   // ctx_base: first partial slot of context parts
+    float *part_o;                    // partial rows, D floats each (layout: see sys_slot)
+    float *part_lse;                  // their log-sum-exps (log2 domain)
+    int R_sys, sys_range, ctx_split;
     int tps_min, tps_max;             // pages per decode item: bounds of the adaptive choice
-    int c_max;                        // context partial slots per row (workspace layout)
+    int c_dec, c_mq;                  // context partial slots of a decode request / of a multi-row row
+    int mq_split_min;                 // keys per split of a multi-row request: at least this
+    long long dec_base, mq_base;      // first partial row of the decode and multi-row sections
     int skip_sys;                     // system partials come from the tensor-core kernel
     int mode;
 };
@@ -120,6 +122,7 @@ struct Smem {
     int cls_cnt[33];
     int n_dec_req;
     int tps;                  // pages per decode item chosen for this launch
+    int warp_tot[kWarps];
     int item[kTeams];
     int bad;
 
@@ -268,7 +271,7 @@ __device__ __forceinline__ ReqInfo req_info(const Params &p, int n_ctx, int ql, 
         // longer splits for multi-row requests keep the partial traffic small
         // next to the keys each item streams
         int want = ql * 64;
-        r.split = ((want + p.ctx_split - 1) / p.ctx_split) * p.ctx_split;
+        r.split = max(((want + p.ctx_split - 1) / p.ctx_split) * p.ctx_split, p.mq_split_min);
         int nkeys = p.n_prefix + r.n_ctx;
         r.ns = (nkeys + r.split - 1) / r.split;
         r.mt = (ql + kTileM - 1) / kTileM;
@@ -289,9 +292,149 @@ __device__ __forceinline__ int warp_incl_scan(int v)
     return v;
 }
 
+// Exclusive prefix sum over the batch of per-request values v[k] (request
+// tid*PER + k), written to out[0..n] (out[n] = total).
+template <int D, int PER>
+__device__ __forceinline__ void block_scan(const int (&v)[PER], int *out, int n, Smem<D> &s)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int loc = 0;
+#pragma unroll
+    for (int k = 0; k < PER; k++) loc += v[k];
+    int inc = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += t;
+    }
+    if (lane == 31) s.warp_tot[warp] = inc;
+    __syncthreads();
+    int base = inc - loc;
+    for (int j = 0; j < warp; j++) base += s.warp_tot[j];
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int b = tid * PER + k;
+        if (b < n) out[b] = base;
+        base += v[k];
+    }
+    if (tid == kThreads - 1) out[n] = base;
+    __syncthreads();
+}
+
+// The schedule of build_schedule (below) built by the whole CTA, PER
+// requests per thread with block scans: for batches of more than 32
+// requests, where one warp would need several dependent rounds.  Kept out of
+// line: the kernel starts with its code cold (nothing of it in L2 after the
+// other kernels of a model step), and this path inlined beside the one-warp
+// build cost the 32-request step 2.5 us (measured).
+template <int D>
+__device__ __noinline__ void build_schedule_cta(const Params &p, Smem<D> &s)
+{
+    constexpr int PER = (kMaxB + kThreads - 1) / kThreads;
+    constexpr int kClasses = 33;                  // item sizes 0..32 pages
+    constexpr int kItemsPerWarp = 4;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int vq[PER], vm[PER], vp[PER], nn[PER];
+    unsigned flags = 0;
+    if (tid < kClasses) s.cls_cnt[tid] = 0;
+    if (tid == 0) s.bad = 0;
+    const int pp = (p.n_prefix + kBlock - 1) / kBlock;
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        const int b = tid * PER + k;
+        int ql = 0, n = 0, m = 0, pg = 0;
+        if (b < p.B) {
+            ql = p.q_lens ? p.q_lens[b] : p.Lq;
+            n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
+            if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
+            if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
+            if (has_ctx(p.mode) && ql > 1) {
+                const ReqInfo r = req_info(p, n, ql, p.tps_max);
+                m = p.H * r.ns * r.mt;
+            }
+            if (has_ctx(p.mode) && ql == 1) pg = p.HQ * (pp + (n + kBlock - 1) / kBlock);
+        }
+        vq[k] = ql;
+        vm[k] = m;
+        vp[k] = pg;
+        nn[k] = n;
+    }
+    __syncthreads();
+    if (flags) atomicOr(&s.bad, (int)flags);
+    block_scan<D, PER>(vq, s.qo, p.B, s);
+    block_scan<D, PER>(vm, s.mq, p.B, s);
+    block_scan<D, PER>(vp, s.dec, p.B, s);        // s.dec[B]: decode pages over all heads
+    if (tid == 0) {
+        const long long want = (long long)gridDim.x * kWarps * kItemsPerWarp;
+        int t = (int)((s.dec[p.B] + want - 1) / want);
+        s.tps = max(p.tps_min, min(p.tps_max, t));
+    }
+    __syncthreads();
+    const int tps = s.tps;
+    // decode class of every request: its largest item in pages (-1: not decode)
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        const int b = tid * PER + k;
+        if (b < p.B) {
+            s.nctx[b] = nn[k];
+            int c = -1;
+            if (has_ctx(p.mode) && vq[k] == 1) {
+                const ReqInfo r = req_info(p, nn[k], 1, tps);
+                c = (r.pages + r.ns - 1) / r.ns;
+                atomicAdd(&s.cls_cnt[c], 1);
+            }
+            s.dcls[b] = (signed char)c;
+        }
+    }
+    __syncthreads();
+    // counting sort of decode requests: class descending, request index ascending
+    if (warp == 0) {
+        // start position of classes 32..1 (lanes 0..31), then class 0
+        const int v = kClasses - 1 - lane;
+        const int cnt = s.cls_cnt[v];
+        int inc = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += t;
+        }
+        const int c0 = s.cls_cnt[0];
+        __syncwarp();
+        s.cls_cnt[v] = inc - cnt;
+        if (lane == 31) {
+            s.cls_cnt[0] = inc;
+            s.n_dec_req = inc + c0;
+        }
+        __syncwarp();
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            const int c = b < p.B ? s.dcls[b] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, c);
+            const int base = c >= 0 ? s.cls_cnt[c] : 0;
+            if (c >= 0) s.order[base + __popc(same & ((1u << lane) - 1u))] = (short)b;
+            __syncwarp();
+            if (c >= 0 && lane == __ffs(same) - 1) s.cls_cnt[c] = base + __popc(same);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // decode items per sorted position
+    int dv[PER];
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        const int pos = tid * PER + k;
+        dv[k] = 0;
+        if (pos < s.n_dec_req) dv[k] = p.HQ * req_info(p, s.nctx[s.order[pos]], 1, tps).ns;
+    }
+    block_scan<D, PER>(dv, s.dec, s.n_dec_req, s);
+    if (tid == 0 && s.qo[p.B] > p.max_q_total) s.bad |= FLAG_Q_TOTAL;
+    __syncthreads();
+}
+
 // Per-CTA schedule over the batch (B <= kMaxB): row prefix qo, multi-row
-// item prefix mq, and the decode queue.  Built by warp 0 alone, 32 requests
-// per round, with warp shuffles (no block-wide barrier until the end):
+// item prefix mq, and the decode queue.  Up to 32 requests it is built by
+// warp 0 alone with warp shuffles (no block-wide barrier until the end);
+// larger batches use the block-wide build above.
 //   * Pages per decode item: between tps_min and tps_max, chosen so that the
 //     decode queue holds about kItemsPerWarp items per warp of the grid (fine
 //     enough for the dynamic queue to balance, coarse enough to keep the
@@ -306,6 +449,10 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
     constexpr int kClasses = 33;                  // item sizes 0..32 pages
     constexpr int kItemsPerWarp = 4;
     const int lane = threadIdx.x & 31;
+    if (p.B > 32) {
+        build_schedule_cta<D>(p, s);
+        return;
+    }
     if ((threadIdx.x >> 5) == 0) {
         const int pp = (p.n_prefix + kBlock - 1) / kBlock;
         unsigned flags = 0;
@@ -402,9 +549,29 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
 }
 
 // ----------------------------------------------------------------------------- merge (relay fusion)
-__device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int h)
+// Partial rows in the workspace (index into part_lse, and in units of D
+// floats into part_o):
+//   system part k (key range) of compact row r, head h:  (k * max_q_total + r) * H + h
+//   context part k of the decode request b (one row):     dec_base + (k * B + b) * H + h
+//   context part k of compact row r of a multi-row request:  mq_base + (k * max_q_total + r) * H + h
+// so a decode row reserves context slots once per request, not once per row
+// of the max_q_total bound.
+__device__ __forceinline__ size_t sys_slot(const Params &p, int k, int r, int h)
 {
-    return ((size_t)part * p.max_q_total + r) * p.H + h;
+    return ((size_t)k * p.max_q_total + r) * p.H + h;
+}
+__device__ __forceinline__ size_t dec_slot(const Params &p, int k, int b, int h)
+{
+    return (size_t)p.dec_base + ((size_t)k * p.B + b) * p.H + h;
+}
+__device__ __forceinline__ size_t mq_slot(const Params &p, int k, int r, int h)
+{
+    return (size_t)p.mq_base + ((size_t)k * p.max_q_total + r) * p.H + h;
+}
+// part j of a row: the n_sys system ranges first, then the context splits
+__device__ __forceinline__ size_t part_slot(const Params &p, int j, int n_sys, bool dec, int r, int b, int h)
+{
+    return j < n_sys ? sys_slot(p, j, r, h) : dec ? dec_slot(p, j - n_sys, b, h) : mq_slot(p, j - n_sys, r, h);
 }
 
 // Merge the partials of one output row (compact row r = row i of request b,
@@ -413,7 +580,7 @@ __device__ __forceinline__ size_t part_row(const Params &p, int part, int r, int
 // round trip), then the parts' output rows are loaded eight at a time with
 // all eight loads in flight together.  Lane t handles D/32 adjacent elements.
 template <int D>
-__device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx,
+__device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx, bool dec,
                           bool have_lk0 = false, float lk0 = 0.f)
 {
     constexpr int V = D / 32;
@@ -431,9 +598,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
         if (j0 == 0 && have_lk0) {
             lk = lane < cnt ? lk0 : kNegInf;
         } else if (lane < cnt) {
-            const int j = j0 + lane;
-            const int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-            lk = __ldcg(p.part_lse + part_row(p, part, r, h));
+            lk = __ldcg(p.part_lse + part_slot(p, j0 + lane, n_sys, dec, r, b, h));
         }
         float mk = lk;
 #pragma unroll
@@ -452,8 +617,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
             for (int k = 0; k < CH; k++) {
                 const int j = j0 + c0 + k;
                 if (c0 + k < cnt) {
-                    const int part = j < n_sys ? j : p.ctx_base + (j - n_sys);
-                    const float *src = p.part_o + part_row(p, part, r, h) * D + d0;
+                    const float *src = p.part_o + part_slot(p, j, n_sys, dec, r, b, h) * D + d0;
                     if constexpr (V == 4) {
                         const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
                         x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
@@ -737,9 +901,10 @@ __device__ __forceinline__ void load_q_rows(unsigned (&qf)[D / 16][4], const __h
 }
 
 // Write one warp's partial rows (normalised output, log2-sum-exp).
+// (system part k when !mq, else context part k of a multi-row request)
 template <int D>
-__device__ __forceinline__ void write_row_partials(const Params &p, const RowState<D> &ws, int part, int hA, int rA,
-                                                   bool vA, int hB, int rB, bool vB)
+__device__ __forceinline__ void write_row_partials(const Params &p, const RowState<D> &ws, bool mq, int k, int hA,
+                                                   int rA, bool vA, int hB, int rB, bool vB)
 {
     const int tig = threadIdx.x & 3;
     float l0 = ws.l[0], l1 = ws.l[1];
@@ -752,7 +917,8 @@ __device__ __forceinline__ void write_row_partials(const Params &p, const RowSta
         if (!(half ? vB : vA)) continue;
         float l = half ? l1 : l0, m = ws.m[half];
         float inv = l > 0.f ? 1.f / l : 0.f;
-        size_t pr = part_row(p, part, half ? rB : rA, half ? hB : hA);
+        const int r = half ? rB : rA, h = half ? hB : hA;
+        const size_t pr = mq ? mq_slot(p, k, r, h) : sys_slot(p, k, r, h);
         float *po = p.part_o + pr * D;
 #pragma unroll
         for (int n = 0; n < D / 8; n++)
@@ -884,7 +1050,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
-    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
+    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, false, rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
 }
 
 // Context item of a request with several query rows (causal within the context).
@@ -933,7 +1099,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
     ws.l[0] = ws.l[1] = 0.f;
     run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0)
-        write_row_partials<D>(p, ws, p.ctx_base + split, h, s.qo[b] + iA, iA < ql, h, s.qo[b] + iB, iB < ql);
+        write_row_partials<D>(p, ws, true, split, h, s.qo[b] + iA, iA < ql, h, s.qo[b] + iB, iB < ql);
 }
 
 // ============================================================================= phase 2: decode items
@@ -1105,7 +1271,7 @@ __device__ void dec_epilogue(const Params &p, const Smem<D> &s, const DecItem<D>
     L += __shfl_xor_sync(0xffffffffu, L, 16);
     L = __shfl_sync(0xffffffffu, L, 0);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const size_t pr = part_row(p, p.ctx_base + it.split, s.qo[it.b], it.h);
+    const size_t pr = dec_slot(p, it.split, it.b, it.h);
     if (tig == 0) {
         float *po = p.part_o + pr * D;
 #pragma unroll
@@ -1219,7 +1385,7 @@ __device__ void dec_epilogue_grp(const Params &p, const Smem<D> &s, const DecIte
         const int c = 2 * tig + e;
         if (c >= it.nh) continue;
         const float inv = L[e] > 0.f ? 1.f / L[e] : 0.f;
-        const size_t pr = part_row(p, p.ctx_base + it.split, s.qo[it.b], it.h + c);
+        const size_t pr = dec_slot(p, it.split, it.b, it.h + c);
         float *po = p.part_o + pr * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; mt++) {
@@ -1414,26 +1580,24 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
         // split size and the log-sum-exps of the first 32 slots the row may
         // use are loaded together (one round trip).  Lane k's slot is part k
         // of the row whatever its context turns out to be (system ranges
-        // first, then context splits from ctx_base), which is what merge_row
-        // reads for its first 32 parts; slots past the row's own parts are
-        // inside the workspace and masked there.
+        // first, then context splits), which is what merge_row reads for its
+        // first 32 parts; slots past the row's own parts are inside the
+        // workspace and masked there.
         const int lane = threadIdx.x & 31;
         const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
         const int r = w / p.H, h = w % p.H;
         if (r >= p.B * p.Lq) return;
         const int b = r / p.Lq;
         const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
-        const int ncand = n_sys + (has_ctx(p.mode) ? p.c_max : 0);
+        const bool dec = p.Lq == 1;
+        const int ncand = n_sys + (has_ctx(p.mode) ? (dec ? p.c_dec : p.c_mq) : 0);
         float lk = kNegInf;
-        if (lane < ncand) {
-            const int part = lane < n_sys ? lane : p.ctx_base + (lane - n_sys);
-            lk = __ldcg(p.part_lse + part_row(p, part, r, h));
-        }
+        if (lane < ncand) lk = __ldcg(p.part_lse + part_slot(p, lane, n_sys, dec, r, b, h));
         const int tps = __ldcg(p.sched);
         const int nc = has_ctx(p.mode) ? __ldg(p.ctx_lens + b) : 0;
         if (tps < 0) return;
         const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
-        merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, true, lk);
+        merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, dec, true, lk);
         return;
     }
     const int tps = p.sched[0];
@@ -1448,7 +1612,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     const int ql = qo[b + 1] - qo[b];
     const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
     const int n_ctx = has_ctx(p.mode) ? req_info(p, nctx[b], ql, tps).ns : 0;
-    merge_row<D>(p, r, b, r - qo[b], h, n_sys, n_ctx);
+    merge_row<D>(p, r, b, r - qo[b], h, n_sys, n_ctx, ql == 1);
 }
 
 // ============================================================================= KV append
