@@ -260,6 +260,105 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- the other workloads
+def measure_workload(relay, case, dev, timed, as_graph, steps, warmup, baseline=True, sys_step=False):
+    """Relay step (and optionally the non-relay baseline and the system step
+    alone) of one workload, timed like the headline: graph replay, L2 flushed
+    before every step, CUDA events on the launching stream."""
+    g = {k: getattr(case, k).to(dev) for k in ("q", "sys_k", "sys_v", "k_cache", "v_cache", "block_tables",
+                                              "ctx_lens")}
+    ql = None if case.q_lens is None else case.q_lens.to(dev)
+    mq = case.total_q() if ql is not None else 0
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, Hkv=case.Hkv, max_q_total=mq)
+    ws = relay.make_workspace(dims, dev)
+    out = torch.empty_like(g["q"])
+
+    def step():
+        relay.relay_attention_decode(g["q"], g["sys_k"], g["sys_v"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                     g["ctx_lens"], ql, out=out, workspace=ws, dims=dims)
+    ms, _ = timed(as_graph(step), steps, warmup)
+    abytes = algorithmic_bytes(case)
+    us = 1e3 * statistics.mean(ms)
+    res = {"step_us": us, "algorithmic_bytes": abytes, "hbm_gbs": abytes / (us * 1e-6) / 1e9,
+           "tokens_per_s": case.total_q() / (us * 1e-6), "requests_per_s": case.B / (us * 1e-6),
+           "launches_per_step": launches_per_step(case)}
+    if sys_step:
+        # the system step alone (relay_sys_attn: the tensor-core kernel, then its partials fused into o_sys)
+        o_s = torch.empty(*g["q"].shape, dtype=torch.float32, device=dev)
+        l_s = torch.empty(*g["q"].shape[:3], dtype=torch.float32, device=dev)
+
+        def sys_only():
+            relay.relay_sys_attn(g["q"], g["sys_k"], g["sys_v"], ql, o_sys=o_s, lse_sys=l_s, workspace=ws,
+                                 max_q_total=mq)
+        ms_s, _ = timed(as_graph(sys_only), steps, warmup)
+        sus = 1e3 * statistics.mean(ms_s)
+        flops = 4 * case.total_q() * case.Ls * case.D * case.H
+        res["system_step"] = {"us": sus, "flops": flops, "tflops": flops / (sus * 1e-6) / 1e12,
+                              "what": "relay_sys_attn: sys_tc_kernel (tcgen05) + fusion of its partials into o_sys"}
+        del o_s, l_s
+    if baseline:
+        kp, vp, ids = synth.with_system_in_pool(case)
+        kp, vp, ids = kp.to(dev), vp.to(dev), ids.to(dev)
+        dims_b = relay.make_dims(g["q"], case.Ls, kp.shape[0], case.max_blocks, max_q_total=mq, Hkv=case.Hkv)
+        ws_b = relay.make_workspace(dims_b, dev)
+        out_b = torch.empty_like(out)
+
+        def base_step():
+            relay.relay_baseline_decode(g["q"], kp, vp, ids, case.Ls, g["block_tables"], g["ctx_lens"], ql,
+                                        out=out_b, workspace=ws_b, dims=dims_b)
+        ms_b, _ = timed(as_graph(base_step), steps, warmup)
+        bus = 1e3 * statistics.mean(ms_b)
+        res["nonrelay_us"] = bus
+        res["relay_speedup"] = bus / us
+        del kp, vp, ids, ws_b, out_b
+    del g, ws, out
+    return res
+
+
+def run_configs(args, relay, dev, timed, as_graph, peaks):
+    """The other workloads of the study at their full sizes (one line each in
+    `configs`): the Llama-30B system-prompt-length sweep with the non-relay
+    baseline ("flat in Ls"), the batch-256 Llama-2-7B step, and the Llama-2-13B
+    mixed step whose system step runs on the tensor cores."""
+    steps = max(3, args.steps // 4)
+    hbm = peaks["hbm_gbs"]
+    out = {"timing": f"{steps} timed steps per point after {args.warmup} warm-up steps, graph replay, "
+                     "L2 flushed before every step, CUDA events"}
+    pts = []
+    for Ls in synth.SWEEP_LS:
+        case = synth.make_case(synth.workload("llama30b_sweep", Ls=Ls), seed=args.seed)
+        r = measure_workload(relay, case, dev, timed, as_graph, steps, args.warmup)
+        pts.append({"Ls": Ls, "relay_us": r["step_us"], "nonrelay_us": r["nonrelay_us"],
+                    "relay_speedup": r["relay_speedup"], "algorithmic_bytes": r["algorithmic_bytes"],
+                    "hbm_gbs": r["hbm_gbs"], "frac": r["hbm_gbs"] / hbm})
+        del case
+    out["llama30b_sweep"] = {
+        "shape": "H=52, D=128, B=32, 1 query row each, ctx U[128,512], Ls swept", "points": pts,
+        "relay_growth_16384_over_512": pts[-1]["relay_us"] / pts[0]["relay_us"],
+        "nonrelay_growth_16384_over_512": pts[-1]["nonrelay_us"] / pts[0]["nonrelay_us"],
+        "algorithmic_bytes_growth_16384_over_512": pts[-1]["algorithmic_bytes"] / pts[0]["algorithmic_bytes"]}
+    case = synth.make_case("llama2_7b_b256", seed=args.seed)
+    r = measure_workload(relay, case, dev, timed, as_graph, steps, args.warmup)
+    r["frac"] = r["hbm_gbs"] / hbm
+    out["llama2_7b_b256"] = dict(r, shape="H=32, D=128, B=256, Ls=4096, ctx lognormal(256, 1) in [1, 2048]")
+    del case
+    case = synth.make_case("llama2_13b_mixed", seed=args.seed)
+    r = measure_workload(relay, case, dev, timed, as_graph, steps, args.warmup, sys_step=True)
+    tf = peaks["bf16_tflops"]
+    flops = r["system_step"]["flops"]
+    hbm_floor = r["algorithmic_bytes"] / (hbm * 1e9) * 1e6
+    tensor_floor = flops / (tf * 1e12) * 1e6
+    r["roofline"] = {"hbm_floor_us": hbm_floor, "tensor_floor_us": tensor_floor,
+                     "frac_of_max_floor": max(hbm_floor, tensor_floor) / r["step_us"],
+                     "system_step_tensor_frac": r["system_step"]["tflops"] / tf,
+                     "peaks": f"{peaks['source']} copy bandwidth {hbm:.0f} GB/s, dense bf16 {tf:.0f} TFLOP/s "
+                              "(fp16 has the same nominal tensor rate)"}
+    out["llama2_13b_mixed"] = dict(r, shape="H=40, D=128, B=64 (56 x 1 row, 8 x 128-row chunks), Ls=32768, "
+                                            "ctx U[1,4096]")
+    del case
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU timing
 def run_relay(args):
     world, rank, local = dist_env()
@@ -487,6 +586,10 @@ def run_relay(args):
                              "flattened": "4 x relay_attention_decode (two kernels each)"}}
         del o_parts, l_parts, ws_t, flat
 
+    configs = None
+    if not args.no_configs:
+        configs = run_configs(args, relay, dev, timed, as_graph, load_peaks())
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = time_oracle(case, frac_rows=1.0, min_seconds=10.0, max_reps=200)
@@ -530,6 +633,8 @@ def run_relay(args):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     return 0
 
@@ -572,6 +677,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--quick", action="store_true", help="relay timing only: no baseline, e2e or CPU legs")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (Llama-30B sweep, batch 256, 13B mixed)")
     ap.add_argument("--ctx-split", type=int, default=0, help="context keys per decode work item (0: automatic)")
     ap.add_argument("--sys-range", type=int, default=0, help="system keys per work item (0: automatic)")
     ap.add_argument("--ref-stride", type=int, default=8, help="reference arm: time every n-th output row")
