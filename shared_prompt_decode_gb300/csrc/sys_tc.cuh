@@ -312,8 +312,12 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 
 
 
-// blockIdx.x = (range * pairs + pair) * Hkv + hk.  tmK / tmV view sys_k / sys_v
-// as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box and 128-byte swizzle.
+// System step: blockIdx.x = (range * Hkv + hk) * pairs + pair, so the tile
+// pairs that stream the same keys (one KV head, one key range) are adjacent
+// in launch order, run in the same wave and share those keys through L2.
+// Prefill: blockIdx.x = pair' * Hkv + hk, pairs latest first.  tmK / tmV view
+// sys_k / sys_v as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box
+// and 128-byte swizzle.
 //
 // PREFILL: causal self-attention of the system prompt itself (its Ls query
 // rows, in q = [Ls][H][128]; row t sees system keys 0..t), one key range:
@@ -351,8 +355,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int Mtot = PREFILL ? p.Ls : min(qo[p.B], p.max_q_total);
     const int Mv = Mtot * p.G;                       // virtual rows of a KV head
     const int T = (Mv + kRowsTC - 1) / kRowsTC;
-    const int hk = blockIdx.x % p.Hkv;
-    const int pair = PREFILL ? p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs : (blockIdx.x / p.Hkv) % p.pairs;
+    const int hk = PREFILL ? blockIdx.x % p.Hkv : (blockIdx.x / p.pairs) % p.Hkv;
+    const int pair = PREFILL ? p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs : blockIdx.x % p.pairs;
     const int rho = blockIdx.x / (p.Hkv * p.pairs);
     if (2 * pair >= T || rho >= p.R) return;        // the whole CTA leaves together
     const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
