@@ -577,14 +577,30 @@ def run_relay(args):
                 relay.relay_attention_decode(qg, fk, fv, g["k_cache"], g["v_cache"], btg, clg, out=og, workspace=wsg,
                                              dims=fd)
         ms_f, _ = timed(as_graph(flat_step), max(5, args.steps // 8), args.warmup)
+        # the same tree in one unit: five shared segments, request b sees the global prompt and its group's
+        segs_k = [g["sys_k"]] + [k for k, _ in grp]
+        segs_v = [g["sys_v"]] + [v for _, v in grp]
+        seg_mask = torch.tensor([1 | (2 << (b % groups)) for b in range(case.B)], dtype=torch.int32, device=dev)
+        dims_f = relay.make_dims(g["q"], 0, case.num_blocks, case.max_blocks, Hkv=case.Hkv)
+        ws_f = torch.zeros(relay.prefixes_workspace_size(dims_f, [case.Ls] + [Lp] * groups), dtype=torch.uint8,
+                           device=dev)
+        out_fu = torch.empty_like(out)
+
+        def fused_step():
+            relay.relay_attention_decode_prefixes(g["q"], segs_k, segs_v, seg_mask, g["k_cache"], g["v_cache"],
+                                                  g["block_tables"], g["ctx_lens"], out=out_fu, workspace=ws_f,
+                                                  dims=dims_f)
+        ms_fu, _ = timed(as_graph(fused_step), max(5, args.steps // 8), args.warmup)
         kv_tok = 2 * case.Hkv * case.D * 2
         tree = {"groups": groups, "group_prompt_tokens": Lp,
+                "fused_us": 1e3 * statistics.mean(ms_fu),
                 "tree_us": 1e3 * statistics.mean(ms_t), "flattened_us": 1e3 * statistics.mean(ms_f),
                 "tree_kv_bytes": (case.Ls + groups * Lp + int(case.ctx_lens.sum())) * kv_tok,
                 "flattened_kv_bytes": (groups * (case.Ls + Lp) + int(case.ctx_lens.sum())) * kv_tok,
-                "launches": {"tree": "5 x relay_sys_attn + relay_ctx_attn (two kernels each) + fuse_n_kernel",
+                "launches": {"fused": "relay_attention_decode_prefixes (two kernels)",
+                             "tree": "5 x relay_sys_attn + relay_ctx_attn (two kernels each) + fuse_n_kernel",
                              "flattened": "4 x relay_attention_decode (two kernels each)"}}
-        del o_parts, l_parts, ws_t, flat
+        del o_parts, l_parts, ws_t, flat, ws_f, out_fu
 
     configs = None
     if not args.no_configs:

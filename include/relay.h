@@ -18,8 +18,10 @@
  *
  * Entry points: relay_attention_decode (all three steps; also an
  * allocation-free variant), relay_sys_attn / relay_ctx_attn / relay_fuse
- * (the steps one at a time), relay_fuse_n (fusion of K parts: a tree of
- * shared prefixes), relay_baseline_decode (the non-relay formulation), and
+ * (the steps one at a time), relay_attention_decode_prefixes (a tree of
+ * shared prefixes in one unit) and relay_fuse_n (fusion of K parts, for
+ * composing such a tree from the separate steps), relay_baseline_decode (the
+ * non-relay formulation), and
  * the steps on either side of the path: relay_kv_append (cache write),
  * relay_rope (rotary positions offset by the system prompt) and
  * relay_sys_prefill (causal attention of the system prompt itself).
@@ -200,6 +202,45 @@ relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q,
 relay_status_t relay_fuse_n(const relay_dims_t *dims, int K, const float *const *o_parts,
                             const float *const *lse_parts, const int32_t *q_lens, void *out,
                             float *lse_out, relay_stream_t stream);
+
+/* Maximum number of shared prefix segments of relay_attention_decode_prefixes. */
+#define RELAY_MAX_SEGMENTS 8
+
+/* Bytes of workspace relay_attention_decode_prefixes needs for `dims` and
+ * these segment lengths (seg_len: HOST array of n_seg token counts); 0 if
+ * invalid.  Sized for the current device (its SM count sets the number of
+ * key ranges per segment). */
+size_t relay_workspace_size_prefixes(const relay_dims_t *dims, int n_seg, const int32_t *seg_len);
+
+/* All three steps for a tree of shared prefixes in one queued unit (two
+ * kernels): relay fusion generalised from one shared system prompt to
+ * several shared segments -- e.g. a global system prompt seen by every
+ * request and one group prompt per group of requests (the multi-level
+ * prefix sharing that the works built on RelayAttention develop; the
+ * fusion itself is the convex combination of the atyun.com RelayAttention
+ * article, section "RelayAttention", over more than two parts).  Request b
+ * attends over the segments s whose bit s is set in seg_mask[b], then its
+ * own paged context; each segment's KV is read from memory once per batch,
+ * by system items of the streaming kernel (never the tensor-core kernel:
+ * for large batches with one prompt, relay_attention_decode is faster), and
+ * the merge kernel fuses every segment's key ranges and the context splits
+ * of each row by their log-sum-exps.  The result equals causal attention
+ * over [the segments it sees, in any order; its context].
+ *  - n_seg in [1, RELAY_MAX_SEGMENTS]; seg_k, seg_v, seg_len: HOST arrays of
+ *    n_seg entries: device pointers to [seg_len[s], Hkv, D] fp16 (16-byte
+ *    aligned; may be NULL when seg_len[s] == 0) and the token counts.
+ *  - seg_mask: device [B] uint32 (nullable: every request sees every
+ *    segment).  A row that sees no key at all gets out = 0, lse = -inf.
+ *  - dims->Ls is not used; the other arguments, layouts and errors are
+ *    those of relay_attention_decode, with the workspace sized by
+ *    relay_workspace_size_prefixes. */
+relay_status_t relay_attention_decode_prefixes(const relay_dims_t *dims, const void *q, int n_seg,
+                                               const void *const *seg_k, const void *const *seg_v,
+                                               const int32_t *seg_len, const uint32_t *seg_mask,
+                                               const void *k_cache, const void *v_cache,
+                                               const int32_t *block_tables, const int32_t *ctx_lens,
+                                               const int32_t *q_lens, void *out, float *lse_out, void *ws,
+                                               size_t ws_bytes, relay_stream_t stream);
 
 /* KV append: the step's new keys and values into the paged context pool (the
  * cache write that precedes attention in every decode iteration; the

@@ -8,6 +8,8 @@ library is missing, importing the binding's functions raises.
 Entry points (same names as the C ABI in include/relay.h):
     relay_attention_decode(...)   all three steps, queued as one unit (two kernels; three with
                                   the tensor-core system step)
+    relay_attention_decode_prefixes(...)  the same for a tree of shared prefixes: several shared
+                                  segments, each request seeing those its mask selects
     relay_sys_attn(...)           step 1: system attention -> fp32 o, lse
     relay_ctx_attn(...)           step 2: context attention -> fp32 o, lse
     relay_fuse(...)               step 3: relay fusion -> fp16 out, lse
@@ -71,6 +73,9 @@ _SIGS = {
     "relay_fuse_n": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP, _VP, _VP]),
     "relay_rope": (ctypes.c_int, [ctypes.POINTER(Dims)] + [_VP] * 4 + [ctypes.c_float, _VP, ctypes.c_size_t, _VP]),
     "relay_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "relay_workspace_size_prefixes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int, _VP]),
+    "relay_attention_decode_prefixes": (ctypes.c_int, [ctypes.POINTER(Dims), _VP, ctypes.c_int, _VP, _VP, _VP, _VP]
+                                        + [_VP] * 8 + [ctypes.c_size_t, _VP]),
 }
 
 
@@ -233,6 +238,70 @@ def relay_attention_decode(q, sys_k, sys_v, k_cache, v_cache, block_tables, ctx_
                                       _ptr(v_cache), _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
                                       _ptr(out), _ptr(lse_out), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "relay_attention_decode")
+    return out
+
+
+MAX_SEGMENTS = 8
+
+
+def prefixes_workspace_size(dims: Dims, seg_lens) -> int:
+    arr = (ctypes.c_int32 * len(seg_lens))(*[int(x) for x in seg_lens])
+    return int(lib().relay_workspace_size_prefixes(ctypes.byref(dims), len(seg_lens), arr))
+
+
+def relay_attention_decode_prefixes(q, seg_k, seg_v, seg_mask, k_cache, v_cache, block_tables, ctx_lens,
+                                    q_lens=None, out=None, lse_out=None, workspace=None, scale=None,
+                                    max_q_total=0, ctx_split=0, sys_range=0, stream=None, dims=None):
+    """A tree of shared prefixes: seg_k / seg_v are lists of [L_s, Hkv, D] fp16 segments, seg_mask a
+    [B] int32 tensor whose bit s says that request b sees segment s (None: every request sees every
+    segment).  Returns out [B, Lq, H, D] fp16."""
+    dev = q.device
+    B, Lq, H, D = q.shape
+    if not (1 <= len(seg_k) <= MAX_SEGMENTS) or len(seg_k) != len(seg_v):
+        raise ValueError(f"1..{MAX_SEGMENTS} segments with K and V each")
+    Hkv = k_cache.shape[1]
+    for i, (k, v) in enumerate(zip(seg_k, seg_v)):
+        _same(k, v, (f"seg_k[{i}]", f"seg_v[{i}]"))
+        if k.dim() != 3 or k.shape[1] != Hkv or k.shape[2] != D:
+            raise ValueError(f"seg_k[{i}] {tuple(k.shape)} must be [L, {Hkv}, {D}]")
+        _need(k, f"seg_k[{i}]", torch.float16, dev)
+        _need(v, f"seg_v[{i}]", torch.float16, dev)
+    _pool_shapes(k_cache, v_cache, D, ("k_cache", "v_cache"))
+    _table_shapes(B, block_tables, ctx_lens, q_lens)
+    _shape(seg_mask, "seg_mask", (B,))
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", (B, Lq, H))
+    _need(q, "q", torch.float16)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, torch.float16, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    _opt(q_lens, "q_lens", torch.int32, dev)
+    _opt(seg_mask, "seg_mask", torch.int32, dev)
+    if dims is None:
+        dims = make_dims(q, 0, k_cache.shape[0], block_tables.shape[1], scale, max_q_total, ctx_split, sys_range,
+                         Hkv)
+    _check_dims(dims, q, None, k_cache, block_tables)
+    _check_kv(dims, k_cache, "k_cache")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, dev)
+    _opt(lse_out, "lse_out", torch.float32, dev)
+    lens = [int(k.shape[0]) for k in seg_k]
+    if workspace is None:
+        n = prefixes_workspace_size(dims, lens)
+        if n == 0:
+            raise ValueError(f"invalid dims {dims} or segments {lens}")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    n = len(seg_k)
+    kp = (ctypes.c_void_p * n)(*[k.data_ptr() for k in seg_k])
+    vp = (ctypes.c_void_p * n)(*[v.data_ptr() for v in seg_v])
+    lp = (ctypes.c_int32 * n)(*lens)
+    rc = lib().relay_attention_decode_prefixes(
+        ctypes.byref(dims), _ptr(q), n, kp, vp, lp, _ptr(seg_mask), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens), _ptr(out), _ptr(lse_out), _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    _check(rc, "relay_attention_decode_prefixes")
     return out
 
 

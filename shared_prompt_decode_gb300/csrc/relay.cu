@@ -24,6 +24,7 @@ using namespace relay;
 constexpr int kMaxDevices = 64;
 constexpr int kAutoCtxSplit = 512;
 constexpr int kMaxMqParts = 8;         // context splits of a multi-row request, at most
+static_assert(RELAY_MAX_SEGMENTS == kMaxSegments, "segment limit of the header and the kernels");
 
 struct DevInfo {
     bool ready = false;
@@ -143,9 +144,28 @@ bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared prefix segments of a call: the system prompt alone (one segment of
+// dims->Ls tokens), or the levels of a tree of shared prefixes.
+struct Segments {
+    int n = 0;
+    int len[kMaxSegments] = {};
+    const void *k[kMaxSegments] = {}, *v[kMaxSegments] = {};
+};
+
+Segments one_segment(const relay_dims_t *d, const void *k, const void *v)
+{
+    Segments sg;
+    sg.n = 1;
+    sg.len[0] = d->Ls;
+    sg.k[0] = k;
+    sg.v[0] = v;
+    return sg;
+}
+
 struct Plan {
     int Mtot = 0;
     int R_sys = 0, sys_range = kTileK, ctx_split = kAutoCtxSplit;
+    int seg_R[kMaxSegments] = {}, seg_range[kMaxSegments] = {}, seg_part0[kMaxSegments] = {};
     int c_dec = 0, c_mq = 0, mq_split_min = 0, n_prefix = 0;
     int tps_min = 32, tps_max = 32;
     bool tc = false;          // system step on the tensor-core kernel
@@ -157,7 +177,9 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Work-item sizes and workspace layout for one mode, for a GPU of `sms` SMs
 // (one streaming CTA per SM; the number of system key ranges depends on it).
-Plan make_plan(const relay_dims_t *d, int mode, int sms)
+// `seg`: several shared prefix segments (never on the tensor-core kernel);
+// null: the one system prompt of dims->Ls tokens.
+Plan make_plan(const relay_dims_t *d, int mode, int sms, const Segments *seg = nullptr)
 {
     Plan pl;
     pl.Mtot = d->max_q_total > 0 ? d->max_q_total : d->B * d->Lq;
@@ -166,7 +188,7 @@ Plan make_plan(const relay_dims_t *d, int mode, int sms)
     pl.n_prefix = mode == MODE_BASELINE ? d->Ls : 0;
     const int G = d->H / kv_heads(d);            // query heads per KV head
     const long long Mv = (long long)pl.Mtot * G;   // rows of the system step per KV head
-    pl.tc = sys && d->D == 128 && d->Ls > 0 && Mv > kTcMinRows;
+    pl.tc = !seg && sys && d->D == 128 && d->Ls > 0 && Mv > kTcMinRows;
     if (pl.tc) {
         // (head, tile pair, key range) items, one CTA each.  The number of
         // ranges R minimises the makespan in waves of one CTA per SM times
@@ -190,29 +212,44 @@ Plan make_plan(const relay_dims_t *d, int mode, int sms)
         int range = d->sys_range > 0 ? d->sys_range : round_up((d->Ls + r_best - 1) / r_best, tc::kKeysTC);
         pl.sys_range = range;
         pl.R_sys = (d->Ls + range - 1) / range;
+        pl.seg_range[0] = range;
+        pl.seg_R[0] = pl.R_sys;
     } else if (sys) {
-        if (d->Ls > 0) {
-            int range = d->sys_range;
-            if (range == 0) {
-                // Enough system items to spread over the GPU, but long enough
-                // ranges that each range's partial results stay small next to
-                // the system keys it streams.
-                const int tiles = (int)((Mv + kTileM - 1) / kTileM);
-                const int hkv = kv_heads(d);
-                int r_want = (sms + hkv * tiles - 1) / (hkv * tiles);
-                // cap on the ranges from the query rows per head (not the
-                // virtual rows of a head group), so the items stay short
-                int r_cap = d->Ls / std::max(256, 16 * pl.Mtot);
-                int r = std::max(1, std::min(r_want, r_cap));
-                range = round_up((d->Ls + r - 1) / r, kTileK);
+        const Segments one = one_segment(d, nullptr, nullptr);
+        const Segments &sg = seg ? *seg : one;
+        long long total = 0;
+        for (int i = 0; i < sg.n; i++) total += sg.len[i];
+        pl.R_sys = 0;
+        for (int i = 0; i < sg.n; i++) {
+            const int L = sg.len[i];
+            int range = kTileK, R = 0;
+            if (L > 0) {
+                range = d->sys_range;
+                if (range == 0) {
+                    // Enough system items to spread over the GPU (segments
+                    // share it by length), but long enough ranges that each
+                    // range's partial results stay small next to the keys it
+                    // streams.
+                    const int tiles = (int)((Mv + kTileM - 1) / kTileM);
+                    const int hkv = kv_heads(d);
+                    const long long share = std::max<long long>(1, (long long)sms * L / std::max<long long>(1, total));
+                    int r_want = (int)((share + (long long)hkv * tiles - 1) / ((long long)hkv * tiles));
+                    // cap on the ranges from the query rows per head (not the
+                    // virtual rows of a head group), so the items stay short
+                    int r_cap = L / std::max(256, 16 * pl.Mtot);
+                    int r = std::max(1, std::min(r_want, r_cap));
+                    range = round_up((L + r - 1) / r, kTileK);
+                }
+                R = (L + range - 1) / range;
+            } else if (mode == MODE_SYS && sg.n == 1) {
+                R = 1;   // one empty range still reports lse = -inf for sys-only output
             }
-            pl.sys_range = range;
-            pl.R_sys = (d->Ls + range - 1) / range;
-        } else {
-            pl.R_sys = 1;   // one empty range still reports lse = -inf for sys-only output
-            pl.sys_range = kTileK;
+            pl.seg_range[i] = range;
+            pl.seg_R[i] = R;
+            pl.seg_part0[i] = pl.R_sys;
+            pl.R_sys += R;
         }
-        if (mode == MODE_FUSED && d->Ls == 0) pl.R_sys = 0;
+        pl.sys_range = pl.seg_range[0];
     }
     if (ctx) {
         // Context splits per request.  A decode request's pages (prefix
@@ -256,8 +293,29 @@ float scale_log2_of(const relay_dims_t *d)
     return sc * 1.4426950408889634f;
 }
 
+// Shared prefix segments from the caller's host arrays: 1..kMaxSegments
+// segments of >= 0 tokens, [len, Hkv, D] fp16 each, 16-byte aligned.
+relay_status_t make_segments(int n_seg, const void *const *k, const void *const *v, const int32_t *len,
+                             Segments *out)
+{
+    if (n_seg < 1 || n_seg > kMaxSegments || !len) return RELAY_ERR_INVALID_ARG;
+    long long total = 0;
+    out->n = n_seg;
+    for (int i = 0; i < n_seg; i++) {
+        if (len[i] < 0) return RELAY_ERR_INVALID_ARG;
+        total += len[i];
+        out->len[i] = len[i];
+        out->k[i] = k ? k[i] : nullptr;
+        out->v[i] = v ? v[i] : nullptr;
+        if (len[i] > 0 && (!out->k[i] || !out->v[i] || !aligned(out->k[i], 16) || !aligned(out->v[i], 16)))
+            return RELAY_ERR_INVALID_ARG;
+    }
+    if (total > INT_MAX / 2) return RELAY_ERR_UNSUPPORTED;
+    return RELAY_OK;
+}
+
 relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws, size_t ws_bytes,
-                            relay_stream_t stream)
+                            relay_stream_t stream, const Segments *seg = nullptr)
 {
     if (!ws) return RELAY_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return RELAY_ERR_INVALID_ARG;
@@ -265,12 +323,12 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     // q_lens every request has Lq rows, and the partial slots are laid out
     // for max_q_total rows) a bound below B * Lq; with q_lens the kernel
     // checks their sum on the device
-    if (ws_bytes < make_plan(d, mode, 1).total) return RELAY_ERR_WORKSPACE;
-    if (!p.q_lens && (long long)d->B * d->Lq > make_plan(d, mode, 1).Mtot) return RELAY_ERR_INVALID_ARG;
+    if (ws_bytes < make_plan(d, mode, 1, seg).total) return RELAY_ERR_WORKSPACE;
+    if (!p.q_lens && (long long)d->B * d->Lq > make_plan(d, mode, 1, seg).Mtot) return RELAY_ERR_INVALID_ARG;
     const DevInfo *dev = nullptr;
     relay_status_t st = device_info(&dev);
     if (st != RELAY_OK) return st;
-    Plan pl = make_plan(d, mode, dev->sms);
+    Plan pl = make_plan(d, mode, dev->sms, seg);
     if (ws_bytes < pl.total) return RELAY_ERR_WORKSPACE;
 
     unsigned char *base = static_cast<unsigned char *>(ws);
@@ -303,6 +361,19 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.mq_base = (long long)pl.mq_base;
     p.skip_sys = pl.tc ? 1 : 0;
     p.mode = mode;
+    {
+        const Segments one = one_segment(d, p.sys_k, p.sys_v);
+        const Segments &sg = seg ? *seg : one;
+        p.n_seg = sg.n;
+        for (int i = 0; i < sg.n; i++) {
+            p.seg_k[i] = static_cast<const __half *>(sg.k[i]);
+            p.seg_v[i] = static_cast<const __half *>(sg.v[i]);
+            p.seg_len[i] = sg.len[i];
+            p.seg_range[i] = pl.seg_range[i];
+            p.seg_R[i] = pl.seg_R[i];
+            p.seg_part0[i] = pl.seg_part0[i];
+        }
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.tc) {
@@ -534,6 +605,55 @@ relay_status_t relay_attention_decode(const relay_dims_t *dims, const void *q, c
     p.out = static_cast<__half *>(out);
     p.lse_out = lse_out;
     return launch_relay(dims, MODE_FUSED, p, ws, ws_bytes, stream);
+}
+
+size_t relay_workspace_size_prefixes(const relay_dims_t *dims, int n_seg, const int32_t *seg_len)
+{
+    if (check_dims(dims) != RELAY_OK) return 0;
+    Segments sg;
+    if (n_seg < 1 || n_seg > kMaxSegments || !seg_len) return 0;
+    for (int i = 0; i < n_seg; i++) {
+        if (seg_len[i] < 0) return 0;
+        sg.len[i] = seg_len[i];
+    }
+    sg.n = n_seg;
+    const DevInfo *dev = nullptr;
+    const int sms = device_info(&dev) == RELAY_OK ? dev->sms : INT_MAX / 4;
+    return make_plan(dims, MODE_FUSED, sms, &sg).total;
+}
+
+relay_status_t relay_attention_decode_prefixes(const relay_dims_t *dims, const void *q, int n_seg,
+                                               const void *const *seg_k, const void *const *seg_v,
+                                               const int32_t *seg_len, const uint32_t *seg_mask,
+                                               const void *k_cache, const void *v_cache,
+                                               const int32_t *block_tables, const int32_t *ctx_lens,
+                                               const int32_t *q_lens, void *out, float *lse_out, void *ws,
+                                               size_t ws_bytes, relay_stream_t stream)
+{
+    relay_status_t st = check_dims(dims);
+    if (st != RELAY_OK) return st;
+    Segments sg;
+    st = make_segments(n_seg, seg_k, seg_v, seg_len, &sg);
+    if (st != RELAY_OK) return st;
+    if (!q || !out || !ctx_lens || (dims->max_blocks_per_seq > 0 && !block_tables) ||
+        (dims->num_blocks > 0 && (!k_cache || !v_cache)))
+        return RELAY_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(lse_out, 4) || !aligned(block_tables, 4) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4) ||
+        !aligned(seg_mask, 4))
+        return RELAY_ERR_INVALID_ARG;
+    if (dims->B == 0) return RELAY_OK;
+    Params p = blank_params();
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const __half *>(k_cache);
+    p.v_cache = static_cast<const __half *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = ctx_lens;
+    p.q_lens = q_lens;
+    p.seg_mask = seg_mask;
+    p.out = static_cast<__half *>(out);
+    p.lse_out = lse_out;
+    return launch_relay(dims, MODE_FUSED, p, ws, ws_bytes, stream, &sg);
 }
 
 relay_status_t relay_baseline_decode(const relay_dims_t *dims, const void *q, const void *k_pool, const void *v_pool,

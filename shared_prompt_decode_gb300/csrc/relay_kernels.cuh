@@ -65,6 +65,7 @@ constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kTileM = 16 * kRowWarps;        // query rows per phase-1 item
 constexpr int kRingBytes = RELAY_RING_KB * 1024;
 constexpr int kMaxB = 512;
+constexpr int kMaxSegments = 8;   // shared prefix segments of one call
 
 enum Mode : int { MODE_FUSED = 0, MODE_SYS = 1, MODE_CTX = 2, MODE_BASELINE = 3 };
 
@@ -99,6 +100,15 @@ struct Params {
     long long dec_base, mq_base;      // first partial row of the decode and multi-row sections
     int skip_sys;                     // system partials come from the tensor-core kernel
     int mode;
+    // Shared prefix segments, each read once per batch: the system prompt
+    // (one segment), or the levels of a tree of shared prefixes.  Request b
+    // sees segment s when bit s of seg_mask[b] is set (seg_mask null: every
+    // request sees every segment).  Segment s has seg_R[s] key ranges of
+    // seg_range[s] keys, whose partials are system parts seg_part0[s] ...
+    int n_seg;
+    const __half *seg_k[kMaxSegments], *seg_v[kMaxSegments];
+    int seg_len[kMaxSegments], seg_range[kMaxSegments], seg_R[kMaxSegments], seg_part0[kMaxSegments];
+    const unsigned *seg_mask;
 };
 
 template <int D>
@@ -117,6 +127,7 @@ struct Smem {
     int mq[kMaxB + 1];        // exclusive prefix of multi-row context items
     int dec[kMaxB + 1];       // exclusive prefix of decode items over the decode order
     int nctx[kMaxB];          // context lengths (validated)
+    unsigned segm[kMaxB];     // segments each request sees (bit s: segment s)
     short order[kMaxB];       // decode requests, longest item first
     signed char dcls[kMaxB];  // largest item of a decode request in pages (-1: not a decode request)
     int cls_cnt[33];
@@ -346,6 +357,7 @@ __device__ __noinline__ void build_schedule_cta(const Params &p, Smem<D> &s)
         if (b < p.B) {
             ql = p.q_lens ? p.q_lens[b] : p.Lq;
             n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
+            s.segm[b] = p.seg_mask ? p.seg_mask[b] : ~0u;
             if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
             if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
             if (has_ctx(p.mode) && ql > 1) {
@@ -463,6 +475,7 @@ __device__ void build_schedule(const Params &p, Smem<D> &s)
             if (b < p.B) {
                 ql = p.q_lens ? p.q_lens[b] : p.Lq;
                 n = (has_ctx(p.mode) && p.ctx_lens) ? p.ctx_lens[b] : 0;
+                s.segm[b] = p.seg_mask ? p.seg_mask[b] : ~0u;
                 if (ql < 0 || ql > p.Lq) { flags |= FLAG_BAD_Q_LEN; ql = 0; }
                 if (n < 0 || n > p.max_blocks * kBlock) { flags |= FLAG_BAD_CTX_LEN; ql = 0; n = 0; }
                 if (has_ctx(p.mode) && ql > 1) {
@@ -1007,23 +1020,27 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
 // System items run over the virtual rows v = r * G + c of one KV head hk:
 // query row r of the batch with query head hk * G + c, so a KV head's
 // system keys are read once per 64 virtual rows whatever the head grouping
-// (multi-head: G = 1, v = r).
+// (multi-head: G = 1, v = r).  Items of a shared prefix segment: every KV
+// head, row tile and key range of it; rows of requests that do not see the
+// segment get no key (their partial has lse = -inf and counts for nothing).
 template <int D>
 __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
 {
     // KV heads vary fastest: CTAs that run concurrently read whole [Hkv, D]
-    // rows of the system cache together instead of one head's slivers
+    // rows of the segment together instead of one head's slivers
     const int Mv = Mtot * p.G;
     const int T = (Mv + kTileM - 1) / kTileM;
+    int seg = 0;
+    while (seg + 1 < p.n_seg && item >= p.Hkv * T * p.seg_R[seg]) item -= p.Hkv * T * p.seg_R[seg++];
     const int hk = item % p.Hkv;
     const int tau = (item / p.Hkv) % T;
     const int rho = item / (p.Hkv * T);
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;
 
-    KeySrc src{p.sys_k, p.sys_v, nullptr, nullptr, 0, p.Hkv, hk, 0};
-    const int key0 = rho * p.sys_range;
-    const int key_hi = min(key0 + p.sys_range, p.Ls);
+    KeySrc src{p.seg_k[seg], p.seg_v[seg], nullptr, nullptr, 0, p.Hkv, hk, 0};
+    const int key0 = rho * p.seg_range[seg];
+    const int key_hi = min(key0 + p.seg_range[seg], p.seg_len[seg]);
 
     const RowRoles rr = row_roles(min(kTileM, Mv - tau * kTileM));
     const int vW = tau * kTileM + rr.rg * 16;
@@ -1031,13 +1048,16 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     const int rA = vA / p.G, hA = hk * p.G + vA % p.G;
     const int rB = vB / p.G, hB = hk * p.G + vB % p.G;
     const __half *qa = nullptr, *qb = nullptr;
+    int endA = key0, endB = key0;     // keys the rows see: none unless their request sees the segment
     if (vA < Mv) {
         int b = find_owner(s.qo, p.B, rA);
         qa = p.q + (((size_t)b * p.Lq + (rA - s.qo[b])) * p.H + hA) * D;
+        if ((s.segm[b] >> seg) & 1u) endA = key_hi;
     }
     if (vB < Mv) {
         int b = find_owner(s.qo, p.B, rB);
         qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + hB) * D;
+        if ((s.segm[b] >> seg) & 1u) endB = key_hi;
     }
     unsigned qf[D / 16][4];
     load_q_rows<D>(qf, qa, qb);     // the query rows are requested before the item's tiles
@@ -1049,8 +1069,9 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
         for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
-    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, key_hi, key_hi, p.scale_log2, p.ctrl);
-    if (rr.active && rr.kg == 0) write_row_partials<D>(p, ws, false, rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
+    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
+    if (rr.active && rr.kg == 0)
+        write_row_partials<D>(p, ws, false, p.seg_part0[seg] + rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
 }
 
 // Context item of a request with several query rows (causal within the context).
@@ -1533,7 +1554,9 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     }
     const int Mtot = s.qo[p.B];
     const int T = (Mtot * p.G + kTileM - 1) / kTileM;     // tiles of virtual rows per KV head
-    const int n_sys = (has_sys(p.mode) && !p.skip_sys) ? p.Hkv * p.R_sys * T : 0;
+    int n_sys = 0;                                         // system items of every segment
+    if (has_sys(p.mode) && !p.skip_sys)
+        for (int sg = 0; sg < p.n_seg; sg++) n_sys += p.Hkv * T * p.seg_R[sg];
     const int n_rows = n_sys + s.mq[p.B];
     const int n_dec = s.dec[s.n_dec_req];
 

@@ -260,3 +260,32 @@ def test_binding_checks_shapes(relay):
                                 torch.zeros(32, 4, 128, dtype=f16), lse_out=torch.zeros(32, 2, dtype=f32))
     with pytest.raises(ValueError, match="k_new"):
         relay.relay_rope(q, a["ctx_lens"], 32, k_new=torch.zeros(2, 2, 4, 64, dtype=f16))
+
+
+def test_prefixes_host_validation(relay):
+    lib = relay.lib()
+    d = _dims(relay, Ls=0)
+    vp = ctypes.c_void_p
+    lens = (ctypes.c_int32 * 3)(2048, 512, 512)
+    ptrs = (ctypes.c_void_p * 3)(FAKE, FAKE + 4096, FAKE + 8192)
+    assert lib.relay_workspace_size_prefixes(ctypes.byref(d), 3, lens) > 0
+    one = lib.relay_workspace_size_prefixes(ctypes.byref(d), 1, lens)
+    assert 0 < one < lib.relay_workspace_size_prefixes(ctypes.byref(d), 3, lens)   # more segments, more parts
+    for n in (0, 9):
+        assert lib.relay_workspace_size_prefixes(ctypes.byref(d), n, lens) == 0
+    assert lib.relay_workspace_size_prefixes(ctypes.byref(d), 2, (ctypes.c_int32 * 2)(5, -1)) == 0
+
+    def call(n=3, k=ptrs, v=ptrs, L=lens, mask=None, q=FAKE, dims=d, B0=False):
+        dd = _dims(relay, Ls=0, B=0) if B0 else dims
+        return lib.relay_attention_decode_prefixes(ctypes.byref(dd), vp(q), n, k, v, L, vp(mask) if mask else None,
+                                                   vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), None,
+                                                   vp(FAKE), 1 << 30, None)
+    assert call(n=0) == relay.ERR_INVALID_ARG
+    assert call(n=9) == relay.ERR_INVALID_ARG
+    assert call(L=(ctypes.c_int32 * 3)(10, -1, 3)) == relay.ERR_INVALID_ARG
+    assert call(k=(ctypes.c_void_p * 3)(FAKE, None, FAKE)) == relay.ERR_INVALID_ARG        # segment 1 has keys
+    assert call(k=(ctypes.c_void_p * 3)(FAKE, FAKE + 8, FAKE)) == relay.ERR_INVALID_ARG    # not 16-byte aligned
+    assert call(mask=FAKE + 2) == relay.ERR_INVALID_ARG                                    # mask not 4-byte aligned
+    assert call(q=None) == relay.ERR_INVALID_ARG
+    # an empty segment may have no pointers; with nothing to do, nothing is queued
+    assert call(k=(ctypes.c_void_p * 3)(FAKE, FAKE, FAKE), L=(ctypes.c_int32 * 3)(64, 0, 64), B0=True) == relay.OK

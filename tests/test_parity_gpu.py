@@ -601,3 +601,56 @@ def test_tree_prefixes(name, groups, Lp):
         idx = [b for b in range(base.B) if group_of[b] == p]
         T.check(got_o[idx], ref_o[idx], f"out (group {p})")
         T.check(got_l[idx], ref_l[idx], f"lse (group {p})")
+
+
+# ----------------------------------------------------------------------------- shared prefix segments, one unit
+# relay_attention_decode_prefixes: several shared segments (a global prompt
+# and group prompts: a tree of shared prefixes), each request seeing the
+# segments its mask selects, all fused in one streaming kernel and one merge;
+# against the oracle over each request's explicit concatenation [its
+# segments; its context].  Cases: the Llama-2-7B batch with a 2048-token
+# global prompt and four 512-token group prompts; grouped-query heads; three
+# segments with an empty one and requests that see none (pure context, or
+# nothing at all); multi-row requests.
+PREFIX_CASES = [
+    ("llama2_7b", {}, [2048, 512, 512, 512, 512], lambda b: 1 | (2 << (b % 4))),
+    ("tiny_gqa", {}, [256, 40, 40], lambda b: 1 | (2 << (b % 2))),
+    ("tiny", dict(pool_blocks=40), [100, 0, 77], lambda b: [0b101, 0b001, 0b000, 0b110][b]),
+    ("tiny", dict(Lq=3, chunk_requests=2), [64, 130], lambda b: [1, 3, 2, 3][b]),
+]
+
+
+@pytest.mark.parametrize("name,over,lens,mask_of", PREFIX_CASES,
+                         ids=["llama2_7b_global_4groups", "gqa_2groups", "empty_and_unseen", "chunks"])
+def test_prefix_segments(name, over, lens, mask_of):
+    import shared_prompt_decode_gb300 as relay
+    from dataclasses import replace
+    base = synth.make_case(synth.workload(name, **over), 91, ctx_lens=[0, 5, 0, 17] if name == "tiny" and
+                           "pool_blocks" in over else None)
+    gen = torch.Generator().manual_seed(92)
+    segs = [((torch.randn(L, base.Hkv, base.D, generator=gen) * base.wl.value_scale).half(),
+             (torch.randn(L, base.Hkv, base.D, generator=gen) * base.wl.value_scale).half()) for L in lens]
+    masks = [mask_of(b) for b in range(base.B)]
+    g = T.to_dev(base)
+    lse = torch.full((base.B, base.Lq, base.H), float("nan"), dtype=torch.float32, device=T.DEV)
+    out = torch.full_like(g["q"], float("nan"))
+    relay.relay_attention_decode_prefixes(
+        g["q"], [k.to(T.DEV) for k, _ in segs], [v.to(T.DEV) for _, v in segs],
+        torch.tensor(masks, dtype=torch.int32, device=T.DEV), g["k_cache"], g["v_cache"], g["block_tables"],
+        g["ctx_lens"], g["q_lens"], out=out, lse_out=lse, max_q_total=base.total_q() if base.q_lens is not None else 0)
+    torch.cuda.synchronize()
+    got_o, got_l = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    for m in sorted(set(masks)):
+        seen = [i for i in range(len(lens)) if (m >> i) & 1]
+        k = torch.cat([segs[i][0] for i in seen]) if seen else torch.zeros(0, base.Hkv, base.D, dtype=torch.float16)
+        v = torch.cat([segs[i][1] for i in seen]) if seen else torch.zeros(0, base.Hkv, base.D, dtype=torch.float16)
+        flat = replace(base, sys_k=k, sys_v=v)
+        ref_o, ref_l = oracle.attention_full(flat)
+        idx = [b for b in range(base.B) if masks[b] == m]
+        vm = T.valid_mask(base)[idx]
+        T.check(got_o[idx][vm], ref_o[idx][vm], f"out (mask {m:b})")
+        T.check(got_l[idx][vm], ref_l[idx][vm], f"lse (mask {m:b})")
+    # rows past q_lens untouched
+    ql = base.q_lens_list()
+    for b in range(base.B):
+        assert torch.isnan(out[b, ql[b]:].float()).all()
