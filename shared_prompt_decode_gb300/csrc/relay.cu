@@ -32,6 +32,21 @@ struct DevInfo {
     int occ64 = 0, occ128 = 0;
 };
 
+// Streaming-kernel instances: D = 128 has one per row-item class (ROWS =
+// -1: any; 0: none; 1, 2, 4: system items only, in that many key groups), in
+// the multi-head and grouped-query flavours; D = 64 has the general one.
+template <int D, bool GRP, int ROWS>
+cudaError_t prepare_one(int *occ)
+{
+    cudaError_t e = cudaFuncSetAttribute(relay_kernel<D, GRP, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(Smem<D>));
+    int o = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, relay_kernel<D, GRP, ROWS>, kThreads, sizeof(Smem<D>));
+    *occ = std::min(*occ, o);
+    return e;
+}
+
 // Batches with more query rows per head than this run the system step on the
 // tensor cores (tcgen05), where it is compute-bound; below it the step stays
 // inside the streaming kernel, where it is memory-bound and overlaps context.
@@ -42,20 +57,22 @@ std::mutex g_mu;
 template <int D>
 cudaError_t prepare_kernel(int *occ)
 {
-    // both decode flavours (multi-head, grouped-query) use the same shared memory
-    cudaError_t e = cudaFuncSetAttribute(relay_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(Smem<D>));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(relay_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(Smem<D>));
-    if (e != cudaSuccess) return e;
-    int o1 = 0, o2 = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, relay_kernel<D, false>, kThreads, sizeof(Smem<D>));
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, relay_kernel<D, true>, kThreads, sizeof(Smem<D>));
-    *occ = std::min(o1, o2);
+    *occ = 1 << 30;
+    cudaError_t e = prepare_one<D, false, -1>(occ);
+    if (e == cudaSuccess) e = prepare_one<D, true, -1>(occ);
+    if constexpr (D == 128) {
+        if (e == cudaSuccess) e = prepare_one<D, false, 0>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, true, 0>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, false, 1>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, true, 1>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, false, 2>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, true, 2>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, false, 4>(occ);
+        if (e == cudaSuccess) e = prepare_one<D, true, 4>(occ);
+    }
     return e;
 }
+
 
 relay_status_t device_info(const DevInfo **out)
 {
@@ -293,6 +310,30 @@ float scale_log2_of(const relay_dims_t *d)
     return sc * 1.4426950408889634f;
 }
 
+// Key groups of a system tile with `rows` virtual rows (the device's row_roles).
+int key_groups(int rows)
+{
+    const int rg = (rows + 15) / 16;
+    int np2 = 1;
+    while (np2 < rg) np2 <<= 1;
+    return std::min(kRowWarps / np2, kTileK / 8);
+}
+
+// The row-item class of a launch (the ROWS of relay_kernel), -1 unless the
+// shape fixes it: every request has its Lq = 1 row (no q_lens), so there is
+// no multi-row item, and every system tile has the same number of key groups.
+int row_class(const relay_dims_t *d, const Plan &pl, int mode, int G, bool have_q_lens)
+{
+    if (d->D != 128 || have_q_lens || d->Lq != 1) return -1;
+    const bool sys_items = (mode == MODE_FUSED || mode == MODE_SYS) && !pl.tc && pl.R_sys > 0;
+    if (!sys_items) return 0;
+    const int Mv = d->B * G;                          // virtual rows per KV head
+    const int T = (Mv + kTileM - 1) / kTileM;
+    const int kg_last = key_groups(Mv - (T - 1) * kTileM);
+    if (T > 1 && kg_last != key_groups(kTileM)) return -1;
+    return kg_last;
+}
+
 // Shared prefix segments from the caller's host arrays: 1..kMaxSegments
 // segments of >= 0 tokens, [len, Hkv, D] fp16 each, 16-byte aligned.
 relay_status_t make_segments(int n_seg, const void *const *k, const void *const *v, const int32_t *len,
@@ -403,11 +444,33 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
     if (d->D == 128) {
-        if (p.G > 1) relay_kernel<128, true><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
-        else relay_kernel<128, false><<<dev->sms * dev->occ128, kThreads, sizeof(Smem<128>), s>>>(p);
+        const unsigned grid = dev->sms * dev->occ128;
+        constexpr size_t sm = sizeof(Smem<128>);
+        switch (row_class(d, pl, mode, p.G, p.q_lens != nullptr)) {
+        case 0:
+            if (p.G > 1) relay_kernel<128, true, 0><<<grid, kThreads, sm, s>>>(p);
+            else relay_kernel<128, false, 0><<<grid, kThreads, sm, s>>>(p);
+            break;
+        case 1:
+            if (p.G > 1) relay_kernel<128, true, 1><<<grid, kThreads, sm, s>>>(p);
+            else relay_kernel<128, false, 1><<<grid, kThreads, sm, s>>>(p);
+            break;
+        case 2:
+            if (p.G > 1) relay_kernel<128, true, 2><<<grid, kThreads, sm, s>>>(p);
+            else relay_kernel<128, false, 2><<<grid, kThreads, sm, s>>>(p);
+            break;
+        case 4:
+            if (p.G > 1) relay_kernel<128, true, 4><<<grid, kThreads, sm, s>>>(p);
+            else relay_kernel<128, false, 4><<<grid, kThreads, sm, s>>>(p);
+            break;
+        default:
+            if (p.G > 1) relay_kernel<128, true, -1><<<grid, kThreads, sm, s>>>(p);
+            else relay_kernel<128, false, -1><<<grid, kThreads, sm, s>>>(p);
+            break;
+        }
     } else {
-        if (p.G > 1) relay_kernel<64, true><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
-        else relay_kernel<64, false><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+        if (p.G > 1) relay_kernel<64, true, -1><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+        else relay_kernel<64, false, -1><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
 

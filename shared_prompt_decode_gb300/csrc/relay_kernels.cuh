@@ -964,18 +964,25 @@ __device__ __forceinline__ RowRoles row_roles(int rows)
     return r;
 }
 
-template <int D>
+// KGF: 0 = any key-group count (chosen per item); else the only count this
+// kernel instance meets (the host knows it), so that only that pipeline is
+// compiled in.
+template <int D, int KGF>
 __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0, int key_hi, const RowRoles &rr,
                                          const unsigned (&qf)[D / 16][4], RowState<D> &ws, int end0, int end1,
                                          float scale_log2, unsigned *flags)
 {
     const int kpk = kTileK / rr.KG;          // keys per key group
     const int kb = rr.kg * kpk;
-    switch (rr.KG) {
-    case 1: row_pipeline<D, 8>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
-    case 2: row_pipeline<D, 4>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
-    case 4: row_pipeline<D, 2>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
-    default: row_pipeline<D, 1>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+    if constexpr (KGF > 0) {
+        row_pipeline<D, 8 / KGF>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags);
+    } else {
+        switch (rr.KG) {
+        case 1: row_pipeline<D, 8>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+        case 2: row_pipeline<D, 4>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+        case 4: row_pipeline<D, 2>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+        default: row_pipeline<D, 1>(s, src, key0, key_hi, kb, qf, ws, end0, end1, rr.active, scale_log2, flags); break;
+        }
     }
     if (rr.KG == 1) return;
     // combine the key groups' states into the kg == 0 warps (ring is idle now)
@@ -1023,7 +1030,7 @@ __device__ __forceinline__ void run_rows(Smem<D> &s, const KeySrc &src, int key0
 // (multi-head: G = 1, v = r).  Items of a shared prefix segment: every KV
 // head, row tile and key range of it; rows of requests that do not see the
 // segment get no key (their partial has lse = -inf and counts for nothing).
-template <int D>
+template <int D, int KGF>
 __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
 {
     // KV heads vary fastest: CTAs that run concurrently read whole [Hkv, D]
@@ -1069,7 +1076,7 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
         for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
-    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
+    run_rows<D, KGF>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0)
         write_row_partials<D>(p, ws, false, p.seg_part0[seg] + rho, hA, rA, vA < Mv, hB, rB, vB < Mv);
 }
@@ -1118,7 +1125,7 @@ __device__ void mq_item(const Params &p, Smem<D> &s, int local)
         for (int e = 0; e < 4; e++) ws.o[d][e] = 0.f;
     ws.m[0] = ws.m[1] = kNegInf;
     ws.l[0] = ws.l[1] = 0.f;
-    run_rows<D>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
+    run_rows<D, 0>(s, src, key0, key_hi, rr, qf, ws, endA, endB, p.scale_log2, p.ctrl);
     if (rr.active && rr.kg == 0)
         write_row_partials<D>(p, ws, true, split, h, s.qo[b] + iA, iA < ql, h, s.qo[b] + iB, iB < ql);
 }
@@ -1534,8 +1541,15 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 }
 
 // ============================================================================= persistent kernel
-// GRP: decode items serve a group of query heads sharing one KV head (G > 1)
-template <int D, bool GRP>
+// GRP: decode items serve a group of query heads sharing one KV head (G > 1).
+// ROWS: the row items this instance handles.  -1: any (system items of any
+// row count, multi-row context items).  0: none (no system items on this
+// kernel, no multi-row request).  1, 2, 4: system items only, all split into
+// that many key groups (the host knows it from the shape when every request
+// has one query row).  The kernel starts with its code cold, and every
+// pipeline compiled into it costs start-up time whether it runs or not
+// (3.5 us of a 70 us step, measured), hence the instances.
+template <int D, bool GRP, int ROWS>
 __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1562,12 +1576,16 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
 
     // phase 1: row items, two independent row teams per CTA (first items
     // static); a team with no row item starts on decode items at once
-    {
+    if constexpr (ROWS != 0) {
         const int team = team_of();
         const bool leader = (threadIdx.x % kRowThreads) == 0;
         for (int item = blockIdx.x + team * gridDim.x; item < n_rows;) {
-            if (item < n_sys) sys_item<D>(p, s, item, Mtot);
-            else mq_item<D>(p, s, item - n_sys);
+            if constexpr (ROWS > 0) {
+                sys_item<D, ROWS>(p, s, item, Mtot);
+            } else {
+                if (item < n_sys) sys_item<D, 0>(p, s, item, Mtot);
+                else mq_item<D>(p, s, item - n_sys);
+            }
             if (leader) s.item[team] = (int)(kTeams * gridDim.x + atomicAdd(&p.ctrl[CTRL_ROW_ITEMS], 1u));
             team_sync();
             item = s.item[team];
