@@ -487,8 +487,13 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = d->D == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128>, p)
-                                : cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+    // speculative partial-row loads only where the merge is latency-bound:
+    // at most 1024 (row, head) pairs (the extra rows cost L2 bandwidth above)
+    const bool spec = !p.q_lens && warps <= 1024;
+    cudaError_t e;
+    if (d->D == 128) e = spec ? cudaLaunchKernelEx(&cfg, merge_kernel<128, true>, p)
+                              : cudaLaunchKernelEx(&cfg, merge_kernel<128, false>, p);
+    else e = cudaLaunchKernelEx(&cfg, merge_kernel<64, false>, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return RELAY_ERR_CUDA;

@@ -1038,7 +1038,9 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     const int Mv = Mtot * p.G;
     const int T = (Mv + kTileM - 1) / kTileM;
     int seg = 0;
-    while (seg + 1 < p.n_seg && item >= p.Hkv * T * p.seg_R[seg]) item -= p.Hkv * T * p.seg_R[seg++];
+    if (p.n_seg > 1)
+        while (seg + 1 < p.n_seg && item >= p.Hkv * T * p.seg_R[seg]) item -= p.Hkv * T * p.seg_R[seg++];
+    const bool all_see = p.seg_mask == nullptr;
     const int hk = item % p.Hkv;
     const int tau = (item / p.Hkv) % T;
     const int rho = item / (p.Hkv * T);
@@ -1059,12 +1061,12 @@ __device__ void sys_item(const Params &p, Smem<D> &s, int item, int Mtot)
     if (vA < Mv) {
         int b = find_owner(s.qo, p.B, rA);
         qa = p.q + (((size_t)b * p.Lq + (rA - s.qo[b])) * p.H + hA) * D;
-        if ((s.segm[b] >> seg) & 1u) endA = key_hi;
+        if (all_see || ((s.segm[b] >> seg) & 1u)) endA = key_hi;
     }
     if (vB < Mv) {
         int b = find_owner(s.qo, p.B, rB);
         qb = p.q + (((size_t)b * p.Lq + (rB - s.qo[b])) * p.H + hB) * D;
-        if ((s.segm[b] >> seg) & 1u) endB = key_hi;
+        if (all_see || ((s.segm[b] >> seg) & 1u)) endB = key_hi;
     }
     unsigned qf[D / 16][4];
     load_q_rows<D>(qf, qa, qb);     // the query rows are requested before the item's tiles
@@ -1602,8 +1604,11 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
 // ============================================================================= merge kernel
 // One warp per (row, head): combines the row's system partials and context
 // partials.  Launched as a programmatic dependent of relay_kernel: it waits
-// for that grid (and its memory) before reading anything it wrote.
-template <int D>
+// for that grid (and its memory) before reading anything it wrote.  SPEC
+// (small batches without q_lens, where the merge is one L2 round trip after
+// another): the first candidate partial rows are requested together with
+// their log-sum-exps.
+template <int D, bool SPEC>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
 {
     __shared__ int qo[kMaxB + 1];
@@ -1632,13 +1637,75 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
         const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
         const bool dec = p.Lq == 1;
         const int ncand = n_sys + (has_ctx(p.mode) ? (dec ? p.c_dec : p.c_mq) : 0);
+        // The output rows of the first kSpec candidate parts are requested in
+        // the same round trip too (slot k is part k whatever the row's part
+        // count turns out to be), so a row of at most kSpec parts is merged
+        // after one round trip; rows with more take the general path.
+        constexpr int V = D / 32, kSpec = SPEC ? 16 : 0;
+        const int d0 = lane * V;
+        float x[kSpec > 0 ? kSpec : 1][V];
+#pragma unroll
+        for (int k = 0; k < kSpec; k++) {
+            if (k < ncand) {
+                const float *src = p.part_o + part_slot(p, k, n_sys, dec, r, b, h) * D + d0;
+                if constexpr (V == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    x[k][0] = t.x; x[k][1] = t.y;
+                }
+            }
+        }
         float lk = kNegInf;
         if (lane < ncand) lk = __ldcg(p.part_lse + part_slot(p, lane, n_sys, dec, r, b, h));
         const int tps = __ldcg(p.sched);
         const int nc = has_ctx(p.mode) ? __ldg(p.ctx_lens + b) : 0;
         if (tps < 0) return;
         const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
-        merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, dec, true, lk);
+        const int n = n_sys + n_ctx;
+        if (!SPEC || n > kSpec) {
+            merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, dec, true, lk);
+            return;
+        }
+        constexpr float kLn2 = 0.69314718055994531f;
+        if (lane >= n) lk = kNegInf;
+        float M = lk;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float acc[V], W = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; v++) acc[v] = 0.f;
+        if (M != kNegInf) {
+            const float wl = ex2(lk - M);      // lane k: weight of part k (0 past the row's parts)
+#pragma unroll
+            for (int k = 0; k < kSpec; k++) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                if (k < n && w > 0.f) {
+                    W += w;
+#pragma unroll
+                    for (int v = 0; v < V; v++) acc[v] += w * x[k][v];
+                }
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        const float lse = W > 0.f ? (M + lg2(W)) * kLn2 : kNegInf;
+        const size_t orow = (size_t)r * p.H + h;        // row r = b * Lq + i
+        if (p.mode == MODE_FUSED || p.mode == MODE_BASELINE) {
+            __half *dst = p.out + orow * D + d0;
+            if constexpr (V == 4) {
+                *reinterpret_cast<uint2 *>(dst) =
+                    make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+            } else {
+                *reinterpret_cast<unsigned *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+            }
+            if (p.lse_out && lane == 0) p.lse_out[orow] = lse;
+        } else {
+            float *dst = p.o_f32 + orow * D + d0;
+#pragma unroll
+            for (int v = 0; v < V; v++) dst[v] = acc[v] * inv;
+            if (lane == 0) p.lse_f32[orow] = lse;
+        }
         return;
     }
     const int tps = p.sched[0];
