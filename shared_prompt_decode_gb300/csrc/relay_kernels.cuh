@@ -1436,8 +1436,10 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // The first three tickets of every warp are static; later ones come from
-    // the queue, requested one item ahead.  So no warp touches the queue
+    // The first three tickets of every warp are static, in snake order over
+    // the longest-first queue (warp w takes items w, 2 n_w - 1 - w and
+    // 2 n_w + w), so the static rounds give every warp a similar load; later
+    // tickets come from the queue, requested one item ahead.  So no warp touches the queue
     // counter before its first item is done (1216 warps incrementing one
     // address at the same instant hold up the requests behind them).
     const unsigned n_w = gridDim.x * kWarps;
@@ -1452,7 +1454,7 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
         int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
         dec_item<D, GRP>(p, s, id, n_dec, it);
         ++taken;
-        if (taken < kStatic) ticket = taken * n_w + wid;
+        if (taken < kStatic) ticket = (taken & 1) ? (taken + 1) * n_w - 1 - wid : taken * n_w + wid;
         else if (it.id >= 0) request();
     };
 
