@@ -25,6 +25,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kAutoCtxSplit = 512;
 constexpr int kMaxMqParts = 8;         // context splits of a multi-row request, at most
 static_assert(RELAY_MAX_SEGMENTS == kMaxSegments, "segment limit of the header and the kernels");
+static_assert(tc::kPageTC == kBlock, "page size of the tensor-core context path");
 
 struct DevInfo {
     bool ready = false;
@@ -51,6 +52,7 @@ cudaError_t prepare_one(int *occ)
 // tensor cores (tcgen05), where it is compute-bound; below it the step stays
 // inside the streaming kernel, where it is memory-bound and overlaps context.
 constexpr int kTcMinRows = 256;
+constexpr int kTcCtxMinRows = 64;      // rows of a request per KV head (Lq G) for its context on tcgen05
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -161,6 +163,24 @@ bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The paged pool k_cache or v_cache, [num_blocks][Hkv][16][128] fp16, as a
+// 4-D tensor (d, token, head, page) read in {64, 16, 1, 1} boxes (one d-half
+// of one page of one head) with 128-byte swizzle; pages past num_blocks read
+// as zero.
+bool encode_pool_map(CUtensorMap *m, const void *base, int Hkv, int num_blocks)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {128, (cuuint64_t)kBlock, (cuuint64_t)Hkv, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {128 * sizeof(__half), (cuuint64_t)kBlock * 128 * sizeof(__half),
+                                   (cuuint64_t)Hkv * kBlock * 128 * sizeof(__half)};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kBlock, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Shared prefix segments of a call: the system prompt alone (one segment of
 // dims->Ls tokens), or the levels of a tree of shared prefixes.
 struct Segments {
@@ -186,6 +206,9 @@ struct Plan {
     int c_dec = 0, c_mq = 0, mq_split_min = 0, n_prefix = 0;
     int tps_min = 32, tps_max = 32;
     bool tc = false;          // system step on the tensor-core kernel
+    bool ctx_tc = false;      // multi-row requests' own contexts on the tensor-core kernel too
+    int ctx_pairs = 0;        // tile pairs of a request of Lq rows
+    long long n_tc_sys = 0, n_tc_ctx = 0;   // CTAs of the tensor-core grid: system, then context
     size_t dec_base = 0, mq_base = 0, rows = 0;   // partial rows: [system | decode | multi-row] sections
     size_t off_sched = 0, off_part_o = 0, off_part_lse = 0, total = 0;
 };
@@ -231,6 +254,7 @@ Plan make_plan(const relay_dims_t *d, int mode, int sms, const Segments *seg = n
         pl.R_sys = (d->Ls + range - 1) / range;
         pl.seg_range[0] = range;
         pl.seg_R[0] = pl.R_sys;
+        pl.n_tc_sys = n * pl.R_sys;
     } else if (sys) {
         const Segments one = one_segment(d, nullptr, nullptr);
         const Segments &sg = seg ? *seg : one;
@@ -284,9 +308,26 @@ Plan make_plan(const relay_dims_t *d, int mode, int sms, const Segments *seg = n
         pl.c_dec = std::max(1, (max_pages + pl.tps_min - 1) / pl.tps_min);
         const long long max_keys = (long long)pl.n_prefix + (long long)d->max_blocks_per_seq * kBlock;
         pl.mq_split_min = (int)((max_keys + kMaxMqParts - 1) / kMaxMqParts);
+        // Requests of at least kTcCtxMinRows virtual rows per KV head take
+        // their own context on the tensor cores, one split over all of it,
+        // in the same grid as the system step (after its CTAs).
+        pl.ctx_tc = d->D == 128 && pl.n_prefix == 0 && d->Lq > 1 && (long long)d->Lq * G >= kTcCtxMinRows &&
+                    d->num_blocks > 0 && d->max_blocks_per_seq > 0 && d->max_blocks_per_seq <= tc::kMaxPagesTC;
+        if (pl.ctx_tc) {
+            pl.mq_split_min = (int)max_keys;
+            pl.ctx_pairs = tc_pairs(d->Lq * G);
+            // items (request, tile pair): a request of q > 1 rows holds
+            // ceil(q G / 256) < q G / 256 + 1 pairs, and at most
+            // min(B, max_q_total / 2) requests have more than one row
+            const long long n_mr = std::min<long long>(d->B, pl.Mtot / 2);
+            const long long items =
+                std::min((long long)d->B * pl.ctx_pairs, n_mr + ((long long)pl.Mtot * G + 255) / 256);
+            pl.n_tc_ctx = items * kv_heads(d);
+        }
         pl.mq_split_min = round_up(std::max(pl.mq_split_min, 1), pl.ctx_split);
         // multi-row requests exist only when a request may carry several rows
         pl.c_mq = d->Lq > 1 ? std::max(1, (int)((max_keys + pl.mq_split_min - 1) / pl.mq_split_min)) : 0;
+        if (pl.ctx_tc) pl.c_mq = 1;
     }
     const size_t sys_rows = (size_t)(sys ? pl.R_sys : 0) * pl.Mtot * d->H;
     const size_t dec_rows = (size_t)(ctx ? pl.c_dec : 0) * d->B * d->H;
@@ -324,9 +365,13 @@ int key_groups(int rows)
 // no multi-row item, and every system tile has the same number of key groups.
 int row_class(const relay_dims_t *d, const Plan &pl, int mode, int G, bool have_q_lens)
 {
-    if (d->D != 128 || have_q_lens || d->Lq != 1) return -1;
+    if (d->D != 128) return -1;
     const bool sys_items = (mode == MODE_FUSED || mode == MODE_SYS) && !pl.tc && pl.R_sys > 0;
-    if (!sys_items) return 0;
+    // multi-row context items: requests of several rows whose contexts are
+    // not on the tensor cores
+    const bool mq_items = mode != MODE_SYS && d->Lq > 1 && !pl.ctx_tc;
+    if (!sys_items && !mq_items) return 0;
+    if (have_q_lens || d->Lq != 1) return -1;
     const int Mv = d->B * G;                          // virtual rows per KV head
     const int T = (Mv + kTileM - 1) / kTileM;
     const int kg_last = key_groups(Mv - (T - 1) * kTileM);
@@ -401,6 +446,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.dec_base = (long long)pl.dec_base;
     p.mq_base = (long long)pl.mq_base;
     p.skip_sys = pl.tc ? 1 : 0;
+    p.skip_mq = pl.ctx_tc ? 1 : 0;
     p.mode = mode;
     {
         const Segments one = one_segment(d, p.sys_k, p.sys_v);
@@ -417,8 +463,10 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.tc) {
-        // system partials from the tensor cores: one CTA per (head, tile, range)
+    if (pl.n_tc_sys + pl.n_tc_ctx > 0) {
+        // tensor cores: system partials, one CTA per (range, head, tile
+        // pair), then the multi-row requests' context partials, one CTA per
+        // (request, tile pair, head)
         tc::TcParams t{};
         t.B = d->B;
         t.Lq = d->Lq;
@@ -436,11 +484,24 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.R = pl.R_sys;
         t.range = pl.sys_range;
         t.pairs = tc_pairs(pl.Mtot * p.G);
-        CUtensorMap tmK, tmV;
-        if (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls))
+        t.n_sys = (int)pl.n_tc_sys;
+        t.ctx_pairs = pl.ctx_pairs;
+        t.ctx_lens = mode == MODE_SYS ? nullptr : p.ctx_lens;
+        t.block_tables = p.block_tables;
+        t.max_blocks = d->max_blocks_per_seq;
+        t.num_blocks = d->num_blocks;
+        t.mq_base = (long long)pl.mq_base;
+        CUtensorMap tmK{}, tmV{}, tmKc{}, tmVc{};
+        if (pl.tc && (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls)))
             return RELAY_ERR_CUDA;
-        const long long items = (long long)t.pairs * p.Hkv * pl.R_sys;
-        tc::sys_tc_kernel<false><<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, t);
+        if (pl.ctx_tc) {
+            if (!p.k_cache || !p.v_cache || !p.block_tables || !p.ctx_lens) return RELAY_ERR_INVALID_ARG;
+            if (!encode_pool_map(&tmKc, p.k_cache, p.Hkv, d->num_blocks) ||
+                !encode_pool_map(&tmVc, p.v_cache, p.Hkv, d->num_blocks))
+                return RELAY_ERR_CUDA;
+        }
+        tc::sys_tc_kernel<false><<<(unsigned)(pl.n_tc_sys + pl.n_tc_ctx), tc::kThreadsTC, tc::kSmemTC, s>>>(
+            tmK, tmV, tmKc, tmVc, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
     if (d->D == 128) {
@@ -822,7 +883,7 @@ relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, co
         return RELAY_ERR_CUDA;
     const long long items = (long long)t.pairs * t.Hkv;
     tc::sys_tc_kernel<true><<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tmK, tmV, t);
+        tmK, tmV, tmK, tmV, t);
     return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
 }
 

@@ -99,6 +99,7 @@ struct Params {
     int mq_split_min;                 // keys per split of a multi-row request: at least this
     long long dec_base, mq_base;      // first partial row of the decode and multi-row sections
     int skip_sys;                     // system partials come from the tensor-core kernel
+    int skip_mq;                      // so do the multi-row requests' context partials (one split each)
     int mode;
     // Shared prefix segments, each read once per batch: the system prompt
     // (one segment), or the levels of a tree of shared prefixes.  Request b
@@ -1575,7 +1576,7 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     int n_sys = 0;                                         // system items of every segment
     if (has_sys(p.mode) && !p.skip_sys)
         for (int sg = 0; sg < p.n_seg; sg++) n_sys += p.Hkv * T * p.seg_R[sg];
-    const int n_rows = n_sys + s.mq[p.B];
+    const int n_rows = n_sys + (p.skip_mq ? 0 : s.mq[p.B]);
     const int n_dec = s.dec[s.n_dec_req];
 
     // phase 1: row items, two independent row teams per CTA (first items

@@ -52,6 +52,8 @@ namespace tc {
 
 constexpr int kRowsTC = 128;          // query rows per tile (TMEM lanes)
 constexpr int kKeysTC = 64;           // keys per K/V stage
+constexpr int kPageTC = 16;           // tokens per page of the paged pool
+constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
 constexpr int kStagesK = 3, kStagesV = 2;   // V stage j % 2 is freed by the O-done barrier of PV(j)
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
@@ -161,6 +163,16 @@ __device__ __forceinline__ void tma_load_3d(unsigned dst, const CUtensorMap *tm,
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3, %4}], [%5];\n"
                  ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+                 : "memory");
+}
+
+// TMA: one box of a 4-D tensor map at coordinates (x, y, z, w) into shared memory.
+__device__ __forceinline__ void tma_load_4d(unsigned dst, const CUtensorMap *tm, int x, int y, int z, int w,
+                                            unsigned bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];\n"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
                  : "memory");
 }
 
@@ -298,7 +310,18 @@ struct TcParams {
     int Hkv;                         // KV heads
     __half *out;                     // prefill: [Ls][H][128] fp16 output
     float *lse_out;                  // prefill: [Ls][H] natural-log LSE (nullable)
+    // context CTAs, the grid's CTAs from n_sys on: the query rows of the
+    // requests with several rows against their own paged context
+    int n_sys;                       // system CTAs at the front of the grid
+    int ctx_pairs;                   // tile pairs of a request of Lq rows, ceil(ceil(Lq * G / 128) / 2)
+    const int *ctx_lens;             // [B] context lengths (null: no context, system step only)
+    const int *block_tables;         // [B][max_blocks] page ids
+    int max_blocks, num_blocks;
+    long long mq_base;               // partial row of compact row r, head h: mq_base + r * H + h
 };
+
+// tile pairs for Mv virtual rows
+__device__ __forceinline__ int tile_pairs(int Mv) { return ((Mv + kRowsTC - 1) / kRowsTC + 1) / 2; }
 
 __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 {
@@ -319,6 +342,19 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 // sys_k / sys_v as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box
 // and 128-byte swizzle.
 //
+// Context CTAs (decode step, blockIdx.x >= n_sys, after every system CTA so
+// that they fill the last system wave): the rows of one request b with
+// several query rows (q_lens[b] > 1) against the request's own context, one
+// pair of its row tiles, one KV head: blockIdx.x - n_sys = item * Hkv + hk,
+// items in request order and, within a request, latest tile pair first (the
+// longest).  Row i of the request (0 <= i < q_lens[b]) sees context keys
+// below max(0, ctx_lens[b] - q_lens[b] + 1 + i): the chunk's own keys are in
+// the context already, causally.  tmKc / tmVc view k_cache / v_cache as
+// [num_blocks][Hkv][16][128] fp16 with a {64 d, 16 tokens, 1, 1} box: a
+// 64-key stage is four page boxes per d-half, page ids from block_tables
+// staged in shared memory; a page past the context reads page id
+// num_blocks, out of range, so the copy fills it with zeros.
+//
 // PREFILL: causal self-attention of the system prompt itself (its Ls query
 // rows, in q = [Ls][H][128]; row t sees system keys 0..t), one key range:
 // a CTA streams keys up to its last row's position, masks per row on the
@@ -326,10 +362,13 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 // writes the final fp16 output and natural-log LSE instead of partials.
 template <bool PREFILL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-    sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const TcParams p)
+    sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc, const TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     __shared__ int qo[513];
+    __shared__ int blk_sh[kMaxPagesTC];
+    __shared__ int item_sh[4];
     __shared__ unsigned tmem_base_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -338,32 +377,90 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     unsigned char *gbase = smem_raw + (sbase - sraw);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (unsigned)i; };
     volatile int *abort_p = &abort_sh;
+    const bool ctx = !PREFILL && (int)blockIdx.x >= p.n_sys;
 
-    // rows of the batch: prefix of q_lens (B <= 512)
-    if (PREFILL) {
-    } else if (p.q_lens) {
-        if (tid == 0) {
-            int acc = 0;
-            for (int b = 0; b < p.B; b++) { qo[b] = acc; acc += p.q_lens[b]; }
-            qo[p.B] = acc;
+    // Rows of the batch: the prefix qo of q_lens (B <= 512), with the
+    // streaming kernel's reading of bad lengths (a q_lens[b] outside [0, Lq]
+    // or a ctx_lens[b] outside [0, 16 max_blocks] makes the request empty;
+    // that kernel raises the flag), so that both number the rows alike.  A
+    // context CTA also finds its item: (request, tile pair, rows, context).
+    if (!PREFILL && warp == 0) {
+        const int it_want = ctx ? ((int)blockIdx.x - p.n_sys) / p.Hkv : -1;
+        if (lane == 0) item_sh[0] = -1;
+        __syncwarp();
+        if (p.q_lens) {
+            int run_q = 0, run_i = 0;
+            for (int b0 = 0; b0 < p.B; b0 += 32) {
+                const int b = b0 + lane;
+                int ql = 0, n = 0;
+                if (b < p.B) {
+                    ql = p.q_lens[b];
+                    n = p.ctx_lens ? p.ctx_lens[b] : 0;
+                    if (ql < 0 || ql > p.Lq) ql = 0;
+                    if (n < 0 || n > p.max_blocks * kPageTC) { ql = 0; n = 0; }
+                }
+                const int it = (ctx && ql > 1) ? tile_pairs(ql * p.G) : 0;
+                const int iq = warp_incl_scan(ql), ii = warp_incl_scan(it);
+                if (b < p.B) qo[b] = run_q + iq - ql;
+                const int first = run_i + ii - it;
+                if (it_want >= first && it_want < first + it) {
+                    item_sh[0] = b;
+                    item_sh[1] = it - 1 - (it_want - first);   // latest tile pair first
+                    item_sh[2] = ql;
+                    item_sh[3] = n;
+                }
+                run_q += __shfl_sync(0xffffffffu, iq, 31);
+                run_i += __shfl_sync(0xffffffffu, ii, 31);
+            }
+            if (lane == 0) qo[p.B] = run_q;
+        } else {
+            for (int b = lane; b <= p.B; b += 32) qo[b] = b * p.Lq;
+            if (ctx && lane == 0 && p.ctx_pairs > 0) {
+                const int b = it_want / p.ctx_pairs;
+                int n = b < p.B && p.ctx_lens ? p.ctx_lens[b] : 0;
+                if (b < p.B && n >= 0 && n <= p.max_blocks * kPageTC && p.Lq > 1) {
+                    item_sh[0] = b;
+                    item_sh[1] = p.ctx_pairs - 1 - it_want % p.ctx_pairs;
+                    item_sh[2] = p.Lq;
+                    item_sh[3] = n;
+                }
+            }
         }
-    } else {
-        for (int b = tid; b <= p.B; b += kThreadsTC) qo[b] = b * p.Lq;
     }
     if (tid == 0) abort_sh = 0;
     __syncthreads();
-    const int Mtot = PREFILL ? p.Ls : min(qo[p.B], p.max_q_total);
-    const int Mv = Mtot * p.G;                       // virtual rows of a KV head
+    int hk, pair, rho = 0, Mv;
+    int cb = 0, cql = 0, cn = 0;                     // context CTA: request, its rows, its context length
+    if (PREFILL) {
+        Mv = p.Ls * p.G;
+        hk = blockIdx.x % p.Hkv;
+        pair = p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs;
+    } else if (!ctx) {
+        Mv = min(qo[p.B], p.max_q_total) * p.G;      // virtual rows of a KV head
+        hk = (blockIdx.x / p.pairs) % p.Hkv;
+        pair = blockIdx.x % p.pairs;
+        rho = blockIdx.x / (p.Hkv * p.pairs);
+    } else {
+        cb = item_sh[0];
+        if (cb < 0) return;                          // no such item: the whole CTA leaves together
+        hk = ((int)blockIdx.x - p.n_sys) % p.Hkv;
+        pair = item_sh[1];
+        cql = item_sh[2];
+        cn = item_sh[3];
+        Mv = cql * p.G;
+    }
     const int T = (Mv + kRowsTC - 1) / kRowsTC;
-    const int hk = PREFILL ? blockIdx.x % p.Hkv : (blockIdx.x / p.pairs) % p.Hkv;
-    const int pair = PREFILL ? p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs : blockIdx.x % p.pairs;
-    const int rho = blockIdx.x / (p.Hkv * p.pairs);
-    if (2 * pair >= T || rho >= p.R) return;        // the whole CTA leaves together
+    if (2 * pair >= T || (!ctx && rho >= p.R)) return;   // the whole CTA leaves together
     const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
-    const int key0 = PREFILL ? 0 : rho * p.range;
-    // prefill: every key up to the position of the CTA's last row
-    const int key_hi = PREFILL ? (min(Mv, (2 * pair + n_act) * kRowsTC) - 1) / p.G + 1 : min(key0 + p.range, p.Ls);
+    const int v_last = min(Mv, (2 * pair + n_act) * kRowsTC) - 1;   // the CTA's last virtual row
+    const int key0 = (PREFILL || ctx) ? 0 : rho * p.range;
+    // prefill: every key up to the position of the CTA's last row; context:
+    // every key its last row sees
+    const int key_hi = PREFILL ? v_last / p.G + 1
+                     : ctx     ? min(max(cn - cql + 1 + v_last / p.G, 0), cn)
+                               : min(key0 + p.range, p.Ls);
     const int n_tiles = key_hi > key0 ? (key_hi - key0 + kKeysTC - 1) / kKeysTC : 0;
+    const int n_pages = ctx ? (key_hi + kPageTC - 1) / kPageTC : 0;   // context pages read
 
     if (warp == kWarpMmaS) {
         const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(&tmem_base_sh));
@@ -402,14 +499,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int row = tid & 127;
         const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
         const int tile = 2 * pair + wg;
-        const int v = tile * kRowsTC + row;              // virtual row: query row r, query head h
-        const bool row_ok = wg < n_act && v < Mv;
-        const int r = v / p.G, h = hk * p.G + v % p.G;
+        // virtual row: query row r (context CTA: row i of request cb, compact
+        // row r), query head h
+        const int v = tile * kRowsTC + row;
+        const int i_ctx = v / p.G;
+        const int r = ctx ? qo[cb] + i_ctx : v / p.G, h = hk * p.G + v % p.G;
+        const bool row_ok = wg < n_act && v < Mv && (!ctx || r < p.max_q_total);
+        // context keys this row sees: below lim_ctx
+        const int lim_ctx = min(max(cn - cql + 1 + i_ctx, 0), cn);
         {
             // this row's query into the K-major, 128-byte-swizzled Q tile
             const __half *qrow = p.q;
             if (row_ok && PREFILL) {
                 qrow = p.q + ((size_t)r * p.H + h) * 128;
+            } else if (row_ok && ctx) {
+                qrow = p.q + (((size_t)cb * p.Lq + i_ctx) * p.H + h) * 128;
             } else if (row_ok) {
                 const int b = owner_of(qo, p.B, r);
                 qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
@@ -447,7 +551,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                 }
                 const int kbase = key0 + j * kKeysTC;
-                const int lim = PREFILL ? r + 1 : key_hi;     // keys visible to this row: below lim
+                // keys visible to this row: below lim
+                const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
                 if (kbase + kKeysTC > lim) {
 #pragma unroll
                     for (int i = 0; i < 64; i++)
@@ -524,6 +629,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (ok && j + 2 < n_tiles)
                     ok = mbar_wait(bar(kBarKFull + (j + 2) % kStagesK), ((j + 2) / kStagesK) & 1, abort_p);
                 if (!__all_sync(0xffffffffu, ok)) break;
+                if (ctx && wg == 0 && j == n_tiles - 1 && cn < n_pages * kPageTC) {
+                    // the last page's slots past the context hold whatever the
+                    // pool holds there: zero their V rows (P is 0 on them, and
+                    // 0 times a NaN would not be)
+                    const int lo = cn - kbase, cnt = (n_pages * kPageTC - cn) * 16;   // 16-byte chunks
+                    unsigned char *vs = gbase + kOffV + (j % kStagesV) * kStageBytes;
+                    for (int c = row; c < cnt; c += kRowsTC)
+                        *reinterpret_cast<uint4 *>(vs + ((c >> 3) & 1) * kHalfKV + (lo + (c >> 4)) * 128 +
+                                                   (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    fence_async_smem();
+                }
                 tc_fence_before();   // S(j) loads (and a rescale's stores) before the MMAs that follow
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarReady + b));
@@ -536,7 +652,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             fin = __all_sync(0xffffffffu, fin);
             tc_fence_after();
             if (!fin && lane == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
-            const size_t prow = PREFILL ? (size_t)r * p.H + h : ((size_t)rho * p.max_q_total + r) * p.H + h;
+            const size_t prow = PREFILL ? (size_t)r * p.H + h
+                              : ctx     ? (size_t)p.mq_base + (size_t)r * p.H + h
+                                        : ((size_t)rho * p.max_q_total + r) * p.H + h;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int q4 = 0; q4 < 4; q4++) {
@@ -576,6 +694,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // ------------------------------------------------------------ TMA producer
         // K runs up to kStagesK stages ahead and V up to kStagesV, each as
         // soon as its ring has room (polled, so neither ring holds up the other)
+        bool bad_blk = false;
+        if (ctx) {
+            // the request's page ids, checked: an id outside [0, num_blocks)
+            // raises the flag and reads as zeros
+            const int *bt = p.block_tables + (size_t)cb * p.max_blocks;
+            for (int i = lane; i < n_pages; i += 32) {
+                int blk = bt[i];
+                if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                    bad_blk = true;
+                    blk = p.num_blocks;
+                }
+                blk_sh[i] = blk;
+            }
+            __syncwarp();
+            if (__any_sync(0xffffffffu, bad_blk) && lane == 0) atomicOr(p.flags, RELAY_FLAG_BAD_BLOCK);
+        }
+        // four page boxes per d-half of a context stage (pages past the
+        // context: page id num_blocks, zero fill)
+        auto load_ctx = [&](unsigned dst, const CUtensorMap *tm, int j, unsigned mb) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) {
+                const int pg = 4 * j + q4;
+                const int blk = pg < n_pages ? blk_sh[pg] : p.num_blocks;
+                tma_load_4d(dst + q4 * (kPageTC * 128), tm, 0, 0, hk, blk, mb);
+                tma_load_4d(dst + kHalfKV + q4 * (kPageTC * 128), tm, 64, 0, hk, blk, mb);
+            }
+        };
         if (lane == 0) {
             int jk = 0, jv = 0;
             unsigned long long t_last = global_ns();
@@ -585,8 +730,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     (jk < kStagesK || mbar_test(bar(kBarKEmpty + jk % kStagesK), ((jk / kStagesK) - 1) & 1))) {
                     const int s = jk % kStagesK, z = key0 + jk * kKeysTC;
                     mbar_expect_tx(bar(kBarKFull + s), kStageBytes);
-                    tma_load_3d(kstage(s), &tmK, 0, hk, z, bar(kBarKFull + s));
-                    tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, hk, z, bar(kBarKFull + s));
+                    if (ctx) {
+                        load_ctx(kstage(s), &tmKc, jk, bar(kBarKFull + s));
+                    } else {
+                        tma_load_3d(kstage(s), &tmK, 0, hk, z, bar(kBarKFull + s));
+                        tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, hk, z, bar(kBarKFull + s));
+                    }
                     jk++;
                     progress = true;
                 }
@@ -594,8 +743,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
                     const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
                     mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
-                    tma_load_3d(vstage(s), &tmV, 0, hk, z, bar(kBarVFull + s));
-                    tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, hk, z, bar(kBarVFull + s));
+                    if (ctx) {
+                        load_ctx(vstage(s), &tmVc, jv, bar(kBarVFull + s));
+                    } else {
+                        tma_load_3d(vstage(s), &tmV, 0, hk, z, bar(kBarVFull + s));
+                        tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, hk, z, bar(kBarVFull + s));
+                    }
                     jv++;
                     progress = true;
                 }

@@ -356,6 +356,52 @@ def test_tensor_core_system_step(name, B, Lq, Ls, ql):
     T.check_full(case, out2, lse2)
 
 
+# ----------------------------------------------------------------------------- chunk rows' own contexts on tcgen05
+# Requests of Lq * G >= 64 virtual rows per KV head take their own context on
+# the tensor-core kernel, in the grid of the system step: paged copies (four
+# 16-token page boxes per 64-key stage), a causal limit per row, and the V
+# slots past the context zeroed (the pool's unused slots hold NaN).  Long and
+# ragged contexts, two tile pairs of one request (300 rows), contexts shorter
+# than the chunk (rows that see no context key), one-row and empty requests
+# beside them, grouped-query heads, and every request at Lq rows (no q_lens).
+CTX_TC_CASES = [
+    ("mha_pairs", dict(B=6, H=2, Lq=300, Ls=200), [300, 1, 129, 64, 0, 2], [1500, 700, 129, 3000, 50, 1]),
+    ("gqa", dict(B=4, H=8, Hkv=2, Lq=40, Ls=130), [40, 1, 17, 33], [2000, 300, 17, 999]),
+    ("all_rows", dict(B=3, H=2, Lq=64, Ls=64), None, [64, 1000, 333]),
+]
+
+
+@pytest.mark.parametrize("name,over,ql,ctx", CTX_TC_CASES, ids=[c[0] for c in CTX_TC_CASES])
+def test_chunk_context_on_tensor_cores(name, over, ql, ctx):
+    w = synth.Workload(name, D=128, ctx_dist=("uniform", 1, 2), value_scale=0.5, **over)
+    case = synth.make_case(w, 37, ctx_lens=ctx, q_lens=ql)
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+    *_, out2, lse2 = T.run_split(case)
+    T.check_full(case, out2, lse2)
+
+
+def test_chunk_context_bad_block_is_flagged():
+    # a page id outside the pool in a chunk request's context: read as zeros
+    # and flagged; the next clean call in the same workspace is exact
+    import shared_prompt_decode_gb300 as relay
+    w = synth.Workload("ctx_bad", B=3, H=2, D=128, Ls=64, ctx_dist=("uniform", 1, 2), value_scale=0.5, Lq=64)
+    case = synth.make_case(w, 41, ctx_lens=[100, 1, 200], q_lens=[64, 1, 64])
+    g = T.to_dev(case)
+    dims = relay.make_dims(g["q"], case.Ls, case.num_blocks, case.max_blocks, max_q_total=case.total_q())
+    ws = relay.make_workspace(dims)
+    bad = dict(g, block_tables=g["block_tables"].clone())
+    bad["block_tables"][2, 3] = case.num_blocks + 5
+    out = torch.zeros_like(g["q"])
+    relay.relay_attention_decode(bad["q"], bad["sys_k"], bad["sys_v"], bad["k_cache"], bad["v_cache"],
+                                 bad["block_tables"], bad["ctx_lens"], bad["q_lens"], out=out, workspace=ws,
+                                 dims=dims)
+    assert relay.device_status(ws) & relay.FLAG_BAD_BLOCK
+    out, lse = T.run_fused(case, ws=ws, g=g)
+    assert relay.device_status(ws) == 0
+    T.check_full(case, out, lse)
+
+
 # ----------------------------------------------------------------------------- grouped-query heads
 # Hkv KV heads serve H query heads (query head h reads KV head h / (H / Hkv)):
 # every path -- one call, the three separate steps, the non-relay baseline,
