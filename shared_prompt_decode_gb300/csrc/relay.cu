@@ -26,6 +26,7 @@ constexpr int kAutoCtxSplit = 512;
 constexpr int kMaxMqParts = 8;         // context splits of a multi-row request, at most
 static_assert(RELAY_MAX_SEGMENTS == kMaxSegments, "segment limit of the header and the kernels");
 static_assert(tc::kPageTC == kBlock, "page size of the tensor-core context path");
+static_assert(tc::kMaxBatchTC == kMaxB, "batch limit of the tensor-core kernel");
 
 struct DevInfo {
     bool ready = false;
@@ -53,6 +54,7 @@ cudaError_t prepare_one(int *occ)
 // inside the streaming kernel, where it is memory-bound and overlaps context.
 constexpr int kTcMinRows = 256;
 constexpr int kTcCtxMinRows = 64;      // rows of a request per KV head (Lq G) for its context on tcgen05
+constexpr int kTcYieldPct = 13;        // share of the SMs that stream decode contexts beside the tensor cores
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -129,6 +131,16 @@ relay_status_t check_dims(const relay_dims_t *d)
 }
 
 int tc_pairs(int Mtot) { return ((Mtot + tc::kRowsTC - 1) / tc::kRowsTC + 1) / 2; }
+
+// CTAs of a tensor-core grid of `grid` CTAs that hand their SMs to the
+// streaming kernel when the batch has decode requests (the device decides
+// whether it has): kTcYieldPct of the SMs stream, counting those the grid
+// leaves free anyway; at least one CTA stays.
+int tc_yield(int sms, int grid)
+{
+    const int want = (sms * kTcYieldPct + 50) / 100 - (sms - grid);
+    return std::max(0, std::min(want, grid - 1));
+}
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (the library links only the CUDA runtime).
@@ -447,6 +459,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
     p.mq_base = (long long)pl.mq_base;
     p.skip_sys = pl.tc ? 1 : 0;
     p.skip_mq = pl.ctx_tc ? 1 : 0;
+    p.dec_static = (pl.n_tc_sys + pl.n_tc_ctx > 0 || d->B > 32) ? 0 : 3;
     p.mode = mode;
     {
         const Segments one = one_segment(d, p.sys_k, p.sys_v);
@@ -491,6 +504,7 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         t.max_blocks = d->max_blocks_per_seq;
         t.num_blocks = d->num_blocks;
         t.mq_base = (long long)pl.mq_base;
+        t.queue = p.ctrl + CTRL_TC_QUEUE;
         CUtensorMap tmK{}, tmV{}, tmKc{}, tmVc{};
         if (pl.tc && (!encode_sys_map(&tmK, p.sys_k, p.Hkv, d->Ls) || !encode_sys_map(&tmV, p.sys_v, p.Hkv, d->Ls)))
             return RELAY_ERR_CUDA;
@@ -500,40 +514,52 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
                 !encode_pool_map(&tmVc, p.v_cache, p.Hkv, d->num_blocks))
                 return RELAY_ERR_CUDA;
         }
-        tc::sys_tc_kernel<false><<<(unsigned)(pl.n_tc_sys + pl.n_tc_ctx), tc::kThreadsTC, tc::kSmemTC, s>>>(
-            tmK, tmV, tmKc, tmVc, t);
+        // persistent: one CTA per SM at most
+        const long long tc_grid = std::min<long long>(pl.n_tc_sys + pl.n_tc_ctx, dev->sms);
+        t.n_yield = tc_yield(dev->sms, (int)tc_grid);
+        tc::sys_tc_kernel<false><<<(unsigned)tc_grid, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, tmKc, tmVc, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }
-    if (d->D == 128) {
-        const unsigned grid = dev->sms * dev->occ128;
-        constexpr size_t sm = sizeof(Smem<128>);
-        switch (row_class(d, pl, mode, p.G, p.q_lens != nullptr)) {
-        case 0:
-            if (p.G > 1) relay_kernel<128, true, 0><<<grid, kThreads, sm, s>>>(p);
-            else relay_kernel<128, false, 0><<<grid, kThreads, sm, s>>>(p);
-            break;
-        case 1:
-            if (p.G > 1) relay_kernel<128, true, 1><<<grid, kThreads, sm, s>>>(p);
-            else relay_kernel<128, false, 1><<<grid, kThreads, sm, s>>>(p);
-            break;
-        case 2:
-            if (p.G > 1) relay_kernel<128, true, 2><<<grid, kThreads, sm, s>>>(p);
-            else relay_kernel<128, false, 2><<<grid, kThreads, sm, s>>>(p);
-            break;
-        case 4:
-            if (p.G > 1) relay_kernel<128, true, 4><<<grid, kThreads, sm, s>>>(p);
-            else relay_kernel<128, false, 4><<<grid, kThreads, sm, s>>>(p);
-            break;
-        default:
-            if (p.G > 1) relay_kernel<128, true, -1><<<grid, kThreads, sm, s>>>(p);
-            else relay_kernel<128, false, -1><<<grid, kThreads, sm, s>>>(p);
-            break;
+    {
+        // the streaming kernel's instance for this shape
+        void (*fn)(const Params) = nullptr;
+        unsigned grid = 0;
+        size_t smem = 0;
+        const bool grp = p.G > 1;
+        if (d->D == 128) {
+            grid = dev->sms * dev->occ128;
+            smem = sizeof(Smem<128>);
+            switch (row_class(d, pl, mode, p.G, p.q_lens != nullptr)) {
+            case 0: fn = grp ? relay_kernel<128, true, 0> : relay_kernel<128, false, 0>; break;
+            case 1: fn = grp ? relay_kernel<128, true, 1> : relay_kernel<128, false, 1>; break;
+            case 2: fn = grp ? relay_kernel<128, true, 2> : relay_kernel<128, false, 2>; break;
+            case 4: fn = grp ? relay_kernel<128, true, 4> : relay_kernel<128, false, 4>; break;
+            default: fn = grp ? relay_kernel<128, true, -1> : relay_kernel<128, false, -1>; break;
+            }
+        } else {
+            grid = dev->sms * dev->occ64;
+            smem = sizeof(Smem<64>);
+            fn = grp ? relay_kernel<64, true, -1> : relay_kernel<64, false, -1>;
         }
-    } else {
-        if (p.G > 1) relay_kernel<64, true, -1><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
-        else relay_kernel<64, false, -1><<<dev->sms * dev->occ64, kThreads, sizeof(Smem<64>), s>>>(p);
+        // behind the tensor-core grid, a programmatic dependent of it: it
+        // starts on the SMs that grid's last wave frees
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        if (pl.n_tc_sys + pl.n_tc_ctx > 0) {
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+            cudaGetLastError();
+            return RELAY_ERR_CUDA;
+        }
     }
-    if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
 
     // merge kernel: one warp per (row, head), launched as a programmatic
     // dependent so that its launch overlaps the first kernel's tail
@@ -881,8 +907,8 @@ relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, co
     CUtensorMap tmK, tmV;
     if (!encode_sys_map(&tmK, sys_k, t.Hkv, dims->Ls) || !encode_sys_map(&tmV, sys_v, t.Hkv, dims->Ls))
         return RELAY_ERR_CUDA;
-    const long long items = (long long)t.pairs * t.Hkv;
-    tc::sys_tc_kernel<true><<<(unsigned)items, tc::kThreadsTC, tc::kSmemTC, reinterpret_cast<cudaStream_t>(stream)>>>(
+    const long long grid = std::min<long long>((long long)t.pairs * t.Hkv, dev->sms);
+    tc::sys_tc_kernel<true><<<(unsigned)grid, tc::kThreadsTC, tc::kSmemTC, reinterpret_cast<cudaStream_t>(stream)>>>(
         tmK, tmV, tmK, tmV, t);
     return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
 }

@@ -74,7 +74,7 @@ enum : unsigned {
 };
 
 // ctrl words in the workspace
-enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DEC_ITEMS = 3 };
+enum { CTRL_FLAGS = 0, CTRL_ROW_ITEMS = 1, CTRL_DEC_ITEMS = 3, CTRL_TC_QUEUE = 4 /* and 5 */ };
 
 struct Params {
     int B, Lq, H, Ls, num_blocks, max_blocks, max_q_total;
@@ -100,6 +100,7 @@ struct Params {
     long long dec_base, mq_base;      // first partial row of the decode and multi-row sections
     int skip_sys;                     // system partials come from the tensor-core kernel
     int skip_mq;                      // so do the multi-row requests' context partials (one split each)
+    int dec_static;                   // static decode tickets per warp before the queue (0 or 3)
     int mode;
     // Shared prefix segments, each read once per batch: the system prompt
     // (one segment), or the levels of a tree of shared prefixes.  Request b
@@ -593,16 +594,20 @@ __device__ __forceinline__ size_t part_slot(const Params &p, int j, int n_sys, b
 // their softmax mass.  One warp; lane k loads the log-sum-exp of part k (one
 // round trip), then the parts' output rows are loaded eight at a time with
 // all eight loads in flight together.  Lane t handles D/32 adjacent elements.
-template <int D>
+template <int D, int CH = 16>   // CH: partial rows in flight per lane (one round for up to CH partials)
 __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx, bool dec,
                           bool have_lk0 = false, float lk0 = 0.f)
 {
     constexpr int V = D / 32;
-    constexpr int CH = 16;     // partial rows in flight per lane (one round for up to 16 partials)
     constexpr float kLn2 = 0.69314718055994531f;
     const int lane = threadIdx.x & 31;
     const int n = n_sys + n_ctx;
     const int d0 = lane * V;
+    // part j's slot: first + j * stride within its section (system parts,
+    // then context parts)
+    const size_t sys0 = sys_slot(p, 0, r, h), ctx0 = dec ? dec_slot(p, 0, b, h) : mq_slot(p, 0, r, h);
+    const size_t sys_st = (size_t)p.max_q_total * p.H, ctx_st = dec ? (size_t)p.B * p.H : sys_st;
+    auto slot = [&](int j) { return j < n_sys ? sys0 + (size_t)j * sys_st : ctx0 + (size_t)(j - n_sys) * ctx_st; };
     float M = kNegInf, W = 0.f, acc[V];
 #pragma unroll
     for (int v = 0; v < V; v++) acc[v] = 0.f;
@@ -612,7 +617,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
         if (j0 == 0 && have_lk0) {
             lk = lane < cnt ? lk0 : kNegInf;
         } else if (lane < cnt) {
-            lk = __ldcg(p.part_lse + part_slot(p, j0 + lane, n_sys, dec, r, b, h));
+            lk = __ldcg(p.part_lse + slot(j0 + lane));
         }
         float mk = lk;
 #pragma unroll
@@ -631,7 +636,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
             for (int k = 0; k < CH; k++) {
                 const int j = j0 + c0 + k;
                 if (c0 + k < cnt) {
-                    const float *src = p.part_o + part_slot(p, j, n_sys, dec, r, b, h) * D + d0;
+                    const float *src = p.part_o + slot(j) * D + d0;
                     if constexpr (V == 4) {
                         const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
                         x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
@@ -1437,25 +1442,30 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 {
     constexpr int S = Smem<D>::kStagesW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // The first three tickets of every warp are static, in snake order over
-    // the longest-first queue (warp w takes items w, 2 n_w - 1 - w and
-    // 2 n_w + w), so the static rounds give every warp a similar load; later
-    // tickets come from the queue, requested one item ahead.  So no warp touches the queue
-    // counter before its first item is done (1216 warps incrementing one
-    // address at the same instant hold up the requests behind them).
+    // Small batches (dec_static = 3): the first three tickets of every warp
+    // are static, in snake order over the longest-first queue (warp w takes
+    // items w, 2 n_w - 1 - w and 2 n_w + w), so the static rounds give every
+    // warp a similar load and no warp touches the queue counter before its
+    // first item is done (1216 warps incrementing one address at the same
+    // instant hold up the requests behind them).  Large batches, and a grid
+    // whose CTAs start at different times (beside the tensor-core grid),
+    // take every ticket from the queue (dec_static = 0), so that the longest
+    // items go first to whichever warps run.  Queue tickets are requested
+    // one item ahead.
     const unsigned n_w = gridDim.x * kWarps;
     const unsigned wid = blockIdx.x * kWarps + warp;
+    const int n_static = p.dec_static;
     unsigned ticket = wid;
+    if (n_static == 0 && lane == 0) ticket = atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
     int taken = 0;
-    constexpr int kStatic = 3;
     auto request = [&]() {      // ask for a ticket; its value is read later
-        if (lane == 0) ticket = kStatic * n_w + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
+        if (lane == 0) ticket = n_static * n_w + atomicAdd(&p.ctrl[CTRL_DEC_ITEMS], 1u);
     };
     auto take = [&](DecItem<D> &it) {
         int id = __shfl_sync(0xffffffffu, (int)ticket, 0);
         dec_item<D, GRP>(p, s, id, n_dec, it);
         ++taken;
-        if (taken < kStatic) ticket = (taken & 1) ? (taken + 1) * n_w - 1 - wid : taken * n_w + wid;
+        if (taken < n_static) ticket = (taken & 1) ? (taken + 1) * n_w - 1 - wid : taken * n_w + wid;
         else if (it.id >= 0) request();
     };
 
@@ -1555,7 +1565,7 @@ __device__ void decode_phase(const Params &p, Smem<D> &s, int n_dec)
 // pipeline compiled into it costs start-up time whether it runs or not
 // (3.5 us of a 70 us step, measured), hence the instances.
 template <int D, bool GRP, int ROWS>
-__global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
+__device__ __forceinline__ void relay_body(const Params &p)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(smem_raw);
@@ -1604,15 +1614,29 @@ __global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+template <int D, bool GRP, int ROWS>
+__global__ void __launch_bounds__(kThreads, 1) relay_kernel(const Params p)
+{
+    relay_body<D, GRP, ROWS>(p);
+    // Behind the tensor-core grid this grid is a programmatic dependent: it
+    // starts on the SMs that grid's last wave frees (nothing here reads what
+    // that grid writes) and leaves only once that grid has completed, so
+    // that its own completion, which the merge waits for, covers both.
+    // Without a primary grid the wait returns at once.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
 // ============================================================================= merge kernel
 // One warp per (row, head): combines the row's system partials and context
 // partials.  Launched as a programmatic dependent of relay_kernel: it waits
 // for that grid (and its memory) before reading anything it wrote.  SPEC
 // (small batches without q_lens, where the merge is one L2 round trip after
 // another): the first candidate partial rows are requested together with
-// their log-sum-exps.
+// their log-sum-exps.  Otherwise (many rows: the merge is latency-bound by
+// the warps resident) 8 partial rows in flight per lane and three CTAs per
+// SM (four spill registers).
 template <int D, bool SPEC>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
+__global__ void __launch_bounds__(kThreads, SPEC ? 1 : 3) merge_kernel(const Params p)
 {
     __shared__ int qo[kMaxB + 1];
     __shared__ int nctx[kMaxB];
@@ -1668,7 +1692,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
         const int n_ctx = has_ctx(p.mode) ? req_info(p, nc, p.Lq, tps).ns : 0;
         const int n = n_sys + n_ctx;
         if (!SPEC || n > kSpec) {
-            merge_row<D>(p, r, b, r % p.Lq, h, n_sys, n_ctx, dec, true, lk);
+            merge_row<D, SPEC ? 16 : 8>(p, r, b, r % p.Lq, h, n_sys, n_ctx, dec, true, lk);
             return;
         }
         constexpr float kLn2 = 0.69314718055994531f;
@@ -1723,7 +1747,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p)
     const int ql = qo[b + 1] - qo[b];
     const int n_sys = has_sys(p.mode) ? p.R_sys : 0;
     const int n_ctx = has_ctx(p.mode) ? req_info(p, nctx[b], ql, tps).ns : 0;
-    merge_row<D>(p, r, b, r - qo[b], h, n_sys, n_ctx, ql == 1);
+    merge_row<D, 8>(p, r, b, r - qo[b], h, n_sys, n_ctx, ql == 1);
 }
 
 // ============================================================================= KV append

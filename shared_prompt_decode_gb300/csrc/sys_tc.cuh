@@ -54,6 +54,7 @@ constexpr int kRowsTC = 128;          // query rows per tile (TMEM lanes)
 constexpr int kKeysTC = 64;           // keys per K/V stage
 constexpr int kPageTC = 16;           // tokens per page of the paged pool
 constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
+constexpr int kMaxBatchTC = 512;      // requests of a batch
 constexpr int kStagesK = 3, kStagesV = 2;   // V stage j % 2 is freed by the O-done barrier of PV(j)
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
@@ -145,6 +146,11 @@ __device__ __forceinline__ void mbar_drain(unsigned bar, unsigned parity)
     const unsigned long long t0 = global_ns();
     while (!mbar_try(bar, parity) && global_ns() - t0 < kDrainNs) {
     }
+}
+
+__device__ __forceinline__ void mbar_inval(unsigned bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(unsigned bar)
@@ -318,6 +324,8 @@ struct TcParams {
     const int *block_tables;         // [B][max_blocks] page ids
     int max_blocks, num_blocks;
     long long mq_base;               // partial row of compact row r, head h: mq_base + r * H + h
+    unsigned *queue;                 // decode step: [0] items taken, [1] CTAs done; zero before the launch and after
+    int n_yield;                     // CTAs that leave at once when the batch has decode requests
 };
 
 // tile pairs for Mv virtual rows
@@ -335,40 +343,52 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 
 
 
-// System step: blockIdx.x = (range * Hkv + hk) * pairs + pair, so the tile
-// pairs that stream the same keys (one KV head, one key range) are adjacent
-// in launch order, run in the same wave and share those keys through L2.
-// Prefill: blockIdx.x = pair' * Hkv + hk, pairs latest first.  tmK / tmV view
-// sys_k / sys_v as [Ls][Hkv][128] fp16 with a {64 d, 1 head, 64 keys} box
-// and 128-byte swizzle.
+// Items, in queue order (longest first, so that CTAs finish together):
+//   system items, item = (range * Hkv + hk) * pairs + pair: one KV head, a
+//     pair of 128-row tiles of its virtual rows, a range of system keys.
+//     Items that stream the same keys (one KV head, one key range) are
+//     adjacent, so CTAs that run at the same time share them through L2.
+//     tmK / tmV view sys_k / sys_v as [Ls][Hkv][128] fp16 with a {64 d, 1
+//     head, 64 keys} box and 128-byte swizzle.
+//   context items (decode step, after every system item), item - n_sys =
+//     c * Hkv + hk: the rows of one request b with several query rows
+//     (q_lens[b] > 1) against the request's own context, one pair of its
+//     row tiles (c-th in request order, latest tile pair of a request first),
+//     one KV head.  Row i of the request (0 <= i < q_lens[b]) sees context
+//     keys below max(0, ctx_lens[b] - q_lens[b] + 1 + i): the chunk's own
+//     keys are in the context already, causally.  tmKc / tmVc view k_cache /
+//     v_cache as [num_blocks][Hkv][16][128] fp16 with a {64 d, 16 tokens, 1,
+//     1} box: a 64-key stage is four page boxes per d-half, page ids from
+//     block_tables staged in shared memory; a page past the context reads
+//     page id num_blocks, out of range, so the copy fills it with zeros.
+//   PREFILL: causal self-attention of the system prompt itself (its Ls query
+//     rows, in q = [Ls][H][128]; row t sees system keys 0..t), one key
+//     range, item = pair' * Hkv + hk with tile pairs latest (longest) first:
+//     an item streams keys up to its last row's position, masks per row on
+//     the diagonal stages, and writes the final fp16 output and natural-log
+//     LSE instead of partials.
 //
-// Context CTAs (decode step, blockIdx.x >= n_sys, after every system CTA so
-// that they fill the last system wave): the rows of one request b with
-// several query rows (q_lens[b] > 1) against the request's own context, one
-// pair of its row tiles, one KV head: blockIdx.x - n_sys = item * Hkv + hk,
-// items in request order and, within a request, latest tile pair first (the
-// longest).  Row i of the request (0 <= i < q_lens[b]) sees context keys
-// below max(0, ctx_lens[b] - q_lens[b] + 1 + i): the chunk's own keys are in
-// the context already, causally.  tmKc / tmVc view k_cache / v_cache as
-// [num_blocks][Hkv][16][128] fp16 with a {64 d, 16 tokens, 1, 1} box: a
-// 64-key stage is four page boxes per d-half, page ids from block_tables
-// staged in shared memory; a page past the context reads page id
-// num_blocks, out of range, so the copy fills it with zeros.
-//
-// PREFILL: causal self-attention of the system prompt itself (its Ls query
-// rows, in q = [Ls][H][128]; row t sees system keys 0..t), one key range:
-// a CTA streams keys up to its last row's position, masks per row on the
-// diagonal stages, takes tile pairs latest first (the longest first), and
-// writes the final fp16 output and natural-log LSE instead of partials.
+// Persistent: at most one CTA per SM, each taking items from the queue
+// (queue[0]) until it runs dry (prefill: a static snake order); TMEM is
+// allocated once per CTA, the mbarriers are set up afresh for every item.
+// The last CTA to leave (queue[1] counts them) sets both words back to zero
+// for the next launch.
+// In a decode step whose batch also has decode requests, the last n_yield
+// CTAs leave at once: the streaming kernel, a programmatic dependent of this
+// grid, starts on those SMs and streams the decode requests' contexts while
+// the tensor cores of the others run; it takes the remaining SMs as this
+// grid's CTAs leave.
 template <bool PREFILL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc, const TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ int qo[513];
-    __shared__ int blk_sh[kMaxPagesTC];
-    __shared__ int item_sh[4];
+    __shared__ int qo[kMaxBatchTC + 1];          // query rows before request b
+    __shared__ int ip[kMaxBatchTC + 1];          // context items (tile pairs) before request b
+    __shared__ int cn_sh[kMaxBatchTC];           // context length of request b
+    __shared__ int blk_sh[kMaxPagesTC];          // page ids of a context item
+    __shared__ int next_sh, dec_sh;
     __shared__ unsigned tmem_base_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -377,112 +397,66 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     unsigned char *gbase = smem_raw + (sbase - sraw);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (unsigned)i; };
     volatile int *abort_p = &abort_sh;
-    const bool ctx = !PREFILL && (int)blockIdx.x >= p.n_sys;
+    // the streaming grid that follows may take the SMs this grid frees once
+    // every CTA of this grid has started (it waits for this grid before it
+    // leaves)
+    if (!PREFILL) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-    // Rows of the batch: the prefix qo of q_lens (B <= 512), with the
-    // streaming kernel's reading of bad lengths (a q_lens[b] outside [0, Lq]
-    // or a ctx_lens[b] outside [0, 16 max_blocks] makes the request empty;
-    // that kernel raises the flag), so that both number the rows alike.  A
-    // context CTA also finds its item: (request, tile pair, rows, context).
+    // The batch, once per CTA: row prefix qo, with the streaming kernel's
+    // reading of bad lengths (a q_lens[b] outside [0, Lq] or a ctx_lens[b]
+    // outside [0, 16 max_blocks] makes the request empty; that kernel raises
+    // the flag), so that both number the rows alike; the context item prefix
+    // ip and context lengths; whether any request decodes (one row, a
+    // context).
     if (!PREFILL && warp == 0) {
-        const int it_want = ctx ? ((int)blockIdx.x - p.n_sys) / p.Hkv : -1;
-        if (lane == 0) item_sh[0] = -1;
-        __syncwarp();
-        if (p.q_lens) {
-            int run_q = 0, run_i = 0;
-            for (int b0 = 0; b0 < p.B; b0 += 32) {
-                const int b = b0 + lane;
-                int ql = 0, n = 0;
-                if (b < p.B) {
-                    ql = p.q_lens[b];
-                    n = p.ctx_lens ? p.ctx_lens[b] : 0;
-                    if (ql < 0 || ql > p.Lq) ql = 0;
-                    if (n < 0 || n > p.max_blocks * kPageTC) { ql = 0; n = 0; }
-                }
-                const int it = (ctx && ql > 1) ? tile_pairs(ql * p.G) : 0;
-                const int iq = warp_incl_scan(ql), ii = warp_incl_scan(it);
-                if (b < p.B) qo[b] = run_q + iq - ql;
-                const int first = run_i + ii - it;
-                if (it_want >= first && it_want < first + it) {
-                    item_sh[0] = b;
-                    item_sh[1] = it - 1 - (it_want - first);   // latest tile pair first
-                    item_sh[2] = ql;
-                    item_sh[3] = n;
-                }
-                run_q += __shfl_sync(0xffffffffu, iq, 31);
-                run_i += __shfl_sync(0xffffffffu, ii, 31);
+        int run_q = 0, run_i = 0;
+        bool dec = false;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            int ql = 0, n = 0;
+            if (b < p.B) {
+                ql = p.q_lens ? p.q_lens[b] : p.Lq;
+                n = p.ctx_lens ? p.ctx_lens[b] : 0;
+                if (ql < 0 || ql > p.Lq) ql = 0;
+                if (n < 0 || n > p.max_blocks * kPageTC) { ql = 0; n = 0; }
+                cn_sh[b] = n;
             }
-            if (lane == 0) qo[p.B] = run_q;
-        } else {
-            for (int b = lane; b <= p.B; b += 32) qo[b] = b * p.Lq;
-            if (ctx && lane == 0 && p.ctx_pairs > 0) {
-                const int b = it_want / p.ctx_pairs;
-                int n = b < p.B && p.ctx_lens ? p.ctx_lens[b] : 0;
-                if (b < p.B && n >= 0 && n <= p.max_blocks * kPageTC && p.Lq > 1) {
-                    item_sh[0] = b;
-                    item_sh[1] = p.ctx_pairs - 1 - it_want % p.ctx_pairs;
-                    item_sh[2] = p.Lq;
-                    item_sh[3] = n;
-                }
+            dec |= ql == 1 && n > 0;
+            const int it = (p.ctx_pairs > 0 && ql > 1) ? tile_pairs(ql * p.G) : 0;
+            const int iq = warp_incl_scan(ql), ii = warp_incl_scan(it);
+            if (b < p.B) {
+                qo[b] = run_q + iq - ql;
+                ip[b] = run_i + ii - it;
             }
+            run_q += __shfl_sync(0xffffffffu, iq, 31);
+            run_i += __shfl_sync(0xffffffffu, ii, 31);
+        }
+        dec = __any_sync(0xffffffffu, dec);
+        if (lane == 0) {
+            qo[p.B] = run_q;
+            ip[p.B] = run_i;
+            dec_sh = dec ? 1 : 0;
         }
     }
     if (tid == 0) abort_sh = 0;
     __syncthreads();
-    int hk, pair, rho = 0, Mv;
-    int cb = 0, cql = 0, cn = 0;                     // context CTA: request, its rows, its context length
-    if (PREFILL) {
-        Mv = p.Ls * p.G;
-        hk = blockIdx.x % p.Hkv;
-        pair = p.pairs - 1 - (blockIdx.x / p.Hkv) % p.pairs;
-    } else if (!ctx) {
-        Mv = min(qo[p.B], p.max_q_total) * p.G;      // virtual rows of a KV head
-        hk = (blockIdx.x / p.pairs) % p.Hkv;
-        pair = blockIdx.x % p.pairs;
-        rho = blockIdx.x / (p.Hkv * p.pairs);
-    } else {
-        cb = item_sh[0];
-        if (cb < 0) return;                          // no such item: the whole CTA leaves together
-        hk = ((int)blockIdx.x - p.n_sys) % p.Hkv;
-        pair = item_sh[1];
-        cql = item_sh[2];
-        cn = item_sh[3];
-        Mv = cql * p.G;
-    }
-    const int T = (Mv + kRowsTC - 1) / kRowsTC;
-    if (2 * pair >= T || (!ctx && rho >= p.R)) return;   // the whole CTA leaves together
-    const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
-    const int v_last = min(Mv, (2 * pair + n_act) * kRowsTC) - 1;   // the CTA's last virtual row
-    const int key0 = (PREFILL || ctx) ? 0 : rho * p.range;
-    // prefill: every key up to the position of the CTA's last row; context:
-    // every key its last row sees
-    const int key_hi = PREFILL ? v_last / p.G + 1
-                     : ctx     ? min(max(cn - cql + 1 + v_last / p.G, 0), cn)
-                               : min(key0 + p.range, p.Ls);
-    const int n_tiles = key_hi > key0 ? (key_hi - key0 + kKeysTC - 1) / kKeysTC : 0;
-    const int n_pages = ctx ? (key_hi + kPageTC - 1) / kPageTC : 0;   // context pages read
-
-    if (warp == kWarpMmaS) {
+    const int n_items = PREFILL ? p.pairs * p.Hkv : p.n_sys + ip[p.B] * p.Hkv;
+    const bool yield = !PREFILL && dec_sh && (int)blockIdx.x >= (int)gridDim.x - p.n_yield;
+    if (!yield && warp == kWarpMmaS) {
         const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(&tmem_base_sh));
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst), "n"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
-    if (tid == 0) {
-        for (int s = 0; s < kStagesK; s++) {
-            mbar_init(bar(kBarKFull + s), 1);
-            mbar_init(bar(kBarKEmpty + s), 1);
-        }
-        for (int s = 0; s < kStagesV; s++) mbar_init(bar(kBarVFull + s), 1);
-        for (int i = 0; i < 2; i++) {                // per buffer
-            mbar_init(bar(kBarSFull + i), 1);
-            mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
-            mbar_init(bar(kBarODone + i), 1);
-        }
-        mbar_init(bar(kBarQFull), 256);
-        mbar_init(bar(kBarFin), 2);                  // one commit from each MMA thread
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
+    // prefill: static items in snake order over the longest-first list
+    // (CTA c takes c, 2G - 1 - c, 2G + c, ...; G CTAs), which gives every CTA
+    // a similar load without a queue; decode step: the queue
+    int round = 0;
+    auto snake = [&](int r) {
+        const int G = (int)gridDim.x, c = (int)blockIdx.x;
+        return (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
+    };
+    if (tid == 0) next_sh = PREFILL ? snake(0) : yield ? n_items : (int)atomicAdd(p.queue, 1u);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -492,346 +466,445 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
     auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
     auto pbuf = [&](int t, int b) { return (unsigned)(kOffP + (t * 2 + b) * kPBuf); };
+    // the next item from the queue, once every role is done with this one
+    auto next_item = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) next_sh = *abort_p ? n_items : PREFILL ? snake(++round) : (int)atomicAdd(p.queue, 1u);
+        __syncthreads();
+        tc_fence_after();
+        return next_sh;
+    };
 
-    if (warp < 8) {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int wg = warp >> 2;
-        const int row = tid & 127;
-        const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
-        const int tile = 2 * pair + wg;
-        // virtual row: query row r (context CTA: row i of request cb, compact
-        // row r), query head h
-        const int v = tile * kRowsTC + row;
-        const int i_ctx = v / p.G;
-        const int r = ctx ? qo[cb] + i_ctx : v / p.G, h = hk * p.G + v % p.G;
-        const bool row_ok = wg < n_act && v < Mv && (!ctx || r < p.max_q_total);
-        // context keys this row sees: below lim_ctx
-        const int lim_ctx = min(max(cn - cql + 1 + i_ctx, 0), cn);
-        {
-            // this row's query into the K-major, 128-byte-swizzled Q tile
-            const __half *qrow = p.q;
-            if (row_ok && PREFILL) {
-                qrow = p.q + ((size_t)r * p.H + h) * 128;
-            } else if (row_ok && ctx) {
-                qrow = p.q + (((size_t)cb * p.Lq + i_ctx) * p.H + h) * 128;
-            } else if (row_ok) {
-                const int b = owner_of(qo, p.B, r);
-                qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
-            }
-            const unsigned sQ = sbase + kOffQ + (unsigned)(wg * kQTile);
-#pragma unroll
-            for (int c = 0; c < 16; c++) {
-                const unsigned dq = sQ + (c >> 3) * kHalfQ + sw_off(row, c & 7);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dq), "l"(qrow + c * 8),
-                             "r"(row_ok ? 16 : 0));
-            }
-            asm volatile("cp.async.commit_group;\n" ::: "memory");
-            asm volatile("cp.async.wait_all;\n" ::: "memory");
-            fence_async_smem();
-            mbar_arrive(bar(kBarQFull));
+    for (int item = next_sh; item < n_items; item = next_item()) {
+        const bool ctx = !PREFILL && item >= p.n_sys;
+        int hk, pair, rho = 0, Mv;
+        int cb = 0, cql = 0, cn = 0;                     // context item: request, its rows, its context length
+        if (PREFILL) {
+            Mv = p.Ls * p.G;
+            hk = item % p.Hkv;
+            pair = p.pairs - 1 - item / p.Hkv;
+        } else if (!ctx) {
+            Mv = min(qo[p.B], p.max_q_total) * p.G;      // virtual rows of a KV head
+            hk = (item / p.pairs) % p.Hkv;
+            pair = item % p.pairs;
+            rho = item / (p.Hkv * p.pairs);
+        } else {
+            const int c = (item - p.n_sys) / p.Hkv;
+            hk = (item - p.n_sys) % p.Hkv;
+            cb = owner_of(ip, p.B, c);
+            cql = qo[cb + 1] - qo[cb];
+            cn = cn_sh[cb];
+            Mv = cql * p.G;
+            pair = tile_pairs(Mv) - 1 - (c - ip[cb]);    // latest tile pair first
         }
-        if (wg < n_act) {
-            float m_run = kNegInf, l_run = 0.f;
-            int done = 0;
-            for (int j = 0; j < n_tiles; j++) {
-                const int b = j & 1;
-                bool ok = mbar_wait(bar(kBarSFull + b), (j >> 1) & 1, abort_p);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                tc_fence_after();
-                float s[64];
-                {
-                    unsigned a[32], c[32];
-                    tmem_ld32(tS(wg, b) + lane_off, a);
-                    tmem_ld32(tS(wg, b) + lane_off + 32, c);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        s[i] = __uint_as_float(a[i]);
-                        s[32 + i] = __uint_as_float(c[i]);
-                    }
-                }
-                const int kbase = key0 + j * kKeysTC;
-                // keys visible to this row: below lim
-                const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
-                if (kbase + kKeysTC > lim) {
-#pragma unroll
-                    for (int i = 0; i < 64; i++)
-                        if (kbase + i >= lim) s[i] = kNegInf;
-                }
-                float mx[8];
-#pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    mx[k] = max3f(s[k], s[8 + k], s[16 + k]);
-                    mx[k] = max3f(mx[k], s[24 + k], s[32 + k]);
-                    mx[k] = max3f(mx[k], s[40 + k], s[48 + k]);
-                    mx[k] = fmaxf(mx[k], s[56 + k]);
-                }
-                const float mraw = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-                const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
-                bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
-                // lazy rescale: only when this row's max grows by more than 8 (log2)
-                const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
-                bool rescaled = false;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float mn = grow ? mt : m_run;
-                    const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
-                    if (j >= 1) {
-                        // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
-                        ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
-                        if (!__all_sync(0xffffffffu, ok)) break;
-                        pbuf_free = true;
-                        tc_fence_after();
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; q4++) {
-                            unsigned o[32];
-                            tmem_ld32(tO(wg) + lane_off + q4 * 32, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tO(wg) + lane_off + q4 * 32, o);
-                        }
-                        tmem_wait_st();
-                        rescaled = true;
-                    }
-                    l_run *= alpha;
-                    m_run = mn;
-                }
-                const float mu = (m_run == kNegInf) ? 0.f : m_run;
-                unsigned pk[32];
-                const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nmu2 = f2_pack(-mu, -mu);
-                unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};     // pairs of +0.0f
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nmu2), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    ls[i & 3] = f2_add(ls[i & 3], f2_pack(p0, p1));
-                    pk[i] = pack_half2(p0, p1);
-                }
-                {
-                    float a0, a1;
-                    f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
-                    l_run += a0 + a1;
-                }
-                if (!pbuf_free) {
-                    ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
-                    if (!__all_sync(0xffffffffu, ok)) break;
-                }
-                // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
-                unsigned char *pr = gbase + pbuf(wg, b);
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_async_smem();
-                // the MMA threads check only READY: V(j) and K(j+2) must have landed
-                ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
-                if (ok && j + 2 < n_tiles)
-                    ok = mbar_wait(bar(kBarKFull + (j + 2) % kStagesK), ((j + 2) / kStagesK) & 1, abort_p);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                if (ctx && wg == 0 && j == n_tiles - 1 && cn < n_pages * kPageTC) {
-                    // the last page's slots past the context hold whatever the
-                    // pool holds there: zero their V rows (P is 0 on them, and
-                    // 0 times a NaN would not be)
-                    const int lo = cn - kbase, cnt = (n_pages * kPageTC - cn) * 16;   // 16-byte chunks
-                    unsigned char *vs = gbase + kOffV + (j % kStagesV) * kStageBytes;
-                    for (int c = row; c < cnt; c += kRowsTC)
-                        *reinterpret_cast<uint4 *>(vs + ((c >> 3) & 1) * kHalfKV + (lo + (c >> 4)) * 128 +
-                                                   (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    fence_async_smem();
-                }
-                tc_fence_before();   // S(j) loads (and a rescale's stores) before the MMAs that follow
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarReady + b));
-                done = j + 1;
+        const int T = (Mv + kRowsTC - 1) / kRowsTC;
+        if (2 * pair >= T || (!ctx && rho >= p.R)) continue;   // nothing to do (uniform over the CTA)
+        const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
+        const int v_last = min(Mv, (2 * pair + n_act) * kRowsTC) - 1;   // the item's last virtual row
+        const int key0 = (PREFILL || ctx) ? 0 : rho * p.range;
+        // prefill: every key up to the position of the item's last row; context:
+        // every key its last row sees
+        const int key_hi = PREFILL ? v_last / p.G + 1
+                         : ctx     ? min(max(cn - cql + 1 + v_last / p.G, 0), cn)
+                                   : min(key0 + p.range, p.Ls);
+        const int n_tiles = key_hi > key0 ? (key_hi - key0 + kKeysTC - 1) / kKeysTC : 0;
+        const int n_pages = ctx ? (key_hi + kPageTC - 1) / kPageTC : 0;   // context pages read
+
+        if (tid == 0) {
+            for (int s = 0; s < kStagesK; s++) {
+                mbar_init(bar(kBarKFull + s), 1);
+                mbar_init(bar(kBarKEmpty + s), 1);
             }
-            // the row's partial: normalised O and log2-sum-exp, once every MMA
-            // has completed (the single-shot barrier the MMA thread commits last)
-            bool fin = done == n_tiles;
-            if (fin && n_tiles > 0) fin = mbar_wait(bar(kBarFin), 0, abort_p);
-            fin = __all_sync(0xffffffffu, fin);
-            tc_fence_after();
-            if (!fin && lane == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
-            const size_t prow = PREFILL ? (size_t)r * p.H + h
-                              : ctx     ? (size_t)p.mq_base + (size_t)r * p.H + h
-                                        : ((size_t)rho * p.max_q_total + r) * p.H + h;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) {
-                unsigned o[32];
-                if (fin && n_tiles > 0) {
-                    tmem_ld32(tO(wg) + lane_off + q4 * 32, o);   // warp-collective
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i++) o[i] = 0u;
+            for (int s = 0; s < kStagesV; s++) mbar_init(bar(kBarVFull + s), 1);
+            for (int i = 0; i < 2; i++) {                // per buffer
+                mbar_init(bar(kBarSFull + i), 1);
+                mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
+                mbar_init(bar(kBarODone + i), 1);
+            }
+            mbar_init(bar(kBarQFull), 256);
+            mbar_init(bar(kBarFin), 2);                  // one commit from each MMA thread
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        }
+        __syncthreads();
+        if (warp < 8) {
+            // ------------------------------------------------------------ softmax warpgroups
+            const int wg = warp >> 2;
+            const int row = tid & 127;
+            const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
+            const int tile = 2 * pair + wg;
+            // virtual row: query row r (context CTA: row i of request cb, compact
+            // row r), query head h
+            const int v = tile * kRowsTC + row;
+            const int i_ctx = v / p.G;
+            const int r = ctx ? qo[cb] + i_ctx : v / p.G, h = hk * p.G + v % p.G;
+            const bool row_ok = wg < n_act && v < Mv && (!ctx || r < p.max_q_total);
+            // context keys this row sees: below lim_ctx
+            const int lim_ctx = min(max(cn - cql + 1 + i_ctx, 0), cn);
+            {
+                // this row's query into the K-major, 128-byte-swizzled Q tile
+                const __half *qrow = p.q;
+                if (row_ok && PREFILL) {
+                    qrow = p.q + ((size_t)r * p.H + h) * 128;
+                } else if (row_ok && ctx) {
+                    qrow = p.q + (((size_t)cb * p.Lq + i_ctx) * p.H + h) * 128;
+                } else if (row_ok) {
+                    const int b = owner_of(qo, p.B, r);
+                    qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
+                }
+                const unsigned sQ = sbase + kOffQ + (unsigned)(wg * kQTile);
+    #pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    const unsigned dq = sQ + (c >> 3) * kHalfQ + sw_off(row, c & 7);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dq), "l"(qrow + c * 8),
+                                 "r"(row_ok ? 16 : 0));
+                }
+                asm volatile("cp.async.commit_group;\n" ::: "memory");
+                asm volatile("cp.async.wait_all;\n" ::: "memory");
+                fence_async_smem();
+                mbar_arrive(bar(kBarQFull));
+            }
+            if (wg < n_act) {
+                float m_run = kNegInf, l_run = 0.f;
+                int done = 0;
+                for (int j = 0; j < n_tiles; j++) {
+                    const int b = j & 1;
+                    bool ok = mbar_wait(bar(kBarSFull + b), (j >> 1) & 1, abort_p);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    tc_fence_after();
+                    float s[64];
+                    {
+                        unsigned a[32], c[32];
+                        tmem_ld32(tS(wg, b) + lane_off, a);
+                        tmem_ld32(tS(wg, b) + lane_off + 32, c);
+                        tmem_wait_ld();
+    #pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            s[i] = __uint_as_float(a[i]);
+                            s[32 + i] = __uint_as_float(c[i]);
+                        }
+                    }
+                    const int kbase = key0 + j * kKeysTC;
+                    // keys visible to this row: below lim
+                    const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
+                    if (kbase + kKeysTC > lim) {
+    #pragma unroll
+                        for (int i = 0; i < 64; i++)
+                            if (kbase + i >= lim) s[i] = kNegInf;
+                    }
+                    float mx[8];
+    #pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        mx[k] = max3f(s[k], s[8 + k], s[16 + k]);
+                        mx[k] = max3f(mx[k], s[24 + k], s[32 + k]);
+                        mx[k] = max3f(mx[k], s[40 + k], s[48 + k]);
+                        mx[k] = fmaxf(mx[k], s[56 + k]);
+                    }
+                    const float mraw =
+                        max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                    const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
+                    bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
+                    // lazy rescale: only when this row's max grows by more than 8 (log2)
+                    const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
+                    bool rescaled = false;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        const float mn = grow ? mt : m_run;
+                        const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
+                        if (j >= 1) {
+                            // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
+                            ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
+                            if (!__all_sync(0xffffffffu, ok)) break;
+                            pbuf_free = true;
+                            tc_fence_after();
+    #pragma unroll
+                            for (int q4 = 0; q4 < 4; q4++) {
+                                unsigned o[32];
+                                tmem_ld32(tO(wg) + lane_off + q4 * 32, o);
+                                tmem_wait_ld();
+    #pragma unroll
+                                for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                                tmem_st32(tO(wg) + lane_off + q4 * 32, o);
+                            }
+                            tmem_wait_st();
+                            rescaled = true;
+                        }
+                        l_run *= alpha;
+                        m_run = mn;
+                    }
+                    const float mu = (m_run == kNegInf) ? 0.f : m_run;
+                    unsigned pk[32];
+                    const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nmu2 = f2_pack(-mu, -mu);
+                    unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};     // pairs of +0.0f
+    #pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nmu2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        ls[i & 3] = f2_add(ls[i & 3], f2_pack(p0, p1));
+                        pk[i] = pack_half2(p0, p1);
+                    }
+                    {
+                        float a0, a1;
+                        f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
+                        l_run += a0 + a1;
+                    }
+                    if (!pbuf_free) {
+                        ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
+                        if (!__all_sync(0xffffffffu, ok)) break;
+                    }
+                    // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
+                    unsigned char *pr = gbase + pbuf(wg, b);
+    #pragma unroll
+                    for (int c = 0; c < 8; c++)
+                        *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    fence_async_smem();
+                    // the MMA threads check only READY: V(j) and K(j+2) must have landed
+                    ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
+                    if (ok && j + 2 < n_tiles)
+                        ok = mbar_wait(bar(kBarKFull + (j + 2) % kStagesK), ((j + 2) / kStagesK) & 1, abort_p);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    if (ctx && wg == 0 && j == n_tiles - 1 && cn < n_pages * kPageTC) {
+                        // the last page's slots past the context hold whatever the
+                        // pool holds there: zero their V rows (P is 0 on them, and
+                        // 0 times a NaN would not be)
+                        const int lo = cn - kbase, cnt = (n_pages * kPageTC - cn) * 16;   // 16-byte chunks
+                        unsigned char *vs = gbase + kOffV + (j % kStagesV) * kStageBytes;
+                        for (int c = row; c < cnt; c += kRowsTC)
+                            *reinterpret_cast<uint4 *>(vs + ((c >> 3) & 1) * kHalfKV + (lo + (c >> 4)) * 128 +
+                                                       (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        fence_async_smem();
+                    }
+                    tc_fence_before();   // S(j) loads (and a rescale's stores) before the MMAs that follow
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kBarReady + b));
+                    done = j + 1;
+                }
+                // the row's partial: normalised O and log2-sum-exp, once every MMA
+                // has completed (the single-shot barrier the MMA thread commits last)
+                bool fin = done == n_tiles;
+                if (fin && n_tiles > 0) fin = mbar_wait(bar(kBarFin), 0, abort_p);
+                fin = __all_sync(0xffffffffu, fin);
+                tc_fence_after();
+                if (!fin && lane == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
+                const size_t prow = PREFILL ? (size_t)r * p.H + h
+                                  : ctx     ? (size_t)p.mq_base + (size_t)r * p.H + h
+                                            : ((size_t)rho * p.max_q_total + r) * p.H + h;
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    #pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) {
+                    unsigned o[32];
+                    if (fin && n_tiles > 0) {
+                        tmem_ld32(tO(wg) + lane_off + q4 * 32, o);   // warp-collective
+                        tmem_wait_ld();
+                    } else {
+    #pragma unroll
+                        for (int i = 0; i < 32; i++) o[i] = 0u;
+                    }
+                    if (row_ok && PREFILL) {
+                        __half *po = p.out + prow * 128 + q4 * 32;
+    #pragma unroll
+                        for (int i = 0; i < 32; i += 8)
+                            *reinterpret_cast<uint4 *>(po + i) = make_uint4(
+                                pack_half2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
+                                pack_half2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
+                                pack_half2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
+                                pack_half2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+                    } else if (row_ok) {
+                        float *po = p.part_o + prow * 128;
+    #pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            __stcg(reinterpret_cast<float4 *>(po + q4 * 32 + i),
+                                   make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                               __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv));
+                    }
                 }
                 if (row_ok && PREFILL) {
-                    __half *po = p.out + prow * 128 + q4 * 32;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8)
-                        *reinterpret_cast<uint4 *>(po + i) = make_uint4(
-                            pack_half2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
-                            pack_half2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
-                            pack_half2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
-                            pack_half2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+                    if (p.lse_out)
+                        p.lse_out[prow] = (l_run > 0.f && fin) ? (m_run + lg2(l_run)) * 0.69314718055994531f : kNegInf;
                 } else if (row_ok) {
-                    float *po = p.part_o + prow * 128;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        __stcg(reinterpret_cast<float4 *>(po + q4 * 32 + i),
-                               make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                           __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv));
+                    __stcg(p.part_lse + prow, (l_run > 0.f && fin) ? m_run + lg2(l_run) : kNegInf);
                 }
             }
-            if (row_ok && PREFILL) {
-                if (p.lse_out) p.lse_out[prow] = (l_run > 0.f && fin) ? (m_run + lg2(l_run)) * 0.69314718055994531f : kNegInf;
-            } else if (row_ok) {
-                __stcg(p.part_lse + prow, (l_run > 0.f && fin) ? m_run + lg2(l_run) : kNegInf);
-            }
-        }
-    } else if (warp == kWarpLoad) {
-        // ------------------------------------------------------------ TMA producer
-        // K runs up to kStagesK stages ahead and V up to kStagesV, each as
-        // soon as its ring has room (polled, so neither ring holds up the other)
-        bool bad_blk = false;
-        if (ctx) {
-            // the request's page ids, checked: an id outside [0, num_blocks)
-            // raises the flag and reads as zeros
-            const int *bt = p.block_tables + (size_t)cb * p.max_blocks;
-            for (int i = lane; i < n_pages; i += 32) {
-                int blk = bt[i];
-                if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                    bad_blk = true;
-                    blk = p.num_blocks;
-                }
-                blk_sh[i] = blk;
-            }
-            __syncwarp();
-            if (__any_sync(0xffffffffu, bad_blk) && lane == 0) atomicOr(p.flags, RELAY_FLAG_BAD_BLOCK);
-        }
-        // four page boxes per d-half of a context stage (pages past the
-        // context: page id num_blocks, zero fill)
-        auto load_ctx = [&](unsigned dst, const CUtensorMap *tm, int j, unsigned mb) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) {
-                const int pg = 4 * j + q4;
-                const int blk = pg < n_pages ? blk_sh[pg] : p.num_blocks;
-                tma_load_4d(dst + q4 * (kPageTC * 128), tm, 0, 0, hk, blk, mb);
-                tma_load_4d(dst + kHalfKV + q4 * (kPageTC * 128), tm, 64, 0, hk, blk, mb);
-            }
-        };
-        if (lane == 0) {
-            int jk = 0, jv = 0;
-            unsigned long long t_last = global_ns();
-            while ((jk < n_tiles || jv < n_tiles) && !*abort_p) {
-                bool progress = false;
-                if (jk < n_tiles &&
-                    (jk < kStagesK || mbar_test(bar(kBarKEmpty + jk % kStagesK), ((jk / kStagesK) - 1) & 1))) {
-                    const int s = jk % kStagesK, z = key0 + jk * kKeysTC;
-                    mbar_expect_tx(bar(kBarKFull + s), kStageBytes);
-                    if (ctx) {
-                        load_ctx(kstage(s), &tmKc, jk, bar(kBarKFull + s));
-                    } else {
-                        tma_load_3d(kstage(s), &tmK, 0, hk, z, bar(kBarKFull + s));
-                        tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, hk, z, bar(kBarKFull + s));
+        } else if (warp == kWarpLoad) {
+            // ------------------------------------------------------------ TMA producer
+            // K runs up to kStagesK stages ahead and V up to kStagesV, each as
+            // soon as its ring has room (polled, so neither ring holds up the other)
+            bool bad_blk = false;
+            if (ctx) {
+                // the request's page ids, checked: an id outside [0, num_blocks)
+                // raises the flag and reads as zeros
+                const int *bt = p.block_tables + (size_t)cb * p.max_blocks;
+                for (int i = lane; i < n_pages; i += 32) {
+                    int blk = bt[i];
+                    if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                        bad_blk = true;
+                        blk = p.num_blocks;
                     }
-                    jk++;
-                    progress = true;
+                    blk_sh[i] = blk;
                 }
-                // V stage jv % 2 held V(jv-2): free once PV(jv-2) has completed
-                if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
-                    const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
-                    mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
-                    if (ctx) {
-                        load_ctx(vstage(s), &tmVc, jv, bar(kBarVFull + s));
-                    } else {
-                        tma_load_3d(vstage(s), &tmV, 0, hk, z, bar(kBarVFull + s));
-                        tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, hk, z, bar(kBarVFull + s));
-                    }
-                    jv++;
-                    progress = true;
-                }
-                if (progress) {
-                    t_last = global_ns();
-                } else if (global_ns() - t_last > kWaitNs) {
-                    *abort_p = 1;
-                    break;
-                }
+                __syncwarp();
+                if (__any_sync(0xffffffffu, bad_blk) && lane == 0) atomicOr(p.flags, RELAY_FLAG_BAD_BLOCK);
             }
-            // no copy may still be in flight when the CTA leaves
-            for (int s = 0; s < kStagesK && s < jk; s++)
-                mbar_drain(bar(kBarKFull + s), ((s + ((jk - 1 - s) / kStagesK) * kStagesK) / kStagesK) & 1);
-            for (int s = 0; s < kStagesV && s < jv; s++)
-                mbar_drain(bar(kBarVFull + s), ((s + ((jv - 1 - s) / kStagesV) * kStagesV) / kStagesV) & 1);
-        }
-    } else if (warp == kWarpMmaS) {
-        // ------------------------------------------------------------ S = Q K^T
-        if (lane == 0) {
-            const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
-            auto issue_s = [&](int j) {              // S(j) of every tile into S buffer j % 2
-                const unsigned kb = kstage(j % kStagesK);
-                for (int t = 0; t < n_act; t++) {
-                    const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
-#pragma unroll
-                    for (int kk = 0; kk < 8; kk++)
-                        umma_ss(tS(t, j & 1), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
-                                sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
+            // four page boxes per d-half of a context stage (pages past the
+            // context: page id num_blocks, zero fill)
+            auto load_ctx = [&](unsigned dst, const CUtensorMap *tm, int j, unsigned mb) {
+    #pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) {
+                    const int pg = 4 * j + q4;
+                    const int blk = pg < n_pages ? blk_sh[pg] : p.num_blocks;
+                    tma_load_4d(dst + q4 * (kPageTC * 128), tm, 0, 0, hk, blk, mb);
+                    tma_load_4d(dst + kHalfKV + q4 * (kPageTC * 128), tm, 64, 0, hk, blk, mb);
                 }
-                umma_commit(bar(kBarSFull + (j & 1)));
-                umma_commit(bar(kBarKEmpty + j % kStagesK));
             };
-            bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
-            for (int j = 0; ok && j < n_tiles && j < 2; j++) {
-                ok = mbar_wait(bar(kBarKFull + j % kStagesK), (j / kStagesK) & 1, abort_p);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(j);
-            }
-            for (int j = 0; ok && j + 2 < n_tiles; j++) {
-                // READY(j): S(j) read (its buffer is free) and K(j+2) landed
-                ok = mbar_wait(bar(kBarReady + (j & 1)), (j >> 1) & 1, abort_p);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(j + 2);
-            }
-            // every S MMA has completed once the final barrier fires
-            umma_commit(bar(kBarFin));
-            mbar_drain(bar(kBarFin), 0);
-        }
-    } else {
-        // ------------------------------------------------------------ O += P V
-        if (lane == 0) {
-            const uint32_t idO = idesc_f16(kRowsTC, 128, true);
-            bool ok = true;
-            for (int j = 0; ok && j < n_tiles; j++) {
-                const int b = j & 1, sv = j % kStagesV;
-                // READY(j): P(j) stored and V(j) landed
-                ok = mbar_wait(bar(kBarReady + b), (j >> 1) & 1, abort_p);
-                if (!ok) break;
-                tc_fence_after();
-                const unsigned vb = vstage(sv);
-                for (int t = 0; t < n_act; t++) {
-                    const unsigned pa = sbase + pbuf(t, b);
-#pragma unroll
-                    for (int kk = 0; kk < 4; kk++)
-                        umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
-                                (j > 0 || kk > 0));
+            if (lane == 0) {
+                int jk = 0, jv = 0;
+                unsigned long long t_last = global_ns();
+                while ((jk < n_tiles || jv < n_tiles) && !*abort_p) {
+                    bool progress = false;
+                    if (jk < n_tiles &&
+                        (jk < kStagesK || mbar_test(bar(kBarKEmpty + jk % kStagesK), ((jk / kStagesK) - 1) & 1))) {
+                        const int s = jk % kStagesK, z = key0 + jk * kKeysTC;
+                        mbar_expect_tx(bar(kBarKFull + s), kStageBytes);
+                        if (ctx) {
+                            load_ctx(kstage(s), &tmKc, jk, bar(kBarKFull + s));
+                        } else {
+                            tma_load_3d(kstage(s), &tmK, 0, hk, z, bar(kBarKFull + s));
+                            tma_load_3d(kstage(s) + kHalfKV, &tmK, 64, hk, z, bar(kBarKFull + s));
+                        }
+                        jk++;
+                        progress = true;
+                    }
+                    // V stage jv % 2 held V(jv-2): free once PV(jv-2) has completed
+                    if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
+                        const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
+                        mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
+                        if (ctx) {
+                            load_ctx(vstage(s), &tmVc, jv, bar(kBarVFull + s));
+                        } else {
+                            tma_load_3d(vstage(s), &tmV, 0, hk, z, bar(kBarVFull + s));
+                            tma_load_3d(vstage(s) + kHalfKV, &tmV, 64, hk, z, bar(kBarVFull + s));
+                        }
+                        jv++;
+                        progress = true;
+                    }
+                    if (progress) {
+                        t_last = global_ns();
+                    } else if (global_ns() - t_last > kWaitNs) {
+                        *abort_p = 1;
+                        break;
+                    }
                 }
-                umma_commit(bar(kBarODone + b));      // also frees V stage sv for the producer
+                // no copy may still be in flight when the CTA leaves
+                for (int s = 0; s < kStagesK && s < jk; s++)
+                    mbar_drain(bar(kBarKFull + s), ((s + ((jk - 1 - s) / kStagesK) * kStagesK) / kStagesK) & 1);
+                for (int s = 0; s < kStagesV && s < jv; s++)
+                    mbar_drain(bar(kBarVFull + s), ((s + ((jv - 1 - s) / kStagesV) * kStagesV) / kStagesV) & 1);
             }
-            umma_commit(bar(kBarFin));
-            mbar_drain(bar(kBarFin), 0);
+        } else if (warp == kWarpMmaS) {
+            // ------------------------------------------------------------ S = Q K^T
+            if (lane == 0) {
+                const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
+                int n_s = 0;                             // S stages issued
+                auto issue_s = [&](int j) {              // S(j) of every tile into S buffer j % 2
+                    const unsigned kb = kstage(j % kStagesK);
+                    for (int t = 0; t < n_act; t++) {
+                        const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
+    #pragma unroll
+                        for (int kk = 0; kk < 8; kk++)
+                            umma_ss(tS(t, j & 1), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
+                                    sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
+                    }
+                    umma_commit(bar(kBarSFull + (j & 1)));
+                    umma_commit(bar(kBarKEmpty + j % kStagesK));
+                    n_s++;
+                };
+                bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
+                for (int j = 0; ok && j < n_tiles && j < 2; j++) {
+                    ok = mbar_wait(bar(kBarKFull + j % kStagesK), (j / kStagesK) & 1, abort_p);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j);
+                }
+                for (int j = 0; ok && j + 2 < n_tiles; j++) {
+                    // READY(j): S(j) read (its buffer is free) and K(j+2) landed
+                    ok = mbar_wait(bar(kBarReady + (j & 1)), (j >> 1) & 1, abort_p);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j + 2);
+                }
+                // every S MMA has completed once the final barrier fires;
+                // the K-empty signals of the last stages, which nobody waits
+                // for, have landed too before the barriers are set up again
+                umma_commit(bar(kBarFin));
+                mbar_drain(bar(kBarFin), 0);
+                for (int s = 0; s < kStagesK && s < n_s; s++)
+                    mbar_drain(bar(kBarKEmpty + s), ((n_s - 1 - s) / kStagesK) & 1);
+            }
+        } else {
+            // ------------------------------------------------------------ O += P V
+            if (lane == 0) {
+                const uint32_t idO = idesc_f16(kRowsTC, 128, true);
+                bool ok = true;
+                int n_pv = 0;                            // PV stages issued
+                for (int j = 0; ok && j < n_tiles; j++) {
+                    const int b = j & 1, sv = j % kStagesV;
+                    // READY(j): P(j) stored and V(j) landed
+                    ok = mbar_wait(bar(kBarReady + b), (j >> 1) & 1, abort_p);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const unsigned vb = vstage(sv);
+                    for (int t = 0; t < n_act; t++) {
+                        const unsigned pa = sbase + pbuf(t, b);
+    #pragma unroll
+                        for (int kk = 0; kk < 4; kk++)
+                            umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
+                                    (j > 0 || kk > 0));
+                    }
+                    umma_commit(bar(kBarODone + b));      // also frees V stage sv for the producer
+                    n_pv++;
+                }
+                umma_commit(bar(kBarFin));
+                mbar_drain(bar(kBarFin), 0);
+                for (int b = 0; b < 2 && b < n_pv; b++) mbar_drain(bar(kBarODone + b), ((n_pv - 1 - b) >> 1) & 1);
+            }
         }
+
+        // every role is done with the item, and every barrier phase it started
+        // has completed: the barriers may be set up again for the next item
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && !*abort_p) {
+            for (int s = 0; s < kStagesK; s++) {
+                mbar_inval(bar(kBarKFull + s));
+                mbar_inval(bar(kBarKEmpty + s));
+            }
+            for (int s = 0; s < kStagesV; s++) mbar_inval(bar(kBarVFull + s));
+            for (int i = 0; i < 2; i++) {
+                mbar_inval(bar(kBarSFull + i));
+                mbar_inval(bar(kBarReady + i));
+                mbar_inval(bar(kBarODone + i));
+            }
+            mbar_inval(bar(kBarQFull));
+            mbar_inval(bar(kBarFin));
+    }
     }
 
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
-    if (warp == kWarpMmaS) {
+    if (!yield && warp == kWarpMmaS) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(kTmemCols) : "memory");
+    }
+    // the last CTA out resets the queue
+    if (!PREFILL && tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.queue + 1, 1u) == gridDim.x - 1) {
+            p.queue[0] = 0u;
+            p.queue[1] = 0u;
+        }
     }
 }
 
