@@ -466,41 +466,85 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
     auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
     auto pbuf = [&](int t, int b) { return (unsigned)(kOffP + (t * 2 + b) * kPBuf); };
-    // the next item from the queue, once every role is done with this one
-    auto next_item = [&]() {
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) next_sh = *abort_p ? n_items : PREFILL ? snake(++round) : (int)atomicAdd(p.queue, 1u);
-        __syncthreads();
-        tc_fence_after();
-        return next_sh;
+    // An item's coordinates.  run: it has rows (uniform over the CTA).
+    struct Item {
+        bool ctx, run;
+        int hk, pair, rho, Mv, cb, cql, cn, n_act;
     };
-
-    for (int item = next_sh; item < n_items; item = next_item()) {
-        const bool ctx = !PREFILL && item >= p.n_sys;
-        int hk, pair, rho = 0, Mv;
-        int cb = 0, cql = 0, cn = 0;                     // context item: request, its rows, its context length
+    auto describe = [&](int item) {
+        Item d{};
+        d.ctx = !PREFILL && item >= p.n_sys;
         if (PREFILL) {
-            Mv = p.Ls * p.G;
-            hk = item % p.Hkv;
-            pair = p.pairs - 1 - item / p.Hkv;
-        } else if (!ctx) {
-            Mv = min(qo[p.B], p.max_q_total) * p.G;      // virtual rows of a KV head
-            hk = (item / p.pairs) % p.Hkv;
-            pair = item % p.pairs;
-            rho = item / (p.Hkv * p.pairs);
+            d.Mv = p.Ls * p.G;
+            d.hk = item % p.Hkv;
+            d.pair = p.pairs - 1 - item / p.Hkv;
+        } else if (!d.ctx) {
+            d.Mv = min(qo[p.B], p.max_q_total) * p.G;      // virtual rows of a KV head
+            d.hk = (item / p.pairs) % p.Hkv;
+            d.pair = item % p.pairs;
+            d.rho = item / (p.Hkv * p.pairs);
         } else {
             const int c = (item - p.n_sys) / p.Hkv;
-            hk = (item - p.n_sys) % p.Hkv;
-            cb = owner_of(ip, p.B, c);
-            cql = qo[cb + 1] - qo[cb];
-            cn = cn_sh[cb];
-            Mv = cql * p.G;
-            pair = tile_pairs(Mv) - 1 - (c - ip[cb]);    // latest tile pair first
+            d.hk = (item - p.n_sys) % p.Hkv;
+            d.cb = owner_of(ip, p.B, c);
+            d.cql = qo[d.cb + 1] - qo[d.cb];
+            d.cn = cn_sh[d.cb];
+            d.Mv = d.cql * p.G;
+            d.pair = tile_pairs(d.Mv) - 1 - (c - ip[d.cb]);   // latest tile pair first
         }
-        const int T = (Mv + kRowsTC - 1) / kRowsTC;
-        if (2 * pair >= T || (!ctx && rho >= p.R)) continue;   // nothing to do (uniform over the CTA)
-        const int n_act = (2 * pair + 1 < T) ? 2 : 1;    // query tiles with rows
+        const int T = (d.Mv + kRowsTC - 1) / kRowsTC;
+        d.run = item < n_items && 2 * d.pair < T && (d.ctx || d.rho < p.R);
+        d.n_act = (2 * d.pair + 1 < T) ? 2 : 1;            // query tiles with rows
+        return d;
+    };
+    // Virtual row v = (2 pair + wg) 128 + row of an item: query row r (a
+    // context item: row i of request cb, compact row r), query head h.
+    auto row_of = [&](const Item &d, int wg, int row, int &r, int &h, int &i_ctx) {
+        const int v = (2 * d.pair + wg) * kRowsTC + row;
+        i_ctx = v / p.G;
+        r = d.ctx ? qo[d.cb] + i_ctx : v / p.G;
+        h = d.hk * p.G + v % p.G;
+        return wg < d.n_act && v < d.Mv && (!d.ctx || r < p.max_q_total);
+    };
+    // this thread's query row of an item into the K-major, 128-byte-swizzled
+    // Q tile of its warpgroup (zeros for a row the item does not have)
+    auto load_q = [&](const Item &d, int wg, int row) {
+        int r, h, i_ctx;
+        const bool ok = row_of(d, wg, row, r, h, i_ctx);
+        const __half *qrow = p.q;
+        if (ok && PREFILL) {
+            qrow = p.q + ((size_t)r * p.H + h) * 128;
+        } else if (ok && d.ctx) {
+            qrow = p.q + (((size_t)d.cb * p.Lq + i_ctx) * p.H + h) * 128;
+        } else if (ok) {
+            const int b = owner_of(qo, p.B, r);
+            qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
+        }
+        const unsigned sQ = sbase + kOffQ + (unsigned)(wg * kQTile);
+#pragma unroll
+        for (int c = 0; c < 16; c++) {
+            const unsigned dq = sQ + (c >> 3) * kHalfQ + sw_off(row, c & 7);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dq), "l"(qrow + c * 8),
+                         "r"(ok ? 16 : 0));
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    auto fetch = [&]() { return *abort_p ? n_items : PREFILL ? snake(++round) : (int)atomicAdd(p.queue, 1u); };
+
+    bool q_pref = false;          // this thread's Q row of `item` is in flight already
+    for (int item = next_sh; item < n_items;) {
+        const Item d = describe(item);
+        if (!d.run) {                                    // nothing to do (uniform over the CTA)
+            __syncthreads();
+            if (tid == 0) next_sh = fetch();
+            __syncthreads();
+            item = next_sh;
+            q_pref = false;
+            continue;
+        }
+        const bool ctx = d.ctx;
+        const int hk = d.hk, pair = d.pair, rho = d.rho, Mv = d.Mv, cb = d.cb, cql = d.cql, cn = d.cn;
+        const int n_act = d.n_act;
         const int v_last = min(Mv, (2 * pair + n_act) * kRowsTC) - 1;   // the item's last virtual row
         const int key0 = (PREFILL || ctx) ? 0 : rho * p.range;
         // prefill: every key up to the position of the item's last row; context:
@@ -527,46 +571,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         }
         __syncthreads();
+        bool pref_next = false;   // this thread has loaded its Q row of the next item
         if (warp < 8) {
             // ------------------------------------------------------------ softmax warpgroups
             const int wg = warp >> 2;
             const int row = tid & 127;
             const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
-            const int tile = 2 * pair + wg;
-            // virtual row: query row r (context CTA: row i of request cb, compact
-            // row r), query head h
-            const int v = tile * kRowsTC + row;
-            const int i_ctx = v / p.G;
-            const int r = ctx ? qo[cb] + i_ctx : v / p.G, h = hk * p.G + v % p.G;
-            const bool row_ok = wg < n_act && v < Mv && (!ctx || r < p.max_q_total);
+            int r, h, i_ctx;
+            const bool row_ok = row_of(d, wg, row, r, h, i_ctx);
             // context keys this row sees: below lim_ctx
             const int lim_ctx = min(max(cn - cql + 1 + i_ctx, 0), cn);
-            {
-                // this row's query into the K-major, 128-byte-swizzled Q tile
-                const __half *qrow = p.q;
-                if (row_ok && PREFILL) {
-                    qrow = p.q + ((size_t)r * p.H + h) * 128;
-                } else if (row_ok && ctx) {
-                    qrow = p.q + (((size_t)cb * p.Lq + i_ctx) * p.H + h) * 128;
-                } else if (row_ok) {
-                    const int b = owner_of(qo, p.B, r);
-                    qrow = p.q + (((size_t)b * p.Lq + (r - qo[b])) * p.H + h) * 128;
-                }
-                const unsigned sQ = sbase + kOffQ + (unsigned)(wg * kQTile);
-    #pragma unroll
-                for (int c = 0; c < 16; c++) {
-                    const unsigned dq = sQ + (c >> 3) * kHalfQ + sw_off(row, c & 7);
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dq), "l"(qrow + c * 8),
-                                 "r"(row_ok ? 16 : 0));
-                }
-                asm volatile("cp.async.commit_group;\n" ::: "memory");
-                asm volatile("cp.async.wait_all;\n" ::: "memory");
-                fence_async_smem();
-                mbar_arrive(bar(kBarQFull));
-            }
+            if (!q_pref) load_q(d, wg, row);
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+            fence_async_smem();
+            mbar_arrive(bar(kBarQFull));
+            float m_run = kNegInf, l_run = 0.f;
+            int done = 0;
             if (wg < n_act) {
-                float m_run = kNegInf, l_run = 0.f;
-                int done = 0;
                 for (int j = 0; j < n_tiles; j++) {
                     const int b = j & 1;
                     bool ok = mbar_wait(bar(kBarSFull + b), (j >> 1) & 1, abort_p);
@@ -578,7 +599,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         tmem_ld32(tS(wg, b) + lane_off, a);
                         tmem_ld32(tS(wg, b) + lane_off + 32, c);
                         tmem_wait_ld();
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; i++) {
                             s[i] = __uint_as_float(a[i]);
                             s[32 + i] = __uint_as_float(c[i]);
@@ -588,12 +609,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     // keys visible to this row: below lim
                     const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
                     if (kbase + kKeysTC > lim) {
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 64; i++)
                             if (kbase + i >= lim) s[i] = kNegInf;
                     }
                     float mx[8];
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < 8; k++) {
                         mx[k] = max3f(s[k], s[8 + k], s[16 + k]);
                         mx[k] = max3f(mx[k], s[24 + k], s[32 + k]);
@@ -616,12 +637,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             if (!__all_sync(0xffffffffu, ok)) break;
                             pbuf_free = true;
                             tc_fence_after();
-    #pragma unroll
+#pragma unroll
                             for (int q4 = 0; q4 < 4; q4++) {
                                 unsigned o[32];
                                 tmem_ld32(tO(wg) + lane_off + q4 * 32, o);
                                 tmem_wait_ld();
-    #pragma unroll
+#pragma unroll
                                 for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                                 tmem_st32(tO(wg) + lane_off + q4 * 32, o);
                             }
@@ -635,7 +656,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     unsigned pk[32];
                     const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nmu2 = f2_pack(-mu, -mu);
                     unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};     // pairs of +0.0f
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 32; i++) {
                         float x0, x1;
                         f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nmu2), x0, x1);
@@ -654,7 +675,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                     // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
                     unsigned char *pr = gbase + pbuf(wg, b);
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < 8; c++)
                         *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -680,6 +701,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (lane == 0) mbar_arrive(bar(kBarReady + b));
                     done = j + 1;
                 }
+            }
+            // Prefill: the next item of the static order and its query rows,
+            // loaded ahead of the last PV MMAs and the epilogue: the Q tile is
+            // free once S(n_tiles - 1), its last reader, has completed (an idle
+            // tile's at any time).  The softmax warps meet on named barrier 1.
+            // (The decode step takes its next item from the queue only once
+            // the item is done: taken earlier, the last items of the queue
+            // would wait behind long ones, which costs more than the query
+            // load of a long item.)
+            if (PREFILL) {
+                if (tid == 0) next_sh = fetch();
+                asm volatile("bar.sync 1, 256;\n" ::: "memory");
+                const Item dn = describe(next_sh);
+                if (dn.run && !*abort_p && (wg >= n_act || done == n_tiles)) {
+                    load_q(dn, wg, row);
+                    pref_next = true;
+                }
+            }
+            if (wg < n_act) {
                 // the row's partial: normalised O and log2-sum-exp, once every MMA
                 // has completed (the single-shot barrier the MMA thread commits last)
                 bool fin = done == n_tiles;
@@ -691,19 +731,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                   : ctx     ? (size_t)p.mq_base + (size_t)r * p.H + h
                                             : ((size_t)rho * p.max_q_total + r) * p.H + h;
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    #pragma unroll
+#pragma unroll
                 for (int q4 = 0; q4 < 4; q4++) {
                     unsigned o[32];
                     if (fin && n_tiles > 0) {
                         tmem_ld32(tO(wg) + lane_off + q4 * 32, o);   // warp-collective
                         tmem_wait_ld();
                     } else {
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; i++) o[i] = 0u;
                     }
                     if (row_ok && PREFILL) {
                         __half *po = p.out + prow * 128 + q4 * 32;
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; i += 8)
                             *reinterpret_cast<uint4 *>(po + i) = make_uint4(
                                 pack_half2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
@@ -712,7 +752,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                 pack_half2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
                     } else if (row_ok) {
                         float *po = p.part_o + prow * 128;
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; i += 4)
                             __stcg(reinterpret_cast<float4 *>(po + q4 * 32 + i),
                                    make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
@@ -749,7 +789,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             // four page boxes per d-half of a context stage (pages past the
             // context: page id num_blocks, zero fill)
             auto load_ctx = [&](unsigned dst, const CUtensorMap *tm, int j, unsigned mb) {
-    #pragma unroll
+#pragma unroll
                 for (int q4 = 0; q4 < 4; q4++) {
                     const int pg = 4 * j + q4;
                     const int blk = pg < n_pages ? blk_sh[pg] : p.num_blocks;
@@ -810,7 +850,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const unsigned kb = kstage(j % kStagesK);
                     for (int t = 0; t < n_act; t++) {
                         const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 8; kk++)
                             umma_ss(tS(t, j & 1), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
                                     sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
@@ -856,7 +896,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const unsigned vb = vstage(sv);
                     for (int t = 0; t < n_act; t++) {
                         const unsigned pa = sbase + pbuf(t, b);
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < 4; kk++)
                             umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                     (j > 0 || kk > 0));
@@ -874,6 +914,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // has completed: the barriers may be set up again for the next item
         tc_fence_before();
         __syncthreads();
+        if (tid == 0 && !PREFILL) next_sh = fetch();
         if (tid == 0 && !*abort_p) {
             for (int s = 0; s < kStagesK; s++) {
                 mbar_inval(bar(kBarKFull + s));
@@ -887,9 +928,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
             mbar_inval(bar(kBarQFull));
             mbar_inval(bar(kBarFin));
-    }
+        }
+        if (!PREFILL) __syncthreads();
+        tc_fence_after();
+        item = *abort_p ? n_items : next_sh;
+        q_pref = pref_next;
     }
 
+    // query rows prefetched for an item that did not run (after a wait gave up)
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
