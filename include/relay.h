@@ -96,7 +96,7 @@ typedef enum {
 #define RELAY_FLAG_BAD_CTX_LEN  2u  /* ctx_lens[b] outside [0, 16*max_blocks_per_seq] */
 #define RELAY_FLAG_BAD_BLOCK    4u  /* a block id outside [0, num_blocks) */
 #define RELAY_FLAG_Q_TOTAL      8u  /* sum of q_lens above max_q_total */
-#define RELAY_FLAG_WAIT_TIMEOUT 16u  /* a bounded wait inside the tensor-core system step gave up;
+#define RELAY_FLAG_WAIT_TIMEOUT 16u  /* a bounded wait inside the tensor-core kernel gave up;
                                        that call's outputs are not valid */
 
 /* Opaque CUDA stream (binary-compatible with cudaStream_t); NULL = legacy stream. */
@@ -165,17 +165,24 @@ relay_status_t relay_fuse(const relay_dims_t *dims, const float *o_sys, const fl
                           void *out, float *lse_out, relay_stream_t stream);
 
 /* All three steps, queued on `stream` as two kernels, or three when the
- * system step runs on the tensor cores (all of them fit in one CUDA graph):
- *  0. (D = 128 and more than 256 query rows per KV head, counting the query
- *     heads of a group: the system step is compute-bound) a tcgen05 kernel
- *     computes the system partials: one CTA per KV head, pair of 128-row
- *     tiles and range of system keys;
- *  1. a persistent grid (one CTA per SM) works through system items (one
- *     KV head, a range of system keys, up to 64 query rows of the batch: the
- *     system KV is streamed once per batch) -- unless step 0 ran -- and
- *     context items (one request, one head or head group, a range of its
- *     paged context); each item writes an fp32 partial result and its
- *     log-sum-exp to the workspace;
+ * tensor-core kernel runs in front (all of them fit in one CUDA graph):
+ *  0. (D = 128, and more than 256 query rows per KV head counting the query
+ *     heads of a group, where the system step is compute-bound; or requests
+ *     of Lq * H / Hkv >= 64 rows per KV head, whose own contexts are as dense)
+ *     a persistent tcgen05 kernel (one CTA per SM at most) computes the
+ *     system partials -- items of one KV head, a pair of 128-row tiles and a
+ *     range of system keys -- and the context partials of requests with
+ *     several rows -- items of one request, a pair of its row tiles and one
+ *     KV head, over its whole context; when the batch also has one-row
+ *     requests, some of its SMs are left to step 1 from the start;
+ *  1. a persistent grid (one CTA per SM), a programmatic dependent of step
+ *     0 when that runs, works through system items (one KV head, a range of
+ *     system keys, up to 64 query rows of the batch: the system KV is
+ *     streamed once per batch) -- unless step 0 took them -- and context
+ *     items (one request, one head or head group, a range of its paged
+ *     context; those of several-row requests unless step 0 took them); each
+ *     item writes an fp32 partial result and its log-sum-exp to the
+ *     workspace;
  *  2. a merge kernel, launched as a programmatic dependent of step 1,
  *     combines each (row, head)'s partials -- the system ranges and the
  *     context splits -- into `out` (fp16) and `lse_out` (fp32 natural log,
