@@ -591,9 +591,10 @@ __device__ __forceinline__ size_t part_slot(const Params &p, int j, int n_sys, b
 
 // Merge the partials of one output row (compact row r = row i of request b,
 // head h) into the output: the convex combination of the parts weighted by
-// their softmax mass.  One warp; lane k loads the log-sum-exp of part k (one
-// round trip), then the parts' output rows are loaded eight at a time with
-// all eight loads in flight together.  Lane t handles D/32 adjacent elements.
+// their softmax mass.  One warp; lane k loads the log-sum-exp of part k and
+// every lane the first CH parts' output rows, all in one round trip; further
+// parts follow CH at a time with all CH loads in flight together.  Lane t
+// handles D/32 adjacent elements.
 template <int D, int CH = 16>   // CH: partial rows in flight per lane (one round for up to CH partials)
 __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys, int n_ctx, bool dec,
                           bool have_lk0 = false, float lk0 = 0.f)
@@ -611,8 +612,32 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
     float M = kNegInf, W = 0.f, acc[V];
 #pragma unroll
     for (int v = 0; v < V; v++) acc[v] = 0.f;
+    // CH partial rows of parts j0 + c0 .. into x (zeros past cnt)
+    auto load_parts = [&](float (&x)[CH][V], int j0, int c0, int cnt) {
+#pragma unroll
+        for (int k = 0; k < CH; k++) {
+            if (c0 + k < cnt) {
+                const float *src = p.part_o + slot(j0 + c0 + k) * D + d0;
+                if constexpr (V == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                    x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                    x[k][0] = t.x; x[k][1] = t.y;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; v++) x[k][v] = 0.f;
+            }
+        }
+    };
     for (int j0 = 0; j0 < n; j0 += 32) {
         const int cnt = min(32, n - j0);
+        // the first CH partial rows of the chunk are requested together with
+        // its log-sum-exps (the rows do not depend on them, only their
+        // weights do): one round trip for a row of at most CH parts
+        float x[CH][V];
+        load_parts(x, j0, 0, cnt);
         float lk = kNegInf;      // lane k: log-sum-exp of part j0 + k
         if (j0 == 0 && have_lk0) {
             lk = lane < cnt ? lk0 : kNegInf;
@@ -631,24 +656,7 @@ __device__ void merge_row(const Params &p, int r, int b, int i, int h, int n_sys
         M = Mn;
         const float wk = ex2(lk - M);
         for (int c0 = 0; c0 < cnt; c0 += CH) {
-            float x[CH][V];
-#pragma unroll
-            for (int k = 0; k < CH; k++) {
-                const int j = j0 + c0 + k;
-                if (c0 + k < cnt) {
-                    const float *src = p.part_o + slot(j) * D + d0;
-                    if constexpr (V == 4) {
-                        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-                        x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
-                    } else {
-                        const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-                        x[k][0] = t.x; x[k][1] = t.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int v = 0; v < V; v++) x[k][v] = 0.f;
-                }
-            }
+            if (c0 > 0) load_parts(x, j0, c0, cnt);
 #pragma unroll
             for (int k = 0; k < CH; k++) {
                 const float w = __shfl_sync(0xffffffffu, wk, (c0 + k) & 31);
