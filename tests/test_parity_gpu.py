@@ -657,17 +657,22 @@ def test_tree_prefixes(name, groups, Lp):
 # segments; its context].  Cases: the Llama-2-7B batch with a 2048-token
 # global prompt and four 512-token group prompts; grouped-query heads; three
 # segments with an empty one and requests that see none (pure context, or
-# nothing at all); multi-row requests.
+# nothing at all); multi-row requests, on the streaming kernel and (64-row
+# chunks at D = 128) with their contexts on the tensor cores.
 PREFIX_CASES = [
     ("llama2_7b", {}, [2048, 512, 512, 512, 512], lambda b: 1 | (2 << (b % 4))),
     ("tiny_gqa", {}, [256, 40, 40], lambda b: 1 | (2 << (b % 2))),
     ("tiny", dict(pool_blocks=40), [100, 0, 77], lambda b: [0b101, 0b001, 0b000, 0b110][b]),
     ("tiny", dict(Lq=3, chunk_requests=2), [64, 130], lambda b: [1, 3, 2, 3][b]),
+    # 64-row chunks at D = 128: their own contexts run on the tensor cores
+    # while the segments stay on the streaming kernel
+    ("llama2_7b", dict(B=6, Lq=64, chunk_requests=3), [300, 200], lambda b: [1, 3, 2, 3, 1, 2][b]),
 ]
 
 
 @pytest.mark.parametrize("name,over,lens,mask_of", PREFIX_CASES,
-                         ids=["llama2_7b_global_4groups", "gqa_2groups", "empty_and_unseen", "chunks"])
+                         ids=["llama2_7b_global_4groups", "gqa_2groups", "empty_and_unseen", "chunks",
+                              "chunks_tensor_cores"])
 def test_prefix_segments(name, over, lens, mask_of):
     import shared_prompt_decode_gb300 as relay
     from dataclasses import replace
