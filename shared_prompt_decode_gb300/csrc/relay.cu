@@ -54,7 +54,7 @@ cudaError_t prepare_one(int *occ)
 // inside the streaming kernel, where it is memory-bound and overlaps context.
 constexpr int kTcMinRows = 256;
 constexpr int kTcCtxMinRows = 64;      // rows of a request per KV head (Lq G) for its context on tcgen05
-constexpr int kTcYieldPct = 13;        // share of the SMs that stream decode contexts beside the tensor cores
+constexpr int kTcYieldPct = 13;        // most SMs that stream decode contexts beside the tensor cores, %
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -131,16 +131,6 @@ relay_status_t check_dims(const relay_dims_t *d)
 }
 
 int tc_pairs(int Mtot) { return ((Mtot + tc::kRowsTC - 1) / tc::kRowsTC + 1) / 2; }
-
-// CTAs of a tensor-core grid of `grid` CTAs that hand their SMs to the
-// streaming kernel when the batch has decode requests (the device decides
-// whether it has): kTcYieldPct of the SMs stream, counting those the grid
-// leaves free anyway; at least one CTA stays.
-int tc_yield(int sms, int grid)
-{
-    const int want = (sms * kTcYieldPct + 50) / 100 - (sms - grid);
-    return std::max(0, std::min(want, grid - 1));
-}
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (the library links only the CUDA runtime).
@@ -516,7 +506,9 @@ relay_status_t launch_relay(const relay_dims_t *d, int mode, Params p, void *ws,
         }
         // persistent: one CTA per SM at most
         const long long tc_grid = std::min<long long>(pl.n_tc_sys + pl.n_tc_ctx, dev->sms);
-        t.n_yield = tc_yield(dev->sms, (int)tc_grid);
+        t.n_yield = (dev->sms * kTcYieldPct + 50) / 100;
+        t.sms = dev->sms;
+        t.sys_stages = (float)pl.n_tc_sys * (float)((pl.sys_range + tc::kKeysTC - 1) / tc::kKeysTC);
         tc::sys_tc_kernel<false><<<(unsigned)tc_grid, tc::kThreadsTC, tc::kSmemTC, s>>>(tmK, tmV, tmKc, tmVc, t);
         if (cudaGetLastError() != cudaSuccess) return RELAY_ERR_CUDA;
     }

@@ -325,7 +325,9 @@ struct TcParams {
     int max_blocks, num_blocks;
     long long mq_base;               // partial row of compact row r, head h: mq_base + r * H + h
     unsigned *queue;                 // decode step: [0] items taken, [1] CTAs done; zero before the launch and after
-    int n_yield;                     // CTAs that leave at once when the batch has decode requests
+    int n_yield;                     // at most this many SMs stream decode contexts beside the tensor cores
+    int sms;                         // SMs of the GPU
+    float sys_stages;                // 64-key stages of all system items
 };
 
 // tile pairs for Mv virtual rows
@@ -373,11 +375,15 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 // allocated once per CTA, the mbarriers are set up afresh for every item.
 // The last CTA to leave (queue[1] counts them) sets both words back to zero
 // for the next launch.
-// In a decode step whose batch also has decode requests, the last n_yield
-// CTAs leave at once: the streaming kernel, a programmatic dependent of this
-// grid, starts on those SMs and streams the decode requests' contexts while
-// the tensor cores of the others run; it takes the remaining SMs as this
-// grid's CTAs leave.
+// In a decode step whose batch also has decode requests, the last CTAs leave
+// at once: the streaming kernel, a programmatic dependent of this grid,
+// starts on those SMs and streams the decode requests' contexts while the
+// tensor cores of the others run; it takes the remaining SMs as this grid's
+// CTAs leave.  As many SMs stream (counting those this grid leaves free
+// anyway) as the decode bytes need to finish within the tensor-core phase,
+// at most n_yield, from two rates measured on GB300: a 64-key stage of a
+// tile pair takes about 1.04 us, and a streaming CTA beside the tensor
+// cores moves about 76 GB/s.  Every CTA computes the same count.
 template <bool PREFILL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     sys_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     __shared__ int ip[kMaxBatchTC + 1];          // context items (tile pairs) before request b
     __shared__ int cn_sh[kMaxBatchTC];           // context length of request b
     __shared__ int blk_sh[kMaxPagesTC];          // page ids of a context item
-    __shared__ int next_sh, dec_sh;
+    __shared__ int next_sh, yield_sh;
     __shared__ unsigned tmem_base_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -410,7 +416,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // context).
     if (!PREFILL && warp == 0) {
         int run_q = 0, run_i = 0;
-        bool dec = false;
+        int dec_pages = 0, ctx_stages = 0;    // decode pages of one KV head; context stages of one KV head
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int b = b0 + lane;
             int ql = 0, n = 0;
@@ -421,8 +427,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (n < 0 || n > p.max_blocks * kPageTC) { ql = 0; n = 0; }
                 cn_sh[b] = n;
             }
-            dec |= ql == 1 && n > 0;
             const int it = (p.ctx_pairs > 0 && ql > 1) ? tile_pairs(ql * p.G) : 0;
+            dec_pages += ql == 1 ? (n + kPageTC - 1) / kPageTC : 0;
+            ctx_stages += it * ((n + kKeysTC - 1) / kKeysTC);
             const int iq = warp_incl_scan(ql), ii = warp_incl_scan(it);
             if (b < p.B) {
                 qo[b] = run_q + iq - ql;
@@ -431,17 +438,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             run_q += __shfl_sync(0xffffffffu, iq, 31);
             run_i += __shfl_sync(0xffffffffu, ii, 31);
         }
-        dec = __any_sync(0xffffffffu, dec);
+        dec_pages = __reduce_add_sync(0xffffffffu, dec_pages);
+        ctx_stages = __reduce_add_sync(0xffffffffu, ctx_stages);
         if (lane == 0) {
             qo[p.B] = run_q;
             ip[p.B] = run_i;
-            dec_sh = dec ? 1 : 0;
+            int y = 0;
+            if (dec_pages > 0) {
+                const float tc_us = (p.sys_stages + (float)ctx_stages * p.Hkv) * 1.04f / (float)p.sms;
+                const float bytes = (float)dec_pages * p.Hkv * (kPageTC * 128 * 2 * 2);
+                const float need = tc_us > 1.f ? ceilf(bytes / (76.0e3f * tc_us)) : (float)p.n_yield;
+                y = min((int)fminf(need, (float)p.n_yield), p.n_yield) - (p.sms - (int)gridDim.x);
+                y = max(0, min(y, (int)gridDim.x - 1));
+            }
+            yield_sh = y;
         }
     }
     if (tid == 0) abort_sh = 0;
     __syncthreads();
     const int n_items = PREFILL ? p.pairs * p.Hkv : p.n_sys + ip[p.B] * p.Hkv;
-    const bool yield = !PREFILL && dec_sh && (int)blockIdx.x >= (int)gridDim.x - p.n_yield;
+    const bool yield = !PREFILL && (int)blockIdx.x >= (int)gridDim.x - yield_sh;
     if (!yield && warp == kWarpMmaS) {
         const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(&tmem_base_sh));
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst), "n"(kTmemCols)
