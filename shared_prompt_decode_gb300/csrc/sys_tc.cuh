@@ -4,42 +4,42 @@
 // "RelayAttention": the per-request matrix-vector products over the shared
 // system prompt grouped into one matrix-matrix product).
 //
-// One CTA per item: KV head hk, a pair of 128-row tiles of its virtual rows
-// (v = r * G + c: query row r of the batch with query head hk * G + c, so
-// under grouped-query attention the heads of a group share every K/V stage
-// too; multi-head: G = 1, v = r), a range of system keys.  Both tiles share
-// every K/V stage.  Warps
-// have fixed roles:
+// An item: KV head hk, a pair of 128-row tiles of its virtual rows (v = r *
+// G + c: query row r of the batch with query head hk * G + c, so under
+// grouped-query attention the heads of a group share every K/V stage too;
+// multi-head: G = 1, v = r), a range of keys.  Both tiles share every K/V
+// stage.  Warps have fixed roles:
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile; row t of a tile
 //                   lives in TMEM lane t and is owned by thread t, so the
 //                   online softmax needs no cross-thread reduction
 //   warp 8          streams 64-key K and V stages in with TMA (128-byte
-//                   swizzle, zero fill past the end of the prompt), K and V
-//                   on rings of their own
+//                   swizzle, zero fill past the end of the keys), K and V on
+//                   4-stage rings of their own
 //   warp 9          owns TMEM and issues the S MMAs from one thread
 //   warp 10         issues the PV MMAs from one thread
 // Per 64-key stage j and query tile:
 //   S = Q K^T        tcgen05.mma kind::f16, M=128 N=64, Q and K K-major in
 //                    shared memory, fp32 into TMEM S buffer j % 2
-//   P = exp2(S - m)  by the tile's warpgroup, fp16, into shared-memory P
-//                    buffer j % 2
-//   O += P V         tcgen05.mma, M=128 N=128: P and V from shared memory, V
-//                    in its natural [key][d] order (MN-major), never transposed
-// The S thread runs two stages ahead of the PV thread: S(j+2) is issued
-// while PV(j) is.  S and P are double-buffered.  A thread that has MMAs in
-// flight waits for them to drain before its next shared-memory read
-// completes, so every barrier check on an issuing thread empties the tensor
-// pipe.  The MMA threads therefore check one barrier per stage: READY(j),
-// raised by the warpgroups once P(j) is stored (so S(j) has been read, and
-// its S buffer may take S(j+2)) and once they have seen V(j) and K(j+2)
-// land; the two threads' checks overlap each other's MMAs.
-// Each barrier signalled per stage has one instance per buffer, so that no
-// parity wait can be two phases behind.  O is rescaled only when a row's
-// running maximum grows by more than 2^8 (P <= 256 otherwise, well inside
-// fp16).  Every wait is bounded in time; a wait that gives up raises
+//   P = exp2(S - m)  by the tile's warpgroup, as fp16 pairs into the first 32
+//                    columns of the same S buffer (tcgen05.st)
+//   O += P V         tcgen05.mma, M=128 N=128: P from TMEM, V from shared
+//                    memory in its natural [key][d] order (MN-major), never
+//                    transposed
+// The PV thread issues PV(j) on READY(j), raised by the warpgroups once P(j)
+// is in TMEM and they have seen V(j) and K(j+2) land; the S thread issues
+// S(j+2) into the same S buffer once PV(j) has completed (O-done(j)).  A
+// thread that has MMAs in flight waits for them to drain before its next
+// shared-memory read completes, so every barrier check on an issuing thread
+// empties the tensor pipe: each MMA thread checks one barrier per stage, and
+// the two threads' checks overlap each other's MMAs.
+// Each barrier signalled per stage has one instance per buffer or ring slot,
+// so that no parity wait can be two phases behind.  O is rescaled only when a
+// row's running maximum grows by more than 2^8 (P <= 256 otherwise, well
+// inside fp16).  Every wait is bounded in time; a wait that gives up raises
 // RELAY_FLAG_WAIT_TIMEOUT and the CTA drains its copies and MMAs before it
 // frees TMEM and leaves.  Each row's result is one fp32 partial (normalised
-// output and log2-sum-exp), merged later with the context partials.
+// output and log2-sum-exp), merged later with the context partials, or
+// (prefill) the final fp16 row and its log-sum-exp.
 #pragma once
 
 #include <cuda.h>
@@ -55,7 +55,7 @@ constexpr int kKeysTC = 64;           // keys per K/V stage
 constexpr int kPageTC = 16;           // tokens per page of the paged pool
 constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
 constexpr int kMaxBatchTC = 512;      // requests of a batch
-constexpr int kStagesK = 3, kStagesV = 2;   // V stage j % 2 is freed by the O-done barrier of PV(j)
+constexpr int kStagesK = 4, kStagesV = 4;   // K stage j % 4 is freed when S(j) completes, V stage j % 4 when PV(j) does
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
 // A protocol wait gives up after RELAY_WAIT_LIMIT_NS (1 s).  A test build
@@ -71,12 +71,10 @@ constexpr unsigned long long kDrainNs = 1000000000ull;
 // shared-memory map (byte offsets from a 1024-aligned base), D = 128
 constexpr int kHalfQ = kRowsTC * 128;             // one d-half of a Q tile: [128 rows][64 d] fp16 = 16 KB
 constexpr int kQTile = 2 * kHalfQ;                // 32 KB
-constexpr int kPBuf = kRowsTC * kKeysTC * 2;      // one P buffer: [128 rows][64 keys] fp16 = 16 KB
 constexpr int kHalfKV = kKeysTC * 128;            // one d-half of a K or V stage: [64 keys][64 d] = 8 KB
 constexpr int kStageBytes = 2 * kHalfKV;          // a K stage or a V stage: two d-halves
 constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + 2 * kQTile;         // [tile][buffer]
-constexpr int kOffK = kOffP + 4 * kPBuf;
+constexpr int kOffK = kOffQ + 2 * kQTile;
 constexpr int kOffV = kOffK + kStagesK * kStageBytes;
 constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
 constexpr int kNumBars = 24;
@@ -86,9 +84,9 @@ constexpr int kTmemCols = 512;
 constexpr unsigned kColO = 0, kColS = 256;
 
 // mbarrier slots
-constexpr int kBarKFull = 0, kBarKEmpty = 3, kBarVFull = 6;                  // per stage
-constexpr int kBarSFull = 10, kBarReady = 12, kBarODone = 14;               // per buffer, both tiles
-constexpr int kBarQFull = 16, kBarFin = 17;
+constexpr int kBarKFull = 0, kBarKEmpty = 4, kBarVFull = 8, kBarVEmpty = 12;   // per stage
+constexpr int kBarSFull = 16, kBarReady = 18, kBarODone = 20;                   // per S buffer, both tiles
+constexpr int kBarQFull = 22, kBarFin = 23;
 
 // --------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count)
@@ -481,7 +479,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     auto tS = [&](int t, int b) { return tmem + kColS + (unsigned)(t * 128 + b * 64); };
     auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
     auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
-    auto pbuf = [&](int t, int b) { return (unsigned)(kOffP + (t * 2 + b) * kPBuf); };
     // An item's coordinates.  run: it has rows (uniform over the CTA).
     struct Item {
         bool ctx, run;
@@ -576,8 +573,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_init(bar(kBarKFull + s), 1);
                 mbar_init(bar(kBarKEmpty + s), 1);
             }
-            for (int s = 0; s < kStagesV; s++) mbar_init(bar(kBarVFull + s), 1);
-            for (int i = 0; i < 2; i++) {                // per buffer
+            for (int s = 0; s < kStagesV; s++) {
+                mbar_init(bar(kBarVFull + s), 1);
+                mbar_init(bar(kBarVEmpty + s), 1);
+            }
+            for (int i = 0; i < 2; i++) {                // per S buffer
                 mbar_init(bar(kBarSFull + i), 1);
                 mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
                 mbar_init(bar(kBarODone + i), 1);
@@ -640,7 +640,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const float mraw =
                         max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                     const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
-                    bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
                     // lazy rescale: only when this row's max grows by more than 8 (log2)
                     const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
                     bool rescaled = false;
@@ -651,7 +650,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
                             ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
                             if (!__all_sync(0xffffffffu, ok)) break;
-                            pbuf_free = true;
                             tc_fence_after();
 #pragma unroll
                             for (int q4 = 0; q4 < 4; q4++) {
@@ -685,17 +683,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
                         l_run += a0 + a1;
                     }
-                    if (!pbuf_free) {
-                        ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
-                        if (!__all_sync(0xffffffffu, ok)) break;
-                    }
-                    // P row into the K-major, 128-byte-swizzled buffer the PV MMA reads
-                    unsigned char *pr = gbase + pbuf(wg, b);
-#pragma unroll
-                    for (int c = 0; c < 8; c++)
-                        *reinterpret_cast<uint4 *>(pr + sw_off(row, c)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    fence_async_smem();
+                    // P row, fp16 pairs, into the first 32 columns of this row's
+                    // S buffer (S(j) is in registers; S(j+2), the next writer,
+                    // is issued only once PV(j) has read P(j)): the A operand of
+                    // the PV MMA, read from TMEM
+                    tmem_st32(tS(wg, b) + lane_off, pk);
+                    tmem_wait_st();
                     // the MMA threads check only READY: V(j) and K(j+2) must have landed
                     ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
                     if (ok && j + 2 < n_tiles)
@@ -831,8 +824,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         jk++;
                         progress = true;
                     }
-                    // V stage jv % 2 held V(jv-2): free once PV(jv-2) has completed
-                    if (jv < n_tiles && (jv < kStagesV || mbar_test(bar(kBarODone + (jv & 1)), ((jv - 2) >> 1) & 1))) {
+                    // V stage jv % kStagesV held V(jv - kStagesV): free once that PV has completed
+                    if (jv < n_tiles &&
+                        (jv < kStagesV || mbar_test(bar(kBarVEmpty + jv % kStagesV), ((jv / kStagesV) - 1) & 1))) {
                         const int s = jv % kStagesV, z = key0 + jv * kKeysTC;
                         mbar_expect_tx(bar(kBarVFull + s), kStageBytes);
                         if (ctx) {
@@ -883,8 +877,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     issue_s(j);
                 }
                 for (int j = 0; ok && j + 2 < n_tiles; j++) {
-                    // READY(j): S(j) read (its buffer is free) and K(j+2) landed
-                    ok = mbar_wait(bar(kBarReady + (j & 1)), (j >> 1) & 1, abort_p);
+                    // O-done(j): PV(j) has read P(j), which shares S buffer j % 2
+                    // with S(j + 2); before it, READY(j) saw K(j + 2) land
+                    ok = mbar_wait(bar(kBarODone + (j & 1)), (j >> 1) & 1, abort_p);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j + 2);
@@ -911,18 +906,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     tc_fence_after();
                     const unsigned vb = vstage(sv);
                     for (int t = 0; t < n_act; t++) {
-                        const unsigned pa = sbase + pbuf(t, b);
+                        // A = P(j) from TMEM: 16 keys = 8 columns of fp16 pairs per MMA
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++)
-                            umma_ss(tO(t), sw128_desc(pa + kk * 32), sw128_desc(vb + kk * 2048, kHalfKV), idO,
+                            umma_ts(tO(t), tS(t, b) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                     (j > 0 || kk > 0));
                     }
-                    umma_commit(bar(kBarODone + b));      // also frees V stage sv for the producer
+                    umma_commit(bar(kBarODone + b));
+                    umma_commit(bar(kBarVEmpty + sv));    // V stage sv free for the producer
                     n_pv++;
                 }
                 umma_commit(bar(kBarFin));
                 mbar_drain(bar(kBarFin), 0);
                 for (int b = 0; b < 2 && b < n_pv; b++) mbar_drain(bar(kBarODone + b), ((n_pv - 1 - b) >> 1) & 1);
+                for (int v = 0; v < kStagesV && v < n_pv; v++)
+                    mbar_drain(bar(kBarVEmpty + v), ((n_pv - 1 - v) / kStagesV) & 1);
             }
         }
 
@@ -936,7 +934,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_inval(bar(kBarKFull + s));
                 mbar_inval(bar(kBarKEmpty + s));
             }
-            for (int s = 0; s < kStagesV; s++) mbar_inval(bar(kBarVFull + s));
+            for (int s = 0; s < kStagesV; s++) {
+                mbar_inval(bar(kBarVFull + s));
+                mbar_inval(bar(kBarVEmpty + s));
+            }
             for (int i = 0; i < 2; i++) {
                 mbar_inval(bar(kBarSFull + i));
                 mbar_inval(bar(kBarReady + i));
