@@ -55,7 +55,7 @@ constexpr int kKeysTC = 64;           // keys per K/V stage
 constexpr int kPageTC = 16;           // tokens per page of the paged pool
 constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
 constexpr int kMaxBatchTC = 512;      // requests of a batch
-constexpr int kStagesK = 4, kStagesV = 4;   // K stage j % 4 is freed when S(j) completes, V stage j % 4 when PV(j) does
+constexpr int kStagesK = 4, kStagesV = 4;   // K stage j is freed when S(j) completes, V stage j when PV(j) does
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
 // A protocol wait gives up after RELAY_WAIT_LIMIT_NS (1 s).  A test build
@@ -77,16 +77,18 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 2 * kQTile;
 constexpr int kOffV = kOffK + kStagesK * kStageBytes;
 constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
-constexpr int kNumBars = 24;
-constexpr int kSmemTC = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
+constexpr int kSmemTC = kOffBar + 32 * 8 + 1024;   // barriers (at most 32) + alignment slack
 // TMEM columns: O tile 0 | O tile 1 | S tile 0 (2 buffers) | S tile 1 (2 buffers)
 constexpr int kTmemCols = 512;
 constexpr unsigned kColO = 0, kColS = 256;
 
 // mbarrier slots
-constexpr int kBarKFull = 0, kBarKEmpty = 4, kBarVFull = 8, kBarVEmpty = 12;   // per stage
-constexpr int kBarSFull = 16, kBarReady = 18, kBarODone = 20;                   // per S buffer, both tiles
-constexpr int kBarQFull = 22, kBarFin = 23;
+constexpr int kBarKFull = 0, kBarKEmpty = kStagesK;                           // per K stage
+constexpr int kBarVFull = 2 * kStagesK, kBarVEmpty = 2 * kStagesK + kStagesV;   // per V stage
+constexpr int kBarSFull = 2 * (kStagesK + kStagesV);                           // per S buffer, both tiles
+constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4;
+constexpr int kBarQFull = kBarSFull + 6, kBarFin = kBarSFull + 7;
+static_assert(kBarFin < 32, "mbarrier slots");
 
 // --------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count)
