@@ -19,19 +19,20 @@
 //   warp 10         issues the PV MMAs from one thread
 // Per 64-key stage j and query tile:
 //   S = Q K^T        tcgen05.mma kind::f16, M=128 N=64, Q and K K-major in
-//                    shared memory, fp32 into TMEM S buffer j % 2
-//   P = exp2(S - m)  by the tile's warpgroup, as fp16 pairs into the first 32
-//                    columns of the same S buffer (tcgen05.st)
+//                    shared memory, fp32 into the tile's TMEM S buffer
+//   P = exp2(S - m)  by the tile's warpgroup, as fp16 pairs into TMEM P
+//                    buffer j % 2 (tcgen05.st)
 //   O += P V         tcgen05.mma, M=128 N=128: P from TMEM, V from shared
 //                    memory in its natural [key][d] order (MN-major), never
 //                    transposed
-// The PV thread issues PV(j) on READY(j), raised by the warpgroups once P(j)
-// is in TMEM and they have seen V(j) and K(j+2) land; the S thread issues
-// S(j+2) into the same S buffer once PV(j) has completed (O-done(j)).  A
-// thread that has MMAs in flight waits for them to drain before its next
-// shared-memory read completes, so every barrier check on an issuing thread
-// empties the tensor pipe: each MMA thread checks one barrier per stage, and
-// the two threads' checks overlap each other's MMAs.
+// The S thread issues S(j+1) on S-read(j), raised by the warpgroups as soon
+// as S(j) is in their registers and they have seen K(j+1) land, so S(j+1)
+// runs while they compute P(j); the PV thread issues PV(j) on READY(j),
+// raised once P(j) is in TMEM and V(j) has landed; P(j+2) waits for PV(j)
+// (O-done(j)).  A thread that has MMAs in flight waits for them to drain
+// before its next shared-memory read completes, so every barrier check on
+// an issuing thread empties the tensor pipe: each MMA thread checks one
+// barrier per stage, and the two threads' checks overlap each other's MMAs.
 // Each barrier signalled per stage has one instance per buffer or ring slot,
 // so that no parity wait can be two phases behind.  O is rescaled only when a
 // row's running maximum grows by more than 2^8 (P <= 256 otherwise, well
@@ -80,14 +81,16 @@ constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
 constexpr int kSmemTC = kOffBar + 32 * 8 + 1024;   // barriers (at most 32) + alignment slack
 // TMEM columns: O tile 0 | O tile 1 | S tile 0 (2 buffers) | S tile 1 (2 buffers)
 constexpr int kTmemCols = 512;
-constexpr unsigned kColO = 0, kColS = 256;
+// O tile t: columns 128 t ..; S tile t (one buffer): 256 + 64 t ..; P tile t
+// buffer b (fp16 pairs): 384 + 64 t + 32 b ..
+constexpr unsigned kColO = 0, kColS = 256, kColP = 384;
 
 // mbarrier slots
 constexpr int kBarKFull = 0, kBarKEmpty = kStagesK;                           // per K stage
 constexpr int kBarVFull = 2 * kStagesK, kBarVEmpty = 2 * kStagesK + kStagesV;   // per V stage
 constexpr int kBarSFull = 2 * (kStagesK + kStagesV);                           // per S buffer, both tiles
-constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4;
-constexpr int kBarQFull = kBarSFull + 6, kBarFin = kBarSFull + 7;
+constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4, kBarSRead = kBarSFull + 6;
+constexpr int kBarQFull = kBarSFull + 8, kBarFin = kBarSFull + 9;
 static_assert(kBarFin < 32, "mbarrier slots");
 
 // --------------------------------------------------------------------------- PTX wrappers
@@ -478,7 +481,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     tc_fence_after();
     const unsigned tmem = tmem_base_sh;
     auto tO = [&](int t) { return tmem + kColO + (unsigned)(t * 128); };
-    auto tS = [&](int t, int b) { return tmem + kColS + (unsigned)(t * 128 + b * 64); };
+    auto tS = [&](int t) { return tmem + kColS + (unsigned)(t * 64); };
+    auto tP = [&](int t, int b) { return tmem + kColP + (unsigned)(t * 64 + b * 32); };
     auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
     auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
     // An item's coordinates.  run: it has rows (uniform over the CTA).
@@ -583,6 +587,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_init(bar(kBarSFull + i), 1);
                 mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
                 mbar_init(bar(kBarODone + i), 1);
+                mbar_init(bar(kBarSRead + i), 4 * n_act);
             }
             mbar_init(bar(kBarQFull), 256);
             mbar_init(bar(kBarFin), 2);                  // one commit from each MMA thread
@@ -614,8 +619,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     float s[64];
                     {
                         unsigned a[32], c[32];
-                        tmem_ld32(tS(wg, b) + lane_off, a);
-                        tmem_ld32(tS(wg, b) + lane_off + 32, c);
+                        tmem_ld32(tS(wg) + lane_off, a);
+                        tmem_ld32(tS(wg) + lane_off + 32, c);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; i++) {
@@ -623,6 +628,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             s[32 + i] = __uint_as_float(c[i]);
                         }
                     }
+                    // S(j) is in registers: the S buffer may take S(j+1), whose
+                    // keys must have landed (the S thread checks only S-read)
+                    if (j + 1 < n_tiles)
+                        ok = mbar_wait(bar(kBarKFull + (j + 1) % kStagesK), ((j + 1) / kStagesK) & 1, abort_p);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kBarSRead + b));
                     const int kbase = key0 + j * kKeysTC;
                     // keys visible to this row: below lim
                     const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
@@ -644,7 +657,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
                     // lazy rescale: only when this row's max grows by more than 8 (log2)
                     const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
-                    bool rescaled = false;
+                    bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
                     if (__any_sync(0xffffffffu, grow)) {
                         const float mn = grow ? mt : m_run;
                         const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
@@ -652,6 +665,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
                             ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
                             if (!__all_sync(0xffffffffu, ok)) break;
+                            pbuf_free = true;
                             tc_fence_after();
 #pragma unroll
                             for (int q4 = 0; q4 < 4; q4++) {
@@ -663,7 +677,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                 tmem_st32(tO(wg) + lane_off + q4 * 32, o);
                             }
                             tmem_wait_st();
-                            rescaled = true;
                         }
                         l_run *= alpha;
                         m_run = mn;
@@ -685,16 +698,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
                         l_run += a0 + a1;
                     }
-                    // P row, fp16 pairs, into the first 32 columns of this row's
-                    // S buffer (S(j) is in registers; S(j+2), the next writer,
-                    // is issued only once PV(j) has read P(j)): the A operand of
+                    // P row, fp16 pairs, into P buffer j % 2 of this tile once
+                    // PV(j-2), its last reader, has completed: the A operand of
                     // the PV MMA, read from TMEM
-                    tmem_st32(tS(wg, b) + lane_off, pk);
+                    if (!pbuf_free) {
+                        ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
+                        if (!__all_sync(0xffffffffu, ok)) break;
+                        tc_fence_after();
+                    }
+                    tmem_st32(tP(wg, b) + lane_off, pk);
                     tmem_wait_st();
-                    // the MMA threads check only READY: V(j) and K(j+2) must have landed
+                    // the PV thread checks only READY: V(j) must have landed
                     ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
-                    if (ok && j + 2 < n_tiles)
-                        ok = mbar_wait(bar(kBarKFull + (j + 2) % kStagesK), ((j + 2) / kStagesK) & 1, abort_p);
                     if (!__all_sync(0xffffffffu, ok)) break;
                     if (ctx && wg == 0 && j == n_tiles - 1 && cn < n_pages * kPageTC) {
                         // the last page's slots past the context hold whatever the
@@ -864,7 +879,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
 #pragma unroll
                         for (int kk = 0; kk < 8; kk++)
-                            umma_ss(tS(t, j & 1), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
+                            umma_ss(tS(t), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
                                     sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
                     }
                     umma_commit(bar(kBarSFull + (j & 1)));
@@ -872,19 +887,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     n_s++;
                 };
                 bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
-                for (int j = 0; ok && j < n_tiles && j < 2; j++) {
-                    ok = mbar_wait(bar(kBarKFull + j % kStagesK), (j / kStagesK) & 1, abort_p);
-                    if (!ok) break;
+                if (ok && n_tiles > 0) ok = mbar_wait(bar(kBarKFull), 0, abort_p);
+                if (ok && n_tiles > 0) {
                     tc_fence_after();
-                    issue_s(j);
+                    issue_s(0);
                 }
-                for (int j = 0; ok && j + 2 < n_tiles; j++) {
-                    // O-done(j): PV(j) has read P(j), which shares S buffer j % 2
-                    // with S(j + 2); before it, READY(j) saw K(j + 2) land
-                    ok = mbar_wait(bar(kBarODone + (j & 1)), (j >> 1) & 1, abort_p);
+                for (int j = 0; ok && j + 1 < n_tiles; j++) {
+                    // S-read(j): S(j) is in the softmax warps' registers, so the
+                    // one S buffer may take S(j+1), and K(j+1) has landed
+                    ok = mbar_wait(bar(kBarSRead + (j & 1)), (j >> 1) & 1, abort_p);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 2);
+                    issue_s(j + 1);
                 }
                 // every S MMA has completed once the final barrier fires;
                 // the K-empty signals of the last stages, which nobody waits
@@ -911,7 +925,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         // A = P(j) from TMEM: 16 keys = 8 columns of fp16 pairs per MMA
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++)
-                            umma_ts(tO(t), tS(t, b) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
+                            umma_ts(tO(t), tP(t, b) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                     (j > 0 || kk > 0));
                     }
                     umma_commit(bar(kBarODone + b));
@@ -944,6 +958,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_inval(bar(kBarSFull + i));
                 mbar_inval(bar(kBarReady + i));
                 mbar_inval(bar(kBarODone + i));
+                mbar_inval(bar(kBarSRead + i));
             }
             mbar_inval(bar(kBarQFull));
             mbar_inval(bar(kBarFin));
