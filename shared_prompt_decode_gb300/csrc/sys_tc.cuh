@@ -25,14 +25,15 @@
 //   O += P V         tcgen05.mma, M=128 N=128: P from TMEM, V from shared
 //                    memory in its natural [key][d] order (MN-major), never
 //                    transposed
-// The S thread issues S(j+1) on S-read(j), raised by the warpgroups as soon
-// as S(j) is in their registers and they have seen K(j+1) land, so S(j+1)
-// runs while they compute P(j); the PV thread issues PV(j) on READY(j),
+// The S thread issues S(j+1) once K(j+1) has landed and on S-read(j), raised
+// by the warpgroups as soon as S(j) is in their registers, so S(j+1) runs
+// while they compute P(j); the PV thread issues PV(j) on READY(j),
 // raised once P(j) is in TMEM and V(j) has landed; P(j+2) waits for PV(j)
 // (O-done(j)).  A thread that has MMAs in flight waits for them to drain
 // before its next shared-memory read completes, so every barrier check on
-// an issuing thread empties the tensor pipe: each MMA thread checks one
-// barrier per stage, and the two threads' checks overlap each other's MMAs.
+// an issuing thread empties the tensor pipe: the PV thread checks one barrier
+// per stage; the S thread's K check empties the pipe of S(j), which S-read(j)
+// waits for anyway; the two threads' checks overlap each other's MMAs.
 // Each barrier signalled per stage has one instance per buffer or ring slot,
 // so that no parity wait can be two phases behind.  O is rescaled only when a
 // row's running maximum grows by more than 2^8 (P <= 256 otherwise, well
@@ -628,11 +629,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             s[32 + i] = __uint_as_float(c[i]);
                         }
                     }
-                    // S(j) is in registers: the S buffer may take S(j+1), whose
-                    // keys must have landed (the S thread checks only S-read)
-                    if (j + 1 < n_tiles)
-                        ok = mbar_wait(bar(kBarKFull + (j + 1) % kStagesK), ((j + 1) / kStagesK) & 1, abort_p);
-                    if (!__all_sync(0xffffffffu, ok)) break;
+                    // S(j) is in registers: the S buffer may take S(j+1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kBarSRead + b));
@@ -707,9 +704,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         tc_fence_after();
                     }
                     tmem_st32(tP(wg, b) + lane_off, pk);
-                    tmem_wait_st();
                     // the PV thread checks only READY: V(j) must have landed
+                    // (checked while the P store completes)
                     ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
+                    tmem_wait_st();
                     if (!__all_sync(0xffffffffu, ok)) break;
                     if (ctx && wg == 0 && j == n_tiles - 1 && cn < n_pages * kPageTC) {
                         // the last page's slots past the context hold whatever the
@@ -893,9 +891,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     issue_s(0);
                 }
                 for (int j = 0; ok && j + 1 < n_tiles; j++) {
-                    // S-read(j): S(j) is in the softmax warps' registers, so the
-                    // one S buffer may take S(j+1), and K(j+1) has landed
-                    ok = mbar_wait(bar(kBarSRead + (j & 1)), (j >> 1) & 1, abort_p);
+                    // K(j+1) landed (checking drains S(j), which has to complete
+                    // before S-read(j) anyway), then S-read(j): S(j) is in the
+                    // softmax warps' registers, so the one S buffer may take S(j+1)
+                    ok = mbar_wait(bar(kBarKFull + (j + 1) % kStagesK), ((j + 1) / kStagesK) & 1, abort_p);
+                    if (ok) ok = mbar_wait(bar(kBarSRead + (j & 1)), (j >> 1) & 1, abort_p);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j + 1);
