@@ -80,17 +80,16 @@ constexpr int kOffK = kOffQ + 2 * kQTile;
 constexpr int kOffV = kOffK + kStagesK * kStageBytes;
 constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
 constexpr int kSmemTC = kOffBar + 32 * 8 + 1024;   // barriers (at most 32) + alignment slack
-// TMEM columns: O tile 0 | O tile 1 | S tile 0 (2 buffers) | S tile 1 (2 buffers)
+// TMEM columns: O tile t: 128 t .. (128); S tile t (one buffer, fp32): 256 +
+// 64 t .. (64); P tile t buffer b (fp16 pairs): 384 + 64 t + 32 b .. (32)
 constexpr int kTmemCols = 512;
-// O tile t: columns 128 t ..; S tile t (one buffer): 256 + 64 t ..; P tile t
-// buffer b (fp16 pairs): 384 + 64 t + 32 b ..
 constexpr unsigned kColO = 0, kColS = 256, kColP = 384;
 
 // mbarrier slots
 constexpr int kBarKFull = 0, kBarKEmpty = kStagesK;                           // per K stage
 constexpr int kBarVFull = 2 * kStagesK, kBarVEmpty = 2 * kStagesK + kStagesV;   // per V stage
-constexpr int kBarSFull = 2 * (kStagesK + kStagesV);                           // per S buffer, both tiles
-constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4, kBarSRead = kBarSFull + 6;
+constexpr int kBarSFull = 2 * (kStagesK + kStagesV);                           // per stage parity, both tiles
+constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4, kBarSRead = kBarSFull + 6;   // per parity
 constexpr int kBarQFull = kBarSFull + 8, kBarFin = kBarSFull + 9;
 static_assert(kBarFin < 32, "mbarrier slots");
 
@@ -871,7 +870,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             if (lane == 0) {
                 const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
                 int n_s = 0;                             // S stages issued
-                auto issue_s = [&](int j) {              // S(j) of every tile into S buffer j % 2
+                auto issue_s = [&](int j) {              // S(j) of every tile into its S buffer
                     const unsigned kb = kstage(j % kStagesK);
                     for (int t = 0; t < n_act; t++) {
                         const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
