@@ -54,7 +54,7 @@ cudaError_t prepare_one(int *occ)
 // inside the streaming kernel, where it is memory-bound and overlaps context.
 constexpr int kTcMinRows = 256;
 constexpr int kTcCtxMinRows = 64;      // rows of a request per KV head (Lq G) for its context on tcgen05
-constexpr int kTcYieldPct = 13;        // most SMs that stream decode contexts beside the tensor cores, %
+constexpr int kTcYieldPct = 20;        // most SMs that stream decode contexts beside the tensor cores, %
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
