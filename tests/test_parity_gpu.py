@@ -381,6 +381,18 @@ def test_chunk_context_on_tensor_cores(name, over, ql, ctx):
     T.check_full(case, out2, lse2)
 
 
+def test_mixed_batch_few_decode_requests():
+    # prompt chunks on the tensor cores (system step and their own contexts)
+    # with only four decode requests streaming beside them: the grid yields
+    # only the SMs those requests need; every output against the oracle
+    w = synth.Workload("mixed_few_decode", B=12, H=8, D=128, Ls=4096, ctx_dist=("uniform", 1, 2048),
+                       value_scale=0.5, Lq=128, chunk_requests=8)
+    case = synth.make_case(w, 43)
+    assert case.total_q() > 256
+    out, lse = T.run_fused(case)
+    T.check_full(case, out, lse)
+
+
 def test_chunk_context_bad_block_is_flagged():
     # a page id outside the pool in a chunk request's context: read as zeros
     # and flagged; the next clean call in the same workspace is exact
