@@ -53,11 +53,11 @@ namespace relay {
 namespace tc {
 
 constexpr int kRowsTC = 128;          // query rows per tile (TMEM lanes)
-constexpr int kKeysTC = 64;           // keys per K/V stage
+constexpr int kKeysTC = 128;          // keys per K/V stage
 constexpr int kPageTC = 16;           // tokens per page of the paged pool
 constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
 constexpr int kMaxBatchTC = 512;      // requests of a batch
-constexpr int kStagesK = 4, kStagesV = 4;   // K stage j is freed when S(j) completes, V stage j when PV(j) does
+constexpr int kStagesK = 2, kStagesV = 2;   // K stage j is freed when S(j) completes, V stage j when PV(j) does
 constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
 constexpr int kThreadsTC = 352;
 // A protocol wait gives up after RELAY_WAIT_LIMIT_NS (1 s).  A test build
@@ -73,24 +73,29 @@ constexpr unsigned long long kDrainNs = 1000000000ull;
 // shared-memory map (byte offsets from a 1024-aligned base), D = 128
 constexpr int kHalfQ = kRowsTC * 128;             // one d-half of a Q tile: [128 rows][64 d] fp16 = 16 KB
 constexpr int kQTile = 2 * kHalfQ;                // 32 KB
-constexpr int kHalfKV = kKeysTC * 128;            // one d-half of a K or V stage: [64 keys][64 d] = 8 KB
+constexpr int kHalfKV = kKeysTC * 128;            // one d-half of a K or V stage: [128 keys][64 d] = 16 KB
 constexpr int kStageBytes = 2 * kHalfKV;          // a K stage or a V stage: two d-halves
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 2 * kQTile;
 constexpr int kOffV = kOffK + kStagesK * kStageBytes;
 constexpr int kOffBar = kOffV + kStagesV * kStageBytes;
 constexpr int kSmemTC = kOffBar + 32 * 8 + 1024;   // barriers (at most 32) + alignment slack
-// TMEM columns: O tile t: 128 t .. (128); S tile t (one buffer, fp32): 256 +
-// 64 t .. (64); P tile t buffer b (fp16 pairs): 384 + 64 t + 32 b .. (32)
+// TMEM columns: O tile t: 128 t .. (128); S, one buffer that the two tiles
+// take in turn (fp32): 256 .. (128); P tile t (fp16 pairs): 384 + 64 t .. (64)
 constexpr int kTmemCols = 512;
 constexpr unsigned kColO = 0, kColS = 256, kColP = 384;
+constexpr int kPagesPerStage = kKeysTC / kPageTC;   // page boxes per d-half of a context stage
+// a stage of a tile pair takes about this long (GB300), for the share of SMs
+// that stream decode contexts beside this grid
+constexpr float kStageUs = 1.56f;
 
 // mbarrier slots
 constexpr int kBarKFull = 0, kBarKEmpty = kStagesK;                           // per K stage
 constexpr int kBarVFull = 2 * kStagesK, kBarVEmpty = 2 * kStagesK + kStagesV;   // per V stage
-constexpr int kBarSFull = 2 * (kStagesK + kStagesV);                           // per stage parity, both tiles
-constexpr int kBarReady = kBarSFull + 2, kBarODone = kBarSFull + 4, kBarSRead = kBarSFull + 6;   // per parity
-constexpr int kBarQFull = kBarSFull + 8, kBarFin = kBarSFull + 9;
+constexpr int kBarSFull = 2 * (kStagesK + kStagesV);   // per tile: S of the tile in the S buffer
+constexpr int kBarSRead = kBarSFull + 2;                // per tile: that S in its warpgroup's registers
+constexpr int kBarReady = kBarSFull + 4, kBarODone = kBarSFull + 5;   // per stage, both tiles
+constexpr int kBarQFull = kBarSFull + 6, kBarFin = kBarSFull + 7;
 static_assert(kBarFin < 32, "mbarrier slots");
 
 // --------------------------------------------------------------------------- PTX wrappers
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             ip[p.B] = run_i;
             int y = 0;
             if (dec_pages > 0) {
-                const float tc_us = (p.sys_stages + (float)ctx_stages * p.Hkv) * 1.04f / (float)p.sms;
+                const float tc_us = (p.sys_stages + (float)ctx_stages * p.Hkv) * kStageUs / (float)p.sms;
                 const float bytes = (float)dec_pages * p.Hkv * (kPageTC * 128 * 2 * 2);
                 const float need = tc_us > 1.f ? ceilf(bytes / (76.0e3f * tc_us)) : (float)p.n_yield;
                 y = min((int)fminf(need, (float)p.n_yield), p.n_yield) - (p.sms - (int)gridDim.x);
@@ -481,8 +486,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     tc_fence_after();
     const unsigned tmem = tmem_base_sh;
     auto tO = [&](int t) { return tmem + kColO + (unsigned)(t * 128); };
-    auto tS = [&](int t) { return tmem + kColS + (unsigned)(t * 64); };
-    auto tP = [&](int t, int b) { return tmem + kColP + (unsigned)(t * 64 + b * 32); };
+    const unsigned tS = tmem + kColS;
+    auto tP = [&](int t) { return tmem + kColP + (unsigned)(t * 64); };
     auto kstage = [&](int s) { return sbase + kOffK + (unsigned)(s * kStageBytes); };
     auto vstage = [&](int s) { return sbase + kOffV + (unsigned)(s * kStageBytes); };
     // An item's coordinates.  run: it has rows (uniform over the CTA).
@@ -583,12 +588,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_init(bar(kBarVFull + s), 1);
                 mbar_init(bar(kBarVEmpty + s), 1);
             }
-            for (int i = 0; i < 2; i++) {                // per S buffer
-                mbar_init(bar(kBarSFull + i), 1);
-                mbar_init(bar(kBarReady + i), 4 * n_act);  // one arrival per warp of each active warpgroup
-                mbar_init(bar(kBarODone + i), 1);
-                mbar_init(bar(kBarSRead + i), 4 * n_act);
+            for (int t = 0; t < 2; t++) {                // per tile
+                mbar_init(bar(kBarSFull + t), 1);
+                mbar_init(bar(kBarSRead + t), 4);          // one arrival per warp of the tile's warpgroup
             }
+            mbar_init(bar(kBarReady), 4 * n_act);          // one arrival per warp of each active warpgroup
+            mbar_init(bar(kBarODone), 1);
             mbar_init(bar(kBarQFull), 256);
             mbar_init(bar(kBarFin), 2);                  // one commit from each MMA thread
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -612,99 +617,94 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int done = 0;
             if (wg < n_act) {
                 for (int j = 0; j < n_tiles; j++) {
-                    const int b = j & 1;
-                    bool ok = mbar_wait(bar(kBarSFull + b), (j >> 1) & 1, abort_p);
+                    bool ok = mbar_wait(bar(kBarSFull + wg), j & 1, abort_p);
                     if (!__all_sync(0xffffffffu, ok)) break;
                     tc_fence_after();
-                    float s[64];
+                    float s[128];
                     {
-                        unsigned a[32], c[32];
-                        tmem_ld32(tS(wg) + lane_off, a);
-                        tmem_ld32(tS(wg) + lane_off + 32, c);
+                        unsigned a[4][32];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; c4++) tmem_ld32(tS + lane_off + c4 * 32, a[c4]);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            s[i] = __uint_as_float(a[i]);
-                            s[32 + i] = __uint_as_float(c[i]);
-                        }
+                        for (int i = 0; i < 128; i++) s[i] = __uint_as_float(a[i >> 5][i & 31]);
                     }
-                    // S(j) is in registers: the S buffer may take S(j+1)
+                    // S(j) of this tile is in registers: the S buffer may take the next S
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kBarSRead + b));
+                    if (lane == 0) mbar_arrive(bar(kBarSRead + wg));
                     const int kbase = key0 + j * kKeysTC;
                     // keys visible to this row: below lim
                     const int lim = PREFILL ? r + 1 : ctx ? lim_ctx : key_hi;
                     if (kbase + kKeysTC > lim) {
 #pragma unroll
-                        for (int i = 0; i < 64; i++)
+                        for (int i = 0; i < 128; i++)
                             if (kbase + i >= lim) s[i] = kNegInf;
                     }
                     float mx[8];
 #pragma unroll
                     for (int k = 0; k < 8; k++) {
                         mx[k] = max3f(s[k], s[8 + k], s[16 + k]);
-                        mx[k] = max3f(mx[k], s[24 + k], s[32 + k]);
-                        mx[k] = max3f(mx[k], s[40 + k], s[48 + k]);
-                        mx[k] = fmaxf(mx[k], s[56 + k]);
+#pragma unroll
+                        for (int c = 24; c < 120; c += 16) mx[k] = max3f(mx[k], s[c + k], s[c + 8 + k]);
+                        mx[k] = fmaxf(mx[k], s[120 + k]);
                     }
                     const float mraw =
                         max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                     const float mt = mraw * p.scale_log2;       // scale > 0: the max commutes with it
                     // lazy rescale: only when this row's max grows by more than 8 (log2)
                     const bool grow = mt > m_run + 8.f || (m_run == kNegInf && mt != kNegInf);
-                    bool pbuf_free = j < 2;                     // PV(j-2), the last reader of P buffer b, done
-                    if (__any_sync(0xffffffffu, grow)) {
-                        const float mn = grow ? mt : m_run;
-                        const float alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
-                        if (j >= 1) {
-                            // O holds PV(0..j-1): wait for PV(j-1) (and so every earlier PV)
-                            ok = mbar_wait(bar(kBarODone + (b ^ 1)), ((j - 1) >> 1) & 1, abort_p);
-                            if (!__all_sync(0xffffffffu, ok)) break;
-                            pbuf_free = true;
-                            tc_fence_after();
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; q4++) {
-                                unsigned o[32];
-                                tmem_ld32(tO(wg) + lane_off + q4 * 32, o);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                                tmem_st32(tO(wg) + lane_off + q4 * 32, o);
-                            }
-                            tmem_wait_st();
-                        }
-                        l_run *= alpha;
-                        m_run = mn;
+                    const bool any_grow = __any_sync(0xffffffffu, grow);
+                    float mn = m_run, alpha = 1.f;
+                    if (any_grow) {
+                        mn = grow ? mt : m_run;
+                        alpha = (m_run == kNegInf) ? 0.f : ex2(m_run - mn);
                     }
-                    const float mu = (m_run == kNegInf) ? 0.f : m_run;
-                    unsigned pk[32];
+                    const float mu = (mn == kNegInf) ? 0.f : mn;
+                    unsigned pk[64];
                     const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nmu2 = f2_pack(-mu, -mu);
                     unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};     // pairs of +0.0f
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
+                    for (int i = 0; i < 64; i++) {
                         float x0, x1;
                         f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nmu2), x0, x1);
                         const float p0 = ex2(x0), p1 = ex2(x1);
                         ls[i & 3] = f2_add(ls[i & 3], f2_pack(p0, p1));
                         pk[i] = pack_half2(p0, p1);
                     }
+                    float lsum;
                     {
                         float a0, a1;
                         f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
-                        l_run += a0 + a1;
+                        lsum = a0 + a1;
                     }
-                    // P row, fp16 pairs, into P buffer j % 2 of this tile once
-                    // PV(j-2), its last reader, has completed: the A operand of
-                    // the PV MMA, read from TMEM
-                    if (!pbuf_free) {
-                        ok = mbar_wait(bar(kBarODone + b), ((j - 2) >> 1) & 1, abort_p);
+                    // PV(j-1), the last reader of this tile's P buffer and the
+                    // last writer of its O, has completed
+                    if (j >= 1) {
+                        ok = mbar_wait(bar(kBarODone), (j - 1) & 1, abort_p);
                         if (!__all_sync(0xffffffffu, ok)) break;
                         tc_fence_after();
                     }
-                    tmem_st32(tP(wg, b) + lane_off, pk);
+                    // P row, fp16 pairs, into this tile's P buffer: the A operand
+                    // of the PV MMA, read from TMEM
+                    tmem_st32(tP(wg) + lane_off, *reinterpret_cast<const unsigned(*)[32]>(pk));
+                    tmem_st32(tP(wg) + lane_off + 32, *reinterpret_cast<const unsigned(*)[32]>(pk + 32));
+                    if (any_grow && j >= 1) {
+                        // O holds PV(0..j-1): rescale it to the new running max
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) {
+                            unsigned o[32];
+                            tmem_ld32(tO(wg) + lane_off + q4 * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(tO(wg) + lane_off + q4 * 32, o);
+                        }
+                    }
+                    l_run = l_run * alpha + lsum;
+                    m_run = mn;
                     // the PV thread checks only READY: V(j) must have landed
-                    // (checked while the P store completes)
+                    // (checked while the TMEM stores complete)
                     ok = mbar_wait(bar(kBarVFull + j % kStagesV), (j / kStagesV) & 1, abort_p);
                     tmem_wait_st();
                     if (!__all_sync(0xffffffffu, ok)) break;
@@ -719,9 +719,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                                        (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                         fence_async_smem();
                     }
-                    tc_fence_before();   // S(j) loads (and a rescale's stores) before the MMAs that follow
+                    tc_fence_before();   // S(j) loads and the TMEM stores before the MMAs that follow
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kBarReady + b));
+                    if (lane == 0) mbar_arrive(bar(kBarReady));
                     done = j + 1;
                 }
             }
@@ -809,15 +809,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 __syncwarp();
                 if (__any_sync(0xffffffffu, bad_blk) && lane == 0) atomicOr(p.flags, RELAY_FLAG_BAD_BLOCK);
             }
-            // four page boxes per d-half of a context stage (pages past the
-            // context: page id num_blocks, zero fill)
+            // kPagesPerStage page boxes per d-half of a context stage (pages
+            // past the context: page id num_blocks, zero fill)
             auto load_ctx = [&](unsigned dst, const CUtensorMap *tm, int j, unsigned mb) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) {
-                    const int pg = 4 * j + q4;
+                for (int q = 0; q < kPagesPerStage; q++) {
+                    const int pg = kPagesPerStage * j + q;
                     const int blk = pg < n_pages ? blk_sh[pg] : p.num_blocks;
-                    tma_load_4d(dst + q4 * (kPageTC * 128), tm, 0, 0, hk, blk, mb);
-                    tma_load_4d(dst + kHalfKV + q4 * (kPageTC * 128), tm, 64, 0, hk, blk, mb);
+                    tma_load_4d(dst + q * (kPageTC * 128), tm, 0, 0, hk, blk, mb);
+                    tma_load_4d(dst + kHalfKV + q * (kPageTC * 128), tm, 64, 0, hk, blk, mb);
                 }
             };
             if (lane == 0) {
@@ -869,35 +869,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             // ------------------------------------------------------------ S = Q K^T
             if (lane == 0) {
                 const uint32_t idS = idesc_f16(kRowsTC, kKeysTC);
-                int n_s = 0;                             // S stages issued
-                auto issue_s = [&](int j) {              // S(j) of every tile into its S buffer
+                int n_s = 0;                             // stages whose S MMAs have all been issued
+                int pt = -1, pj = 0;                     // the S last issued into the buffer: tile, stage
+                bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
+                for (int j = 0; ok && j < n_tiles; j++) {
+                    // K(j) landed (checking drains the S in flight, which has to
+                    // complete before its warpgroup reads it anyway)
+                    ok = mbar_wait(bar(kBarKFull + j % kStagesK), (j / kStagesK) & 1, abort_p);
                     const unsigned kb = kstage(j % kStagesK);
-                    for (int t = 0; t < n_act; t++) {
+                    for (int t = 0; ok && t < n_act; t++) {
+                        // the buffer's previous S is in its warpgroup's registers
+                        if (pt >= 0) ok = mbar_wait(bar(kBarSRead + pt), pj & 1, abort_p);
+                        if (!ok) break;
+                        tc_fence_after();
                         const unsigned qb = sbase + kOffQ + (unsigned)(t * kQTile);
 #pragma unroll
                         for (int kk = 0; kk < 8; kk++)
-                            umma_ss(tS(t), sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
+                            umma_ss(tS, sw128_desc(qb + (kk >> 2) * kHalfQ + (kk & 3) * 32),
                                     sw128_desc(kb + (kk >> 2) * kHalfKV + (kk & 3) * 32), idS, kk > 0);
+                        umma_commit(bar(kBarSFull + t));
+                        pt = t;
+                        pj = j;
                     }
-                    umma_commit(bar(kBarSFull + (j & 1)));
+                    if (!ok) break;
                     umma_commit(bar(kBarKEmpty + j % kStagesK));
                     n_s++;
-                };
-                bool ok = mbar_wait(bar(kBarQFull), 0, abort_p);
-                if (ok && n_tiles > 0) ok = mbar_wait(bar(kBarKFull), 0, abort_p);
-                if (ok && n_tiles > 0) {
-                    tc_fence_after();
-                    issue_s(0);
-                }
-                for (int j = 0; ok && j + 1 < n_tiles; j++) {
-                    // K(j+1) landed (checking drains S(j), which has to complete
-                    // before S-read(j) anyway), then S-read(j): S(j) is in the
-                    // softmax warps' registers, so the one S buffer may take S(j+1)
-                    ok = mbar_wait(bar(kBarKFull + (j + 1) % kStagesK), ((j + 1) / kStagesK) & 1, abort_p);
-                    if (ok) ok = mbar_wait(bar(kBarSRead + (j & 1)), (j >> 1) & 1, abort_p);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(j + 1);
                 }
                 // every S MMA has completed once the final barrier fires;
                 // the K-empty signals of the last stages, which nobody waits
@@ -914,26 +910,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 bool ok = true;
                 int n_pv = 0;                            // PV stages issued
                 for (int j = 0; ok && j < n_tiles; j++) {
-                    const int b = j & 1, sv = j % kStagesV;
-                    // READY(j): P(j) stored and V(j) landed
-                    ok = mbar_wait(bar(kBarReady + b), (j >> 1) & 1, abort_p);
+                    const int sv = j % kStagesV;
+                    // READY(j): P(j) of every tile stored and V(j) landed
+                    ok = mbar_wait(bar(kBarReady), j & 1, abort_p);
                     if (!ok) break;
                     tc_fence_after();
                     const unsigned vb = vstage(sv);
                     for (int t = 0; t < n_act; t++) {
                         // A = P(j) from TMEM: 16 keys = 8 columns of fp16 pairs per MMA
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++)
-                            umma_ts(tO(t), tP(t, b) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
+                        for (int kk = 0; kk < kKeysTC / 16; kk++)
+                            umma_ts(tO(t), tP(t) + kk * 8, sw128_desc(vb + kk * 2048, kHalfKV), idO,
                                     (j > 0 || kk > 0));
                     }
-                    umma_commit(bar(kBarODone + b));
+                    umma_commit(bar(kBarODone));
                     umma_commit(bar(kBarVEmpty + sv));    // V stage sv free for the producer
                     n_pv++;
                 }
                 umma_commit(bar(kBarFin));
                 mbar_drain(bar(kBarFin), 0);
-                for (int b = 0; b < 2 && b < n_pv; b++) mbar_drain(bar(kBarODone + b), ((n_pv - 1 - b) >> 1) & 1);
+                if (n_pv > 0) mbar_drain(bar(kBarODone), (n_pv - 1) & 1);
                 for (int v = 0; v < kStagesV && v < n_pv; v++)
                     mbar_drain(bar(kBarVEmpty + v), ((n_pv - 1 - v) / kStagesV) & 1);
             }
@@ -953,12 +949,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 mbar_inval(bar(kBarVFull + s));
                 mbar_inval(bar(kBarVEmpty + s));
             }
-            for (int i = 0; i < 2; i++) {
-                mbar_inval(bar(kBarSFull + i));
-                mbar_inval(bar(kBarReady + i));
-                mbar_inval(bar(kBarODone + i));
-                mbar_inval(bar(kBarSRead + i));
+            for (int t = 0; t < 2; t++) {
+                mbar_inval(bar(kBarSFull + t));
+                mbar_inval(bar(kBarSRead + t));
             }
+            mbar_inval(bar(kBarReady));
+            mbar_inval(bar(kBarODone));
             mbar_inval(bar(kBarQFull));
             mbar_inval(bar(kBarFin));
         }
