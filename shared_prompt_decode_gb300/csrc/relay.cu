@@ -54,7 +54,7 @@ cudaError_t prepare_one(int *occ)
 // inside the streaming kernel, where it is memory-bound and overlaps context.
 constexpr int kTcMinRows = 256;
 constexpr int kTcCtxMinRows = 64;      // rows of a request per KV head (Lq G) for its context on tcgen05
-constexpr int kTcYieldPct = 20;        // most SMs that stream decode contexts beside the tensor cores, %
+constexpr int kTcYieldPct = 24;        // most SMs that stream decode contexts beside the tensor cores, %
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -101,6 +101,17 @@ relay_status_t device_info(const DevInfo **out)
             cudaGetLastError();
             return RELAY_ERR_CUDA;
         }
+        // the tensor-core kernel's warpgroups re-split the registers it is
+        // launched with: never launch it with fewer than the split needs (the
+        // raising warpgroups would wait for registers that never come)
+        cudaFuncAttributes fa0{}, fa1{};
+        if (cudaFuncGetAttributes(&fa0, tc::sys_tc_kernel<false>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa1, tc::sys_tc_kernel<true>) != cudaSuccess) {
+            cudaGetLastError();
+            return RELAY_ERR_CUDA;
+        }
+        if (fa0.numRegs * tc::kThreadsTC < tc::kRegSplit || fa1.numRegs * tc::kThreadsTC < tc::kRegSplit)
+            return RELAY_ERR_CUDA;
         d.ready = true;
     }
     *out = &d;

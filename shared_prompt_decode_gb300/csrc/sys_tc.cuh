@@ -12,30 +12,37 @@
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile; row t of a tile
 //                   lives in TMEM lane t and is owned by thread t, so the
 //                   online softmax needs no cross-thread reduction
-//   warp 8          streams 64-key K and V stages in with TMA (128-byte
+//   warp 8          streams 128-key K and V stages in with TMA (128-byte
 //                   swizzle, zero fill past the end of the keys), K and V on
-//                   4-stage rings of their own
+//                   2-stage rings of their own (32 KB stages)
 //   warp 9          owns TMEM and issues the S MMAs from one thread
 //   warp 10         issues the PV MMAs from one thread
-// Per 64-key stage j and query tile:
-//   S = Q K^T        tcgen05.mma kind::f16, M=128 N=64, Q and K K-major in
-//                    shared memory, fp32 into the tile's TMEM S buffer
-//   P = exp2(S - m)  by the tile's warpgroup, as fp16 pairs into TMEM P
-//                    buffer j % 2 (tcgen05.st)
+//   warp 11         completes the third warpgroup (the register split below
+//                   is per warpgroup)
+// In the decode step the softmax warpgroups raise their registers to 224 for
+// an item and the others lower theirs to 56 (setmaxnreg): a thread holds a
+// whole 128-key stage of its row.
+// Per 128-key stage j and query tile t:
+//   S = Q K^T        tcgen05.mma kind::f16, M=128 N=128, Q and K K-major in
+//                    shared memory, fp32 into the one TMEM S buffer, which the
+//                    two tiles take in turn: S_0(j), S_1(j), S_0(j+1), ...
+//   P = exp2(S - m)  by the tile's warpgroup, as fp16 pairs into the tile's
+//                    TMEM P buffer (tcgen05.st)
 //   O += P V         tcgen05.mma, M=128 N=128: P from TMEM, V from shared
 //                    memory in its natural [key][d] order (MN-major), never
 //                    transposed
-// The S thread issues S(j+1) once K(j+1) has landed and on S-read(j), raised
-// by the warpgroups as soon as S(j) is in their registers, so S(j+1) runs
-// while they compute P(j); the PV thread issues PV(j) on READY(j),
-// raised once P(j) is in TMEM and V(j) has landed; P(j+2) waits for PV(j)
+// The S thread issues S_t(j) once K(j) has landed and on S-read of the S the
+// buffer held before (raised by that tile's warpgroup as soon as its S is in
+// registers), so the other tile's S runs while a warpgroup computes its P;
+// the PV thread issues PV(j) of both tiles on READY(j), raised once P(j) is in
+// TMEM and V(j) has landed; P(j+1) and a rescale of O wait for PV(j)
 // (O-done(j)).  A thread that has MMAs in flight waits for them to drain
 // before its next shared-memory read completes, so every barrier check on
 // an issuing thread empties the tensor pipe: the PV thread checks one barrier
-// per stage; the S thread's K check empties the pipe of S(j), which S-read(j)
-// waits for anyway; the two threads' checks overlap each other's MMAs.
-// Each barrier signalled per stage has one instance per buffer or ring slot,
-// so that no parity wait can be two phases behind.  O is rescaled only when a
+// per stage; the S thread's checks wait for an S that has to complete before
+// its warpgroup reads it anyway; the two threads' checks overlap each other's
+// MMAs.  No barrier can complete twice before its waiter has seen the first
+// completion, so parity waits are never a phase behind.  O is rescaled only when a
 // row's running maximum grows by more than 2^8 (P <= 256 otherwise, well
 // inside fp16).  Every wait is bounded in time; a wait that gives up raises
 // RELAY_FLAG_WAIT_TIMEOUT and the CTA drains its copies and MMAs before it
@@ -58,8 +65,15 @@ constexpr int kPageTC = 16;           // tokens per page of the paged pool
 constexpr int kMaxPagesTC = 1024;     // pages of a request's context on the paged path (16384 tokens)
 constexpr int kMaxBatchTC = 512;      // requests of a batch
 constexpr int kStagesK = 2, kStagesV = 2;   // K stage j is freed when S(j) completes, V stage j when PV(j) does
-constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;
-constexpr int kThreadsTC = 352;
+constexpr int kWarpLoad = 8, kWarpMmaS = 9, kWarpMmaPV = 10;   // warp 11 only completes the third warpgroup
+constexpr int kThreadsTC = 384;
+// Registers per thread after the split (setmaxnreg, per warpgroup): the
+// softmax warpgroups hold a 128-key stage of S, the others need few.  The
+// split draws on the block's launch allotment, threads x registers at launch
+// (168 for 384 threads); the host checks that before the first launch.
+constexpr int kRegSoftmax = 224, kRegRoles = 56, kRegLaunch = 168;
+constexpr int kRegSplit = 256 * kRegSoftmax + 128 * kRegRoles;
+static_assert(kRegSplit <= kThreadsTC * kRegLaunch, "register split above the launch allotment");
 // A protocol wait gives up after RELAY_WAIT_LIMIT_NS (1 s).  A test build
 // sets it to 0, so that the first wait not met at once gives up and the
 // abort path below runs; draining copies and MMAs in flight before TMEM is
@@ -335,7 +349,7 @@ struct TcParams {
     unsigned *queue;                 // decode step: [0] items taken, [1] CTAs done; zero before the launch and after
     int n_yield;                     // at most this many SMs stream decode contexts beside the tensor cores
     int sms;                         // SMs of the GPU
-    float sys_stages;                // 64-key stages of all system items
+    float sys_stages;                // K/V stages of all system items
 };
 
 // tile pairs for Mv virtual rows
@@ -359,7 +373,7 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 //     Items that stream the same keys (one KV head, one key range) are
 //     adjacent, so CTAs that run at the same time share them through L2.
 //     tmK / tmV view sys_k / sys_v as [Ls][Hkv][128] fp16 with a {64 d, 1
-//     head, 64 keys} box and 128-byte swizzle.
+//     head, 128 keys} box and 128-byte swizzle.
 //   context items (decode step, after every system item), item - n_sys =
 //     c * Hkv + hk: the rows of one request b with several query rows
 //     (q_lens[b] > 1) against the request's own context, one pair of its
@@ -368,7 +382,7 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 //     keys below max(0, ctx_lens[b] - q_lens[b] + 1 + i): the chunk's own
 //     keys are in the context already, causally.  tmKc / tmVc view k_cache /
 //     v_cache as [num_blocks][Hkv][16][128] fp16 with a {64 d, 16 tokens, 1,
-//     1} box: a 64-key stage is four page boxes per d-half, page ids from
+//     1} box: a 128-key stage is eight page boxes per d-half, page ids from
 //     block_tables staged in shared memory; a page past the context reads
 //     page id num_blocks, out of range, so the copy fills it with zeros.
 //   PREFILL: causal self-attention of the system prompt itself (its Ls query
@@ -389,8 +403,8 @@ __device__ __forceinline__ int owner_of(const int *qo, int n, int x)
 // tensor cores of the others run; it takes the remaining SMs as this grid's
 // CTAs leave.  As many SMs stream (counting those this grid leaves free
 // anyway) as the decode bytes need to finish within the tensor-core phase,
-// at most n_yield, from two rates measured on GB300: a 64-key stage of a
-// tile pair takes about 1.04 us, and a streaming CTA beside the tensor
+// at most n_yield, from two rates measured on GB300: a stage of a tile pair
+// takes about kStageUs, and a streaming CTA beside the tensor
 // cores moves about 76 GB/s.  Every CTA computes the same count.
 template <bool PREFILL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -600,6 +614,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         __syncthreads();
         bool pref_next = false;   // this thread has loaded its Q row of the next item
+        // each role's registers for the item (back to the launch count at its
+        // end); prefill's items are short, and it measured faster without
+        if (!PREFILL) {
+            if (warp < 8)
+                asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegSoftmax));
+            else
+                asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegRoles));
+        }
         if (warp < 8) {
             // ------------------------------------------------------------ softmax warpgroups
             const int wg = warp >> 2;
@@ -903,7 +925,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 for (int s = 0; s < kStagesK && s < n_s; s++)
                     mbar_drain(bar(kBarKEmpty + s), ((n_s - 1 - s) / kStagesK) & 1);
             }
-        } else {
+        } else if (warp == kWarpMmaPV) {
             // ------------------------------------------------------------ O += P V
             if (lane == 0) {
                 const uint32_t idO = idesc_f16(kRowsTC, 128, true);
@@ -935,6 +957,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
         }
 
+        if (!PREFILL) {
+            if (warp < 8)
+                asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegLaunch));
+            else
+                asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegLaunch));
+        }
         // every role is done with the item, and every barrier phase it started
         // has completed: the barriers may be set up again for the next item
         tc_fence_before();
