@@ -325,9 +325,10 @@ def test_device_checks_flag_bad_values(what):
 
 # ----------------------------------------------------------------------------- tensor-core system step
 # Batches with more than 256 query rows per head run the system step on the
-# tcgen05 kernel (pairs of 128-row tiles, 64-key stages, S issued two stages
-# ahead of PV); ragged rows and keys on purpose, and ranges of 1, 2 and 3
-# stages, which take the pipeline's prologue-only and shortest-loop paths.
+# tcgen05 kernel (pairs of 128-row tiles, 128-key stages, one S buffer that
+# the two tiles take in turn); ragged rows and keys on purpose, a lone tile
+# beside a pair (257 rows), and ranges of 1 and 2 stages, which take the
+# pipeline's prologue-only and shortest-loop paths.
 TC_CASES = [
     ("rows257_keys1000", 257, 1, 1000, None),
     ("rows300_keys64", 300, 1, 64, None),
@@ -359,7 +360,7 @@ def test_tensor_core_system_step(name, B, Lq, Ls, ql):
 # ----------------------------------------------------------------------------- chunk rows' own contexts on tcgen05
 # Requests of Lq * G >= 64 virtual rows per KV head take their own context on
 # the tensor-core kernel, in the grid of the system step: paged copies (four
-# 16-token page boxes per 64-key stage), a causal limit per row, and the V
+# 16-token page boxes per 128-key stage), a causal limit per row, and the V
 # slots past the context zeroed (the pool's unused slots hold NaN).  Long and
 # ragged contexts, two tile pairs of one request (300 rows), contexts shorter
 # than the chunk (rows that see no context key), one-row and empty requests
