@@ -162,7 +162,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // sys_k or sys_v, [Ls][H][128] fp16, as a 3-D tensor (d, head, key) read in
-// {64, 1, 64} boxes with 128-byte swizzle; keys past Ls read as zero.
+// {64, 1, 128} boxes with 128-byte swizzle; keys past Ls read as zero.
 bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -173,6 +173,23 @@ bool encode_sys_map(CUtensorMap *m, const void *base, int H, int Ls)
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Prefill output, [Ls][H][128] fp16, as a 3-D tensor (d, head, position)
+// written in {64, G, 128 / G} boxes with 128-byte swizzle: one d-half of a
+// 128-row tile of virtual rows (position t, head hk G + c: row t G + c), the
+// box's rows in that order; rows past Ls are not written.
+bool encode_out_map(CUtensorMap *m, void *base, int H, int Ls, int G)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || G < 1 || tc::kRowsTC % G) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)Ls};
+    const cuuint64_t strides[2] = {128 * sizeof(__half), (cuuint64_t)H * 128 * sizeof(__half)};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(tc::kRowsTC / G)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -910,9 +927,13 @@ relay_status_t relay_sys_prefill(const relay_dims_t *dims, const void *q_sys, co
     CUtensorMap tmK, tmV;
     if (!encode_sys_map(&tmK, sys_k, t.Hkv, dims->Ls) || !encode_sys_map(&tmV, sys_v, t.Hkv, dims->Ls))
         return RELAY_ERR_CUDA;
+    // the output tile goes out through a TMA store where a group's heads fit
+    // a tile evenly (else each thread stores its own row)
+    CUtensorMap tmO = tmK;
+    t.out_tma = (tc::kRowsTC % t.G == 0 && encode_out_map(&tmO, out, dims->H, dims->Ls, t.G)) ? 1 : 0;
     const long long grid = std::min<long long>((long long)t.pairs * t.Hkv, dev->sms);
     tc::sys_tc_kernel<true><<<(unsigned)grid, tc::kThreadsTC, tc::kSmemTC, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tmK, tmV, tmK, tmV, t);
+        tmK, tmV, tmO, tmV, t);
     return cudaGetLastError() == cudaSuccess ? RELAY_OK : RELAY_ERR_CUDA;
 }
 

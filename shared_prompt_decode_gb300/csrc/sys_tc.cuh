@@ -48,7 +48,8 @@
 // RELAY_FLAG_WAIT_TIMEOUT and the CTA drains its copies and MMAs before it
 // frees TMEM and leaves.  Each row's result is one fp32 partial (normalised
 // output and log2-sum-exp), merged later with the context partials, or
-// (prefill) the final fp16 row and its log-sum-exp.
+// (prefill) the final fp16 row and its log-sum-exp; prefill's fp16 tiles go
+// out through TMA stores from a swizzled shared-memory tile.
 #pragma once
 
 #include <cuda.h>
@@ -204,6 +205,15 @@ __device__ __forceinline__ void tma_load_4d(unsigned dst, const CUtensorMap *tm,
                  : "memory");
 }
 
+// TMA: one box of shared memory into a 3-D tensor map at (x, y, z); elements
+// outside the tensor are not written (bulk async-group of the issuing thread).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, unsigned src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -350,6 +360,7 @@ struct TcParams {
     int n_yield;                     // at most this many SMs stream decode contexts beside the tensor cores
     int sms;                         // SMs of the GPU
     float sys_stages;                // K/V stages of all system items
+    int out_tma;                     // prefill: the output tiles go out through tmKc (a map of out), else per row
 };
 
 // tile pairs for Mv virtual rows
@@ -776,8 +787,50 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                   : ctx     ? (size_t)p.mq_base + (size_t)r * p.H + h
                                             : ((size_t)rho * p.max_q_total + r) * p.H + h;
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                if (PREFILL && p.out_tma) {
+                    // The tile's fp16 rows into its warpgroup's K stage (free:
+                    // every MMA of the item has completed), in the 128-byte-
+                    // swizzled layout of the output map's box, then two TMA
+                    // stores (one per d-half) by one thread; rows past Ls are
+                    // not written.  The stage must be read out before the next
+                    // item's K copies: the storing thread waits for that before
+                    // the item ends.
+                    unsigned char *so = gbase + kOffK + wg * kStageBytes;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) {
+                    for (int q4 = 0; q4 < 4; q4++) {
+                        unsigned o[32];
+                        if (fin && n_tiles > 0) {
+                            tmem_ld32(tO(wg) + lane_off + q4 * 32, o);   // warp-collective
+                            tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i++) o[i] = 0u;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            const int c = (q4 & 1) * 4 + k;               // 16-byte chunk within the d-half
+                            const float *f = reinterpret_cast<const float *>(o) + 8 * k;
+                            *reinterpret_cast<uint4 *>(so + (q4 >> 1) * kHalfKV + sw_off(row, c)) =
+                                make_uint4(pack_half2(f[0] * inv, f[1] * inv), pack_half2(f[2] * inv, f[3] * inv),
+                                           pack_half2(f[4] * inv, f[5] * inv), pack_half2(f[6] * inv, f[7] * inv));
+                        }
+                    }
+                    fence_async_smem();
+                    if (wg == 0)
+                        asm volatile("bar.sync 2, 128;\n" ::: "memory");
+                    else
+                        asm volatile("bar.sync 3, 128;\n" ::: "memory");
+                    if (row == 0) {
+                        const int v0 = (2 * pair + wg) * kRowsTC;
+                        const unsigned src = sbase + kOffK + (unsigned)(wg * kStageBytes);
+                        tma_store_3d(&tmKc, src, 0, hk * p.G, v0 / p.G);
+                        tma_store_3d(&tmKc, src + kHalfKV, 64, hk * p.G, v0 / p.G);
+                        asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+                        asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+                    }
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4 && !(PREFILL && p.out_tma); q4++) {
                     unsigned o[32];
                     if (fin && n_tiles > 0) {
                         tmem_ld32(tO(wg) + lane_off + q4 * 32, o);   // warp-collective
@@ -994,6 +1047,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
     // query rows prefetched for an item that did not run (after a wait gave up)
     asm volatile("cp.async.wait_all;\n" ::: "memory");
+    // prefill output tiles stored through TMA by this thread have been written
+    if (PREFILL && p.out_tma && (tid == 0 || tid == kRowsTC)) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) atomicOr(p.flags, RELAY_FLAG_WAIT_TIMEOUT);
